@@ -1,0 +1,162 @@
+"""fp64 CPU oracle for the selective state-space scan (S6).
+
+TEST INFRASTRUCTURE ONLY.  The test suite, the package smoke check and the
+benchmark's CPU-baseline leg are the only callers.  The CUDA library never
+imports, links or runs anything here, and nothing here imports the CUDA
+library: the two share only the seeded input generator, which holds none of
+the method's arithmetic.
+
+The arithmetic lives in ``ssm_oracle.c`` (plain C, fp64, libm ``exp`` and
+``log1p``), compiled on first use into ``liboracle.so`` next to this file.
+This module only marshals numpy arrays into fp64 buffers for it.
+
+Definitions followed (see the header of ``ssm_oracle.c`` for the passages):
+the recurrence h_t = exp(Delta_t A) * h_{t-1} + Delta_t B_t x_t, the readout
+y_t = C_t . h_t + D x_t, the gate silu(z_t), and Delta = softplus(raw + bias).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against
+identities and closed forms that are independent of this code.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` with gcc (fp64, no fast-math, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
+               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def build_variant(out_path: str, source_text: str) -> str:
+    """Compile an edited copy of the oracle source (used by the mutation
+    tests, which plant a mistake in a copy to show the pins catch it)."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(source_text)
+    subprocess.run(["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
+                    "-fPIC", "-shared", "-o", out_path, src, "-lm"], check=True)
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def _bind(lib):
+    lib.oracle_scan_fwd.restype = ctypes.c_int
+    lib.oracle_scan_fwd.argtypes = [ctypes.c_int64] * 4 + [_dp] * 8 + [ctypes.c_int, _dp, _dp, _dp,
+                                                                       ctypes.c_int]
+    lib.oracle_state_update.restype = ctypes.c_int
+    lib.oracle_state_update.argtypes = [ctypes.c_int64] * 3 + [_dp] * 9 + [ctypes.c_int, _dp]
+    lib.oracle_softplus_scalar.restype = ctypes.c_double
+    lib.oracle_softplus_scalar.argtypes = [ctypes.c_double]
+    lib.oracle_silu_scalar.restype = ctypes.c_double
+    lib.oracle_silu_scalar.argtypes = [ctypes.c_double]
+    return lib
+
+
+def load(path: str | None = None):
+    """Load (building if needed) the oracle library; ``path`` selects a variant."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _f64(a, shape=None):
+    if a is None:
+        return None
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    if shape is not None and arr.shape != tuple(shape):
+        raise ValueError(f"expected shape {tuple(shape)}, got {arr.shape}")
+    return arr
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_dp)
+
+
+def scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+             initial_state=None, nthreads=0, lib=None):
+    """Selective scan forward in fp64.
+
+    x, delta, z: (batch, seqlen, dim); B, C: (batch, seqlen, dstate);
+    A: (dim, dstate); D, delta_bias: (dim,); initial_state: (batch, dim, dstate).
+    Returns ``(out, last_state)``, fp64 arrays of shapes (batch, seqlen, dim) and
+    (batch, dim, dstate).
+    """
+    x = _f64(x)
+    bsz, seqlen, dim = x.shape
+    A = _f64(A)
+    dstate = A.shape[1]
+    delta = _f64(delta, x.shape)
+    B = _f64(B, (bsz, seqlen, dstate))
+    C = _f64(C, (bsz, seqlen, dstate))
+    D = _f64(D, (dim,))
+    z = _f64(z, x.shape)
+    delta_bias = _f64(delta_bias, (dim,))
+    initial_state = _f64(initial_state, (bsz, dim, dstate))
+    out = np.empty((bsz, seqlen, dim), dtype=np.float64)
+    last = np.empty((bsz, dim, dstate), dtype=np.float64)
+    rc = (lib or load()).oracle_scan_fwd(bsz, seqlen, dim, dstate, _ptr(x), _ptr(delta), _ptr(A),
+                                         _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+                                         int(bool(delta_softplus)), _ptr(initial_state), _ptr(out),
+                                         _ptr(last), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_scan_fwd rejected its arguments")
+    return out, last
+
+
+def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
+                 lib=None):
+    """One decode step in fp64.  ``state`` (batch, dim, dstate) is not modified;
+    the updated state is returned with the output: ``(out, new_state)``."""
+    st = np.array(state, dtype=np.float64, copy=True, order="C")
+    bsz, dim, dstate = st.shape
+    x = _f64(x, (bsz, dim))
+    delta = _f64(delta, (bsz, dim))
+    A = _f64(A, (dim, dstate))
+    B = _f64(B, (bsz, dstate))
+    C = _f64(C, (bsz, dstate))
+    D = _f64(D, (dim,))
+    z = _f64(z, (bsz, dim))
+    delta_bias = _f64(delta_bias, (dim,))
+    out = np.empty((bsz, dim), dtype=np.float64)
+    rc = (lib or load()).oracle_state_update(bsz, dim, dstate, _ptr(st), _ptr(x), _ptr(delta),
+                                             _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                             _ptr(delta_bias), int(bool(delta_softplus)),
+                                             _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_state_update rejected its arguments")
+    return out, st
+
+
+def softplus(u: float, lib=None) -> float:
+    return (lib or load()).oracle_softplus_scalar(float(u))
+
+
+def silu(v: float, lib=None) -> float:
+    return (lib or load()).oracle_silu_scalar(float(v))

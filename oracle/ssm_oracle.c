@@ -1,0 +1,153 @@
+/*
+ * ssm_oracle.c -- fp64 CPU oracle for the selective state-space scan (S6).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this file's library.  The product path
+ * (the CUDA library) never links, loads or calls it, and this file shares no
+ * code, header, table or constant with it.
+ *
+ * What it computes, and where the definition comes from
+ * (page titles as they appear in the source pages):
+ *
+ *   - State-space model, discrete form: the state equation
+ *     h(t+1) = A h(t) + B x(t) and the observation y(t) = C h(t)
+ *     ("Mamba: Linear-Time Sequence Modeling with Selective State Spaces",
+ *     dhy1.tistory.com, section "0. State Space Models").  The time index is
+ *     read so that the current token enters its own output:
+ *     h_t = dA_t * h_{t-1} + dBx_t,  y_t = C_t . h_t.
+ *   - Selection: Delta, B and C are given per token (per (batch, time)),
+ *     B and C shared by all channels ("Mamba的三大创新" page,
+ *     weblog-19d.pages.dev, section on S4 -> S6 and the gating roles of
+ *     Delta, B, C).
+ *   - Discretisation, stage 1 of that page (zero-order hold): the decay is
+ *     dA = exp(Delta * A) exactly; the input term is taken in its first-order
+ *     (Euler) form dBx = Delta * B * x.
+ *   - Recurrent mode, stage 2 of that page: the linear recurrence evaluated
+ *     with a plain loop over time.
+ *   - Delta = softplus(delta_raw + bias), the skip term D * x added before the
+ *     output gate, and the gate silu(z) = z / (1 + exp(-z)).
+ *
+ * Arithmetic is IEEE fp64 throughout, with libm exp/log1p, and no reordering
+ * beyond the loops written here: for each (batch, channel) pair, time runs
+ * forward, and for each time step the state index runs 0..dstate-1.
+ *
+ * Layouts (row-major, last index fastest):
+ *   x, delta, z, out     : (batch, seqlen, dim)
+ *   B, C                 : (batch, seqlen, dstate)
+ *   A                    : (dim, dstate)
+ *   D, delta_bias        : (dim)
+ *   initial/last state   : (batch, dim, dstate)
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* softplus(u) = log(1 + e^u), evaluated without overflow and without the
+ * cancellation of forming 1 + e^u for very negative u. */
+static double oracle_softplus(double u)
+{
+    if (u > 0.0)
+        return u + log1p(exp(-u));
+    return log1p(exp(u));
+}
+
+/* silu(v) = v * sigmoid(v) = v / (1 + e^{-v}). */
+static double oracle_silu(double v)
+{
+    return v / (1.0 + exp(-v));
+}
+
+/* Full-sequence forward scan.  Returns 0 on success, -1 on bad arguments.
+ * `nthreads` <= 0 lets OpenMP choose. */
+int oracle_scan_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                    const double *x, const double *delta, const double *A,
+                    const double *B, const double *C, const double *D,
+                    const double *z, const double *delta_bias, int delta_softplus,
+                    const double *initial_state, double *out, double *last_state,
+                    int nthreads)
+{
+    if (batch < 0 || seqlen < 0 || dim < 0 || dstate <= 0 || dstate > 4096)
+        return -1;
+    if (!x || !delta || !A || !B || !C || !out)
+        return -1;
+    const int64_t nchan = batch * dim;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t ch = 0; ch < nchan; ++ch) {
+        const int64_t b = ch / dim;
+        const int64_t d = ch % dim;
+        double h[4096];
+        for (int64_t n = 0; n < dstate; ++n)
+            h[n] = initial_state ? initial_state[(b * dim + d) * dstate + n] : 0.0;
+        for (int64_t t = 0; t < seqlen; ++t) {
+            const int64_t tok = (b * seqlen + t) * dim + d;  /* (b, t, d) */
+            const int64_t row = (b * seqlen + t) * dstate;   /* (b, t, :) */
+            const double xv = x[tok];
+            double u = delta[tok] + (delta_bias ? delta_bias[d] : 0.0);
+            const double dt = delta_softplus ? oracle_softplus(u) : u;
+            double y = 0.0;
+            for (int64_t n = 0; n < dstate; ++n) {
+                const double dA = exp(dt * A[d * dstate + n]);
+                h[n] = dA * h[n] + dt * B[row + n] * xv;
+                y += C[row + n] * h[n];
+            }
+            if (D)
+                y += D[d] * xv;
+            if (z)
+                y *= oracle_silu(z[tok]);
+            out[tok] = y;
+        }
+        if (last_state)
+            for (int64_t n = 0; n < dstate; ++n)
+                last_state[(b * dim + d) * dstate + n] = h[n];
+    }
+    return 0;
+}
+
+/* One decode step: the same recurrence for a single token per sequence,
+ * with the state read and written in place.
+ *   state            : (batch, dim, dstate), updated in place
+ *   x, delta, z, out : (batch, dim)
+ *   B, C             : (batch, dstate)
+ */
+int oracle_state_update(int64_t batch, int64_t dim, int64_t dstate, double *state,
+                        const double *x, const double *delta, const double *A,
+                        const double *B, const double *C, const double *D,
+                        const double *z, const double *delta_bias, int delta_softplus,
+                        double *out)
+{
+    if (batch < 0 || dim < 0 || dstate <= 0)
+        return -1;
+    if (!state || !x || !delta || !A || !B || !C || !out)
+        return -1;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t tok = b * dim + d;
+            double *h = state + tok * dstate;
+            double u = delta[tok] + (delta_bias ? delta_bias[d] : 0.0);
+            const double dt = delta_softplus ? oracle_softplus(u) : u;
+            double y = 0.0;
+            for (int64_t n = 0; n < dstate; ++n) {
+                const double dA = exp(dt * A[d * dstate + n]);
+                h[n] = dA * h[n] + dt * B[b * dstate + n] * x[tok];
+                y += C[b * dstate + n] * h[n];
+            }
+            if (D)
+                y += D[d] * x[tok];
+            if (z)
+                y *= oracle_silu(z[tok]);
+            out[tok] = y;
+        }
+    }
+    return 0;
+}
+
+/* Scalar helpers exposed for the pins on the nonlinearities. */
+double oracle_softplus_scalar(double u) { return oracle_softplus(u); }
+double oracle_silu_scalar(double v) { return oracle_silu(v); }

@@ -1,0 +1,237 @@
+"""Independent pins for the fp64 oracle.
+
+Each pin computes what the scan must return from something other than the
+oracle's own loop -- a closed form, a textbook special case, a library
+routine (numpy / scipy) or a hand-derived fixture -- and raises
+AssertionError when the oracle (``lib``: the library under test, which may be
+a deliberately broken copy) disagrees.  Chosen so that a dropped term, a
+wrong sign, a lagged time index, transposed B/C, a missing softplus/bias or a
+gate applied before the skip each fail at least one pin.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+from scipy.special import expit
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def softplus_ref(u):
+    return np.logaddexp(0.0, u)          # numpy's log(e^0 + e^u)
+
+
+def silu_ref(v):
+    return v * expit(v)                  # scipy's logistic sigmoid
+
+
+def rand_problem(seed, bsz=2, L=12, dim=3, N=4, init=True, lti=False):
+    r = np.random.default_rng(seed)
+    x = r.standard_normal((bsz, L, dim))
+    z = r.standard_normal((bsz, L, dim))
+    dl = r.standard_normal((bsz, L, dim))
+    bias = np.log(np.expm1(r.uniform(0.05, 0.5, dim)))
+    B = r.standard_normal((bsz, L, N))
+    C = r.standard_normal((bsz, L, N))
+    A = -np.exp(r.uniform(-1.0, 1.5, (dim, N)))
+    D = r.standard_normal(dim)
+    h0 = r.standard_normal((bsz, dim, N)) if init else None
+    if lti:
+        dl[:] = dl[:, :1, :]
+        B[:] = B[:, :1, :]
+        C[:] = C[:, :1, :]
+    return dict(x=x, delta=dl, z=z, A=A, B=B, C=C, D=D, delta_bias=bias, initial_state=h0)
+
+
+def _run(lib, p, **kw):
+    args = dict(p)
+    args.update(kw)
+    return oracle.scan_fwd(lib=lib, **args)
+
+
+def _rel(a, b):
+    return float(np.max(np.abs(a - b) / (1.0 + np.abs(b))))
+
+
+# P1 -- brute-force closed form y_t = sum_{s<=t} C_t . (prod_{r=s+1..t} dA_r) dBx_s
+#       (+ the decayed initial state), skip, gate; O(L^2 N) with explicit products.
+def pin_closed_form(lib):
+    p = rand_problem(1)
+    out, last = _run(lib, p)
+    x, z, dl, A, B, C, D = (p[k] for k in ("x", "z", "delta", "A", "B", "C", "D"))
+    dt = softplus_ref(dl + p["delta_bias"])
+    bsz, L, dim = x.shape
+    N = A.shape[1]
+    ref = np.zeros_like(out)
+    last_ref = np.zeros_like(last)
+    for b in range(bsz):
+        for d in range(dim):
+            for t in range(L):
+                hs = np.zeros(N)
+                prod0 = np.ones(N)
+                for r in range(t + 1):
+                    prod0 = prod0 * np.exp(dt[b, r, d] * A[d])
+                hs += prod0 * p["initial_state"][b, d]
+                for s in range(t + 1):
+                    prod = np.ones(N)
+                    for r in range(s + 1, t + 1):
+                        prod = prod * np.exp(dt[b, r, d] * A[d])
+                    hs += prod * dt[b, s, d] * B[b, s] * x[b, s, d]
+                ref[b, t, d] = (np.dot(C[b, t], hs) + D[d] * x[b, t, d]) * silu_ref(z[b, t, d])
+                if t == L - 1:
+                    last_ref[b, d] = hs
+    assert _rel(out, ref) < 1e-12, _rel(out, ref)
+    assert _rel(last, last_ref) < 1e-12
+
+
+# P2 -- prefix-sum form: prod_{r=s+1..t} exp(Delta_r A) = exp(A * (S_t - S_s)),
+#       S the running sum of Delta (A does not depend on time).
+def pin_prefix_sum(lib):
+    p = rand_problem(2, bsz=1, L=16, dim=2, N=3, init=False)
+    out, _ = _run(lib, p, z=None, D=None)
+    dt = softplus_ref(p["delta"] + p["delta_bias"])
+    S = np.cumsum(dt, axis=1)
+    ref = np.zeros_like(out)
+    for d in range(2):
+        for t in range(16):
+            acc = 0.0
+            for s in range(t + 1):
+                w = np.exp(p["A"][d] * (S[0, t, d] - S[0, s, d]))
+                acc += np.dot(p["C"][0, t], w * p["B"][0, s]) * dt[0, s, d] * p["x"][0, s, d]
+            ref[0, t, d] = acc
+    assert _rel(out, ref) < 1e-12, _rel(out, ref)
+
+
+# P3 -- LTI special case = global convolution mode: with Delta, B, C constant in
+#       time, y = K * x + D x with K_k = sum_n C_n exp(k Delta A_n) Delta B_n.
+def pin_lti_convolution(lib):
+    p = rand_problem(3, bsz=1, L=20, dim=2, N=4, init=False, lti=True)
+    out, _ = _run(lib, p, z=None)
+    dt = softplus_ref(p["delta"][0, 0] + p["delta_bias"])        # (dim,)
+    ref = np.zeros_like(out)
+    for d in range(2):
+        K = np.array([np.sum(p["C"][0, 0] * np.exp(k * dt[d] * p["A"][d]) * dt[d] * p["B"][0, 0])
+                      for k in range(20)])
+        conv = np.convolve(p["x"][0, :, d], K)[:20]               # numpy's direct convolution
+        ref[0, :, d] = conv + p["D"][d] * p["x"][0, :, d]
+    assert _rel(out, ref) < 1e-12, _rel(out, ref)
+
+
+# P4 -- Delta -> 0 ("small Delta keeps the state and ignores the input"):
+#       softplus(-1e4) underflows to exactly 0, so dA = 1, dBx = 0 and
+#       y_t = (C_t . h_0 + D x_t) silu(z_t), the state unchanged.
+def pin_small_delta(lib):
+    p = rand_problem(4, bsz=2, L=7, dim=3, N=4, init=True)
+    p["delta"] = np.full_like(p["delta"], -1e4)
+    out, last = _run(lib, p)
+    ref = (np.einsum("bln,bdn->bld", p["C"], p["initial_state"]) + p["D"] * p["x"]) * silu_ref(p["z"])
+    assert np.array_equal(last, p["initial_state"])
+    assert _rel(out, ref) < 1e-14, _rel(out, ref)
+
+
+# P5 -- large Delta ("large Delta resets the state, focuses on the current input"):
+#       dA ~ e^{-60|A|} ~ 0, so h_t = Delta_t B_t x_t and
+#       y_t = (Delta_t x_t (C_t . B_t) + D x_t) silu(z_t).
+def pin_large_delta(lib):
+    p = rand_problem(5, bsz=1, L=9, dim=3, N=4, init=True)
+    p["A"] = -1.0 - np.abs(p["A"])
+    p["delta"] = np.full_like(p["delta"], 60.0)
+    p["delta_bias"] = np.zeros(3)
+    out, last = _run(lib, p)
+    dt = softplus_ref(60.0)
+    cb = np.sum(p["C"] * p["B"], axis=-1)[:, :, None]
+    ref = (dt * p["x"] * cb + p["D"] * p["x"]) * silu_ref(p["z"])
+    assert _rel(out, ref) < 1e-12, _rel(out, ref)
+    assert _rel(last[0], dt * p["x"][0, -1][:, None] * p["B"][0, -1][None, :]) < 1e-12
+
+
+# P6 -- split + carry: [0, L1) then [L1, L) from the first part's last state
+#       equals the unsplit run (bit for bit: same operations in the same order).
+def pin_split_carry(lib):
+    p = rand_problem(6, bsz=2, L=15, dim=3, N=4, init=True)
+    out, last = _run(lib, p)
+    L1 = 6
+    cut = lambda a, sl: None if a is None else a[:, sl]
+    first = {k: (cut(v, slice(0, L1)) if k in ("x", "delta", "z", "B", "C") else v) for k, v in p.items()}
+    o1, l1 = _run(lib, first)
+    second = {k: (cut(v, slice(L1, None)) if k in ("x", "delta", "z", "B", "C") else v) for k, v in p.items()}
+    second["initial_state"] = l1
+    o2, l2 = _run(lib, second)
+    assert np.array_equal(np.concatenate([o1, o2], axis=1), out)
+    assert np.array_equal(l2, last)
+
+
+# P7 -- decode = scan: T single-token steps from h_0 equal the scan of T tokens.
+def pin_decode_equals_scan(lib):
+    p = rand_problem(7, bsz=2, L=10, dim=3, N=4, init=True)
+    out, last = _run(lib, p)
+    st = p["initial_state"]
+    for t in range(10):
+        o, st = oracle.state_update(st, p["x"][:, t], p["delta"][:, t], p["A"], p["B"][:, t],
+                                    p["C"][:, t], p["D"], p["z"][:, t], p["delta_bias"], lib=lib)
+        assert np.array_equal(o, out[:, t])
+    assert np.array_equal(st, last)
+
+
+# P8 -- N = 1 with constant decay r = e^{Delta a}, B = C = 1, x = 1: a first-order
+#       IIR filter whose response is the geometric sum y_t = Delta (1 - r^t)/(1 - r).
+def pin_first_order_iir(lib):
+    L, Dl, a = 30, 0.3, -0.7
+    r = math.exp(Dl * a)
+    ones = np.ones((1, L, 1))
+    out, last = oracle.scan_fwd(ones, np.full((1, L, 1), Dl), np.array([[a]]), ones, ones,
+                                delta_softplus=False, lib=lib)
+    ref = np.array([Dl * (1 - r ** t) / (1 - r) for t in range(1, L + 1)])
+    assert _rel(out[0, :, 0], ref) < 1e-13
+    assert abs(last[0, 0, 0] - ref[-1]) < 1e-13
+
+
+# The hand-derived fixture tests/golden/worked_example.txt.
+def _golden():
+    env = {"ln2": math.log(2.0), "ln3": math.log(3.0)}
+    rows = {}
+    with open(os.path.join(GOLDEN, "worked_example.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split(None, 1)
+            rows[key] = [[eval(tok, {}, env) for tok in grp.split()] for grp in rest.split("|")]
+    return rows
+
+
+def pin_worked_example(lib):
+    g = _golden()
+    x = np.array(g["x"][0]).reshape(1, 3, 1)
+    out, last = oracle.scan_fwd(x, np.array(g["delta"][0]).reshape(1, 3, 1),
+                                np.array(g["A"][0]).reshape(1, 2),
+                                np.array(g["B"]).reshape(1, 3, 2), np.array(g["C"]).reshape(1, 3, 2),
+                                D=np.array(g["D"][0]), z=np.array(g["z"][0]).reshape(1, 3, 1),
+                                delta_bias=np.array(g["bias"][0]), lib=lib)
+    assert _rel(out.ravel(), np.array([v[0] for v in g["y"]])) < 1e-15
+    assert _rel(last.ravel(), np.array(g["last"][0])) < 1e-15
+
+
+# Nonlinearities: softplus(0) = ln 2, softplus(u) - softplus(-u) = u, silu(ln 3)
+# = (3/4) ln 3, silu(v) - silu(-v) = v; and against numpy/scipy on a grid.
+def pin_nonlinearities(lib):
+    eps = np.finfo(np.float64).eps
+    assert abs(oracle.softplus(0.0, lib=lib) - math.log(2.0)) <= 2 * eps
+    assert abs(oracle.silu(math.log(3.0), lib=lib) - 0.75 * math.log(3.0)) <= 4 * eps
+    for u in np.linspace(-40, 40, 161):
+        sp = oracle.softplus(u, lib=lib)
+        assert abs(sp - softplus_ref(u)) <= 1e-15 * max(1.0, abs(sp)) + 1e-300
+        assert abs(sp - oracle.softplus(-u, lib=lib) - u) < 1e-13
+        sv = oracle.silu(u, lib=lib)
+        assert abs(sv - silu_ref(u)) <= 1e-15 * max(1.0, abs(sv))
+    assert oracle.softplus(-800.0, lib=lib) == 0.0
+    assert oracle.softplus(800.0, lib=lib) == 800.0
+
+
+ALL_PINS = [pin_closed_form, pin_prefix_sum, pin_lti_convolution, pin_small_delta,
+            pin_large_delta, pin_split_carry, pin_decode_equals_scan, pin_first_order_iir,
+            pin_worked_example, pin_nonlinearities]

@@ -1,0 +1,50 @@
+"""Plant one plausible mistake at a time in a copy of the oracle's C source
+(on the CPU) and check that at least one pin catches it.  Shows the pins are
+strong enough to trust the oracle as the parity reference."""
+import pytest
+
+import oracle
+import pins
+
+MUTATIONS = {
+    # readout before the update: y_t = C_t . h_{t-1} (a lagged time index)
+    "lagged_readout": (
+        "                h[n] = dA * h[n] + dt * B[row + n] * xv;\n"
+        "                y += C[row + n] * h[n];\n",
+        "                y += C[row + n] * h[n];\n"
+        "                h[n] = dA * h[n] + dt * B[row + n] * xv;\n"),
+    "sign_of_A": ("exp(dt * A[d * dstate + n]);\n                h[n] = dA * h[n] + dt * B[row",
+                  "exp(-dt * A[d * dstate + n]);\n                h[n] = dA * h[n] + dt * B[row"),
+    "B_C_transposed": ("h[n] = dA * h[n] + dt * B[row + n] * xv;\n                y += C[row + n]",
+                       "h[n] = dA * h[n] + dt * C[row + n] * xv;\n                y += B[row + n]"),
+    "dropped_skip": ("            if (D)\n                y += D[d] * xv;\n", "\n"),
+    "dropped_softplus": ("const double dt = delta_softplus ? oracle_softplus(u) : u;\n            double y = 0.0;\n            for (int64_t n = 0; n < dstate; ++n) {\n                const double dA = exp(dt * A[d * dstate + n]);\n                h[n] = dA * h[n] + dt * B[row",
+                         "const double dt = u;\n            double y = 0.0;\n            for (int64_t n = 0; n < dstate; ++n) {\n                const double dA = exp(dt * A[d * dstate + n]);\n                h[n] = dA * h[n] + dt * B[row"),
+    "dropped_bias": ("double u = delta[tok] + (delta_bias ? delta_bias[d] : 0.0);\n            const double dt = delta_softplus ? oracle_softplus(u) : u;\n            double y = 0.0;\n            for (int64_t n = 0; n < dstate; ++n) {\n                const double dA = exp(dt * A[d * dstate + n]);\n                h[n] = dA * h[n] + dt * B[row",
+                     "double u = delta[tok];\n            const double dt = delta_softplus ? oracle_softplus(u) : u;\n            double y = 0.0;\n            for (int64_t n = 0; n < dstate; ++n) {\n                const double dA = exp(dt * A[d * dstate + n]);\n                h[n] = dA * h[n] + dt * B[row"),
+    "gate_before_skip": ("            if (D)\n                y += D[d] * xv;\n            if (z)\n                y *= oracle_silu(z[tok]);\n",
+                         "            if (z)\n                y *= oracle_silu(z[tok]);\n            if (D)\n                y += D[d] * xv;\n"),
+    "decay_missing_delta": ("const double dA = exp(dt * A[d * dstate + n]);\n                h[n] = dA * h[n] + dt * B[row",
+                            "const double dA = exp(A[d * dstate + n]);\n                h[n] = dA * h[n] + dt * B[row"),
+    "input_missing_delta": ("h[n] = dA * h[n] + dt * B[row + n] * xv;", "h[n] = dA * h[n] + B[row + n] * xv;"),
+    "state_layout_swapped": ("last_state[(b * dim + d) * dstate + n] = h[n];",
+                             "last_state[(d * batch + b) * dstate + n] = h[n];"),
+    "initial_state_ignored": ("h[n] = initial_state ? initial_state[(b * dim + d) * dstate + n] : 0.0;",
+                              "h[n] = 0.0;"),
+    "silu_sign": ("return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation {name} no longer matches the oracle source"
+    lib = oracle.load(oracle.build_variant(str(tmp_path / f"lib_{name}.so"), src.replace(old, new)))
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin detects the planted mistake {name}"
