@@ -1,0 +1,470 @@
+"""Benchmark of the selective scan (S6) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one ssm_scan_fwd call over the Mamba-1.4B-shaped prefill layer
+(batch 4, seqlen 8192, dim 4096, dstate 16, bf16 I/O, fp32 state), inputs
+resident in HBM (1.08 GB per step, larger than the 126 MB L2, so no flush is
+needed).  Prints ONE JSON line (rank 0):
+
+  value        scanned elements (batch*seqlen*dim) per second, all ranks
+  roofline     HBM roofline of the scan kernel: compulsory bytes (x, delta, z,
+               B, C read; out written) / the kernel's CUDA-event time, against
+               the measured copy bandwidth of this GPU type
+  sfu          the same kernel against its exponential-unit bound (one
+               ex2 per (token, state) item; 32 per clock per SM on B300)
+  e2e          the same metric through the public API from pinned HOST
+               buffers, host->device and device->host copies inside the timing
+  cpu_baseline the fp64 oracle on the host cores, on a bounded sample
+  decode       the one-token state update (256 x 5120 x 16, 128 chained steps)
+
+With --impl reference the fp64 CPU oracle is timed instead (the reference arm),
+on a bounded sample of the same workload per step.
+
+Under torchrun (N > 1) every rank scans its own independent batch (weak
+scaling, no data-path collective); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_137_b300 import synth  # noqa: E402
+
+WORKLOAD = synth.MAMBA_1P4B
+DECODE = synth.DECODE
+METRIC = "selective-scan elements (B*L*D)/s"
+UNIT = "elements/s"
+PEAK_FALLBACK_GBS = 6400.0
+SFU_EX2_PER_CLK_PER_SM = 32        # measured: ex2.approx.f32 lane-ops per clock per SM on B300
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD.name,
+                    help="scan workload name (default: the Mamba-1.4B layer)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target wall time of the oracle sample")
+    return ap.parse_args()
+
+
+def workload_by_name(name):
+    for w in synth.SCAN_WORKLOADS:
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return PEAK_FALLBACK_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_137_b300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (the summary records their hash)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not getattr(self, "lines", None):
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- dist
+def dist_init(n):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, device):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle sample
+def oracle_sample_inputs(inp, w, nchan, b=0):
+    """fp64 copies of channels [0, nchan) of sequence b (all tokens)."""
+    import oracle  # noqa: F401  (test/baseline infrastructure only)
+    sl = slice(0, nchan)
+    f64 = lambda t: None if t is None else t.detach().to("cpu", torch.float64).numpy()
+    return dict(x=f64(inp["x"][b:b + 1, :, sl]), delta=f64(inp["delta"][b:b + 1, :, sl]),
+                A=f64(inp["A"][sl]), B=f64(inp["B"][b:b + 1]), C=f64(inp["C"][b:b + 1]),
+                D=f64(inp["D"][sl]) if inp["D"] is not None else None,
+                z=f64(inp["z"][b:b + 1, :, sl]) if inp["z"] is not None else None,
+                delta_bias=f64(inp["delta_bias"][sl]) if inp["delta_bias"] is not None else None)
+
+
+def calibrate_oracle(inp, w, target_s):
+    """Channel count whose oracle run takes about target_s seconds on all host cores."""
+    import oracle
+    cores = os.cpu_count() or 1
+    oracle.load()
+    probe = min(w.dim, max(cores, 8))
+    s = oracle_sample_inputs(inp, w, probe)
+    t = time.perf_counter()
+    oracle.scan_fwd(**s, nthreads=cores)
+    dt = max(time.perf_counter() - t, 1e-6)
+    nchan = int(min(w.dim, max(probe, probe * target_s / dt)))
+    if nchan >= cores:
+        nchan = (nchan // cores) * cores
+    return nchan, cores
+
+
+def time_oracle(inp, w, target_s):
+    """Run the oracle on a sample sized for about target_s seconds; returns
+    (elements/s, seconds, channels, cores)."""
+    import oracle
+    nchan, cores = calibrate_oracle(inp, w, target_s)
+    s = oracle_sample_inputs(inp, w, nchan)
+    t = time.perf_counter()
+    oracle.scan_fwd(**s, nthreads=cores)
+    dt = time.perf_counter() - t
+    return w.seqlen * nchan / dt, dt, nchan, cores
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 oracle as it stands, on the host cores, each
+    step a bounded sample (about 2 s) of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+    w = workload_by_name(args.workload)
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = synth.make_scan_inputs(w, device=gen_dev)
+    nchan, cores = calibrate_oracle(inp, w, 2.0)
+    s = oracle_sample_inputs(inp, w, nchan)
+    del inp
+    for _ in range(args.warmup):
+        oracle.scan_fwd(**s, nthreads=cores)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.scan_fwd(**s, nthreads=cores)
+    el = time.perf_counter() - t
+    value = w.seqlen * nchan * args.steps / el
+    sample = f"sequence 0, channels 0..{nchan - 1} of {w.dim}, all {w.seqlen} tokens, per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "dim": w.dim,
+            "dstate": w.dstate, "io": w.io, "state": "f32",
+            "l2": f"inputs {w.io_bytes() / 1e9:.2f} GB per step > 126 MB L2; no flush"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    from selective_state_space_137_b300 import binding, ops
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = workload_by_name(args.workload)
+    import dataclasses
+    wr = dataclasses.replace(w, seed=w.seed + 1000 * rank) if rank else w
+    inp = synth.make_scan_inputs(wr, device=str(dev))
+    out = torch.empty_like(inp["x"])
+    last = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device=dev)
+    desc = binding.make_desc(w.batch, w.seqlen, w.dim, w.dstate, inp["x"].dtype)
+    plan = binding.ssm_scan_plan(desc)
+    ws = torch.empty(max(plan.workspace, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        st = binding.ssm_scan_fwd(desc, inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                  inp["D"], inp["z"], inp["delta_bias"], out, last, None, ws,
+                                  ws.numel(), stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_scan_fwd")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(local) as clk:
+        time.sleep(0.25)     # let the sampler start before the timed region
+        ev[0].record(stream)
+        for i in range(args.steps):
+            step()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        time.sleep(0.15)
+    barrier(world)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms = total_ms / args.steps
+    value = world * w.tokens * args.steps / (total_ms * 1e-3)
+
+    peak, peak_kind = peaks()
+    kernel_ms = float(np.mean(per))
+    achieved = w.io_bytes() / (kernel_ms * 1e-3) / 1e9
+    clocks = clk.summary()
+    tag = "scan_fwd_" + w.name
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(tag),
+                "peak_kind": peak_kind, "algorithmic_bytes_per_launch": w.io_bytes(),
+                "kernel_ms": kernel_ms, "frac_of_8tbs": achieved / 8000.0,
+                "kernel_launches_per_step": plan.launches}
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks["sm_mhz"] if clocks else None
+    sfu = None
+    if mhz:
+        peak_items = SFU_EX2_PER_CLK_PER_SM * nsm * mhz * 1e6
+        sfu = {"bound": "sfu", "achieved_items_per_s": w.items / (kernel_ms * 1e-3),
+               "peak_items_per_s": peak_items,
+               "frac": w.items / (kernel_ms * 1e-3) / peak_items,
+               "basis": f"{SFU_EX2_PER_CLK_PER_SM} ex2/clk/SM x {nsm} SMs x median {mhz:.0f} MHz"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": config_of(w),
+            "hbm_gbs": achieved, "gpu_launches": plan.launches * args.steps,
+            "roofline": roofline, "sfu": sfu, "clocks": clocks}
+
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(args, w, inp, desc, plan, dev, world, binding)
+    if not args.no_decode:
+        line["decode"] = run_decode(args, dev, peak, peak_kind)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        val, dt, nchan, cores = time_oracle(inp, w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"sequence 0, channels 0..{nchan - 1} of {w.dim}, "
+                                          f"all {w.seqlen} tokens ({dt:.1f} s wall)"}
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    line["source_hash"] = kernel_source_hash()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, inp, desc, plan, dev, world, binding):
+    """Same metric through the public API with pinned host buffers: each step
+    copies the inputs host->device, scans, and copies out + last_state back."""
+    names = ["x", "delta", "z", "A", "B", "C", "D", "delta_bias"]
+    host = {k: inp[k].cpu().pin_memory() for k in names if inp[k] is not None}
+    dbuf = {k: torch.empty_like(inp[k]) for k in host}
+    out = torch.empty_like(inp["x"])
+    last = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device=dev)
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hlast = torch.empty(last.shape, dtype=last.dtype, pin_memory=True)
+    ws = torch.empty(max(plan.workspace, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = hout.numel() * hout.element_size() + hlast.numel() * hlast.element_size()
+
+    def step():
+        for k, t in host.items():
+            dbuf[k].copy_(t, non_blocking=True)
+        st = binding.ssm_scan_fwd(desc, dbuf["x"], dbuf["delta"], dbuf["A"], dbuf["B"], dbuf["C"],
+                                  dbuf.get("D"), dbuf.get("z"), dbuf.get("delta_bias"), out, last,
+                                  None, ws, ws.numel(), stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_scan_fwd")
+        hout.copy_(out, non_blocking=True)
+        hlast.copy_(last, non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    total = max_over_ranks(a.elapsed_time(b), world, dev)
+    return {"value": world * w.tokens * steps / (total * 1e-3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": total / steps}
+
+
+def run_decode(args, dev, peak, peak_kind):
+    """The decode step of a 256 x 5120 x 16 fp32 state, 128 chained steps:
+    warm (state stays in L2 between steps) and L2-flushed per step."""
+    from selective_state_space_137_b300 import binding
+    w = DECODE
+    inp = synth.make_decode_inputs(w, device=str(dev))
+    state = inp["state"].clone()
+    out = torch.empty((w.batch, w.dim), dtype=inp["x"].dtype, device=dev)
+    desc = binding.make_desc(w.batch, 1, w.dim, w.dstate, inp["x"].dtype)
+    stream = torch.cuda.current_stream(dev)
+
+    def one(s):
+        st = binding.ssm_state_update(desc, state, inp["x"][s], inp["delta"][s], inp["A"],
+                                      inp["B"][s], inp["C"][s], inp["D"], inp["z"][s],
+                                      inp["delta_bias"], out, stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_state_update")
+
+    for s in range(8):
+        one(s)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for s in range(w.steps):
+        one(s)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    warm_ms = a.elapsed_time(b) / w.steps
+    # L2-flushed: write 512 MB between steps, time each step alone
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    for s in range(32):
+        flush.fill_(s & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one(s)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    cold_ms = float(np.median(times))
+    by = w.step_bytes()
+    return {"workload": w.name, "steps_chained": w.steps,
+            "warm": {"ms_per_step": warm_ms, "gb_per_s": by / (warm_ms * 1e-3) / 1e9,
+                     "steps_per_s": 1e3 / warm_ms},
+            "flushed": {"ms_per_step": cold_ms, "gb_per_s": by / (cold_ms * 1e-3) / 1e9,
+                        "steps_per_s": 1e3 / cold_ms},
+            "roofline": {"bound": "hbm", "achieved": by / (cold_ms * 1e-3) / 1e9, "peak": peak,
+                         "unit": "GB/s", "frac": by / (cold_ms * 1e-3) / 1e9 / peak,
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_launch": by,
+                         "traffic": profiled_traffic("state_update_" + w.name)}}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * ssm.h -- C ABI of the B300 selective state-space scan library (libssm_b300.so).
+ *
+ * The library implements the selective state-space model "S6" of
+ * "Mamba: Linear-Time Sequence Modeling with Selective State Spaces":
+ *
+ *   Delta_t   = softplus(delta_raw_t + delta_bias)           (per token, per channel)
+ *   dA_t[n]   = exp(Delta_t * A[n])                          (zero-order-hold decay)
+ *   h_t[n]    = dA_t[n] * h_{t-1}[n] + Delta_t * B_t[n] * x_t (input term, first order)
+ *   y_t       = (sum_n C_t[n] * h_t[n] + D * x_t) * silu(z_t)
+ *
+ * Passages defining it:
+ *   - the state equation h(t+1) = A h(t) + B x(t) and the observation
+ *     y(t) = C h(t): "Mamba: Linear-Time Sequence Modeling with Selective
+ *     State Spaces" (dhy1.tistory.com), section "0. State Space Models";
+ *   - discretisation of (Delta, A, B) by zero-order hold (stage 1) and the
+ *     recurrent mode (stage 2), Delta, B and C made input-dependent, A acting
+ *     per state dimension: "Mamba的三大创新" (weblog-19d.pages.dev), sections
+ *     "S4的4个参数..." and "硬件感知的设计：并行扫描...";
+ *   - constant-time recurrent inference over a fixed-size state (the decode
+ *     step): the same page, model comparison table (RNN / SSM / Mamba rows).
+ * The time index is read so that token t enters its own output (h_t, not
+ * h_{t-1}, is read out).  The input term uses Delta*B (the first-order form of
+ * the zero-order hold), the skip D*x is added before the gate.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *     row-major with the last index fastest, and aligned to their element
+ *     size (the decode state to 16 bytes when dstate >= 4); a misaligned
+ *     pointer is rejected with SSM_ERR_INVALID_ARG.  16-byte aligned tensors
+ *     let the scan take its tiled path (see ssm_scan_plan).  The library
+ *     never allocates, frees or synchronises; work is enqueued on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream) and runs
+ *     asynchronously.  Results are valid once the stream has reached them.
+ *   - "io" tensors (x, delta, z, B, C, out) have the dtype `io_dtype`
+ *     (fp32 or bf16).  A, D, delta_bias and the states are always fp32, and
+ *     the recurrence is always carried in fp32.
+ *   - Optional pointers may be NULL: z (no gate), D (no skip), delta_bias
+ *     (zero bias), initial_state (zero state), last_state (not written).
+ *   - Errors: nothing is enqueued when a call returns other than SSM_OK for an
+ *     argument check.  SSM_ERR_CUDA reports a failed launch (the CUDA error is
+ *     then available from cudaGetLastError in the caller's runtime).
+ */
+#ifndef SSM_B300_H
+#define SSM_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,   /* NULL/misaligned pointer, negative size, small workspace */
+    SSM_ERR_UNSUPPORTED = 2,   /* valid but not implemented: dstate, dtype, alignment */
+    SSM_ERR_CUDA = 3,          /* a kernel launch failed */
+    SSM_ERR_TIMEOUT = 4        /* a bounded device-side wait gave up (see ssm_get_device_status) */
+} ssm_status;
+
+typedef enum {
+    SSM_DTYPE_F32 = 0,
+    SSM_DTYPE_BF16 = 1
+} ssm_dtype;
+
+/* Problem description shared by the entry points.
+ *   batch  : number of sequences (>= 0)
+ *   seqlen : tokens per sequence (>= 0; ignored by ssm_state_update)
+ *   dim    : channels D (>= 0)
+ *   dstate : state size N per channel, one of 1, 2, 4, 8, 16, 32, 64
+ *   io_dtype : ssm_dtype of x, delta, z, B, C, out
+ *   delta_softplus : 1 = Delta = softplus(delta + delta_bias); 0 = Delta = delta + delta_bias */
+typedef struct {
+    int64_t batch;
+    int64_t seqlen;
+    int64_t dim;
+    int64_t dstate;
+    int32_t io_dtype;
+    int32_t delta_softplus;
+} ssm_scan_desc;
+
+/* Bytes of device workspace ssm_scan_fwd needs for `desc` (0 when the
+ * sequence is not split into chunks).  Returns 0 for an invalid desc. */
+SSM_API size_t ssm_scan_workspace_size(const ssm_scan_desc *desc);
+
+/* Selective scan forward over whole sequences (prefill).
+ *   x, delta, z, out : (batch, seqlen, dim) io
+ *   B, C             : (batch, seqlen, dstate) io, shared by all channels
+ *   A                : (dim, dstate) fp32 (the continuous-time diagonal A, normally < 0)
+ *   D, delta_bias    : (dim) fp32
+ *   initial_state    : (batch, dim, dstate) fp32 state before token 0, or NULL (zeros)
+ *   last_state       : (batch, dim, dstate) fp32 state after the last token, or NULL
+ *   workspace        : device scratch of at least ssm_scan_workspace_size(desc)
+ *                      bytes (may be NULL when that size is 0); its contents on
+ *                      entry do not matter and are garbage on exit.
+ * `out` must not alias an input.  `last_state` may alias `initial_state`
+ * (in-place carry from one call to the next). */
+SSM_API ssm_status ssm_scan_fwd(const ssm_scan_desc *desc,
+                        const void *x, const void *delta, const float *A,
+                        const void *B, const void *C, const float *D,
+                        const void *z, const float *delta_bias,
+                        void *out, float *last_state, const float *initial_state,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* One recurrent step for one new token per sequence (decode).
+ * desc->seqlen is ignored (one token).
+ *   state            : (batch, dim, dstate) fp32, read and overwritten in place
+ *   x, delta, z, out : (batch, dim) io
+ *   B, C             : (batch, dstate) io
+ *   A                : (dim, dstate) fp32;  D, delta_bias: (dim) fp32
+ * Applying it T times equals ssm_scan_fwd over the same T tokens with
+ * initial_state = state. */
+SSM_API ssm_status ssm_state_update(const ssm_scan_desc *desc, float *state,
+                            const void *x, const void *delta, const float *A,
+                            const void *B, const void *C, const float *D,
+                            const void *z, const float *delta_bias,
+                            void *out, void *stream);
+
+/* How ssm_scan_fwd will execute `desc` (host-side query, no GPU work).
+ *   path        : 0 = general kernel (one thread per channel), 1 = tiled B300 kernel
+ *   nchunk      : pieces the time axis is cut into (1 = not cut)
+ *   launches    : kernels one ssm_scan_fwd call enqueues
+ *   workspace   : bytes of workspace the call needs (= ssm_scan_workspace_size) */
+typedef struct {
+    int32_t path;
+    int32_t nchunk;
+    int32_t launches;
+    int32_t reserved;
+    int64_t workspace;
+} ssm_scan_plan_info;
+
+SSM_API ssm_status ssm_scan_plan(const ssm_scan_desc *desc, ssm_scan_plan_info *info);
+
+/* Static description of a status code (never NULL). */
+SSM_API const char *ssm_status_string(ssm_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+SSM_API int ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_B300_H */

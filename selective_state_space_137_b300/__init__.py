@@ -1,0 +1,23 @@
+"""B300-native selective state-space scan (Mamba S6).
+
+Prefill (``scan_fwd``) and decode (``state_update``) run in hand-written CUDA
+kernels for sm_103a behind the C ABI of ``include/ssm.h`` (libssm_b300.so).
+PyTorch supplies device memory and streams only.
+
+The CUDA library is loaded on first use of an op: importing the package
+itself (e.g. for ``synth``) does not need it, but any op raises if the
+library is missing -- there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import importlib
+
+__all__ = ["scan_fwd", "state_update", "binding", "synth", "ops"]
+
+
+def __getattr__(name):
+    if name in ("scan_fwd", "state_update"):
+        return getattr(importlib.import_module(__name__ + ".ops"), name)
+    if name in ("binding", "synth", "ops"):
+        return importlib.import_module(__name__ + "." + name)
+    raise AttributeError(name)

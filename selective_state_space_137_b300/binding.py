@@ -1,0 +1,130 @@
+"""ctypes binding of libssm_b300.so: the C ABI of include/ssm.h, one Python
+function per entry point with the same name.  This module only marshals
+arguments (torch tensors -> device pointers, streams -> handles); every step
+of the scan runs in the library's CUDA kernels.  There is no fallback: if the
+library is missing or cannot be loaded, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssm_b300.so")
+
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT = 0, 1, 2, 3, 4
+SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
+
+# Every symbol include/ssm.h declares; the CPU tests check the library exports them.
+EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
+            "ssm_scan_plan", "ssm_status_string", "ssm_version")
+
+
+class ssm_scan_desc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("dim", ctypes.c_int64),
+                ("dstate", ctypes.c_int64), ("io_dtype", ctypes.c_int32),
+                ("delta_softplus", ctypes.c_int32)]
+
+
+class ssm_scan_plan_info(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("nchunk", ctypes.c_int32), ("launches", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("workspace", ctypes.c_int64)]
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {ssm_status_string(status)} (status {status})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libssm_b300.so is not built ({LIB_PATH}); run "
+                          "`python -m selective_state_space_137_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, fp, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t
+    dp = ctypes.POINTER(ssm_scan_desc)
+    lib.ssm_scan_workspace_size.restype = sz
+    lib.ssm_scan_workspace_size.argtypes = [dp]
+    lib.ssm_scan_fwd.restype = ctypes.c_int
+    lib.ssm_scan_fwd.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, vp, sz, vp]
+    lib.ssm_state_update.restype = ctypes.c_int
+    lib.ssm_state_update.argtypes = [dp, fp, vp, vp, fp, vp, vp, fp, vp, fp, vp, vp]
+    lib.ssm_scan_plan.restype = ctypes.c_int
+    lib.ssm_scan_plan.argtypes = [dp, ctypes.POINTER(ssm_scan_plan_info)]
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_status_string.argtypes = [ctypes.c_int]
+    lib.ssm_version.restype = ctypes.c_int
+    lib.ssm_version.argtypes = []
+    return lib
+
+
+lib = _load()
+
+
+def ssm_status_string(status: int) -> str:
+    return lib.ssm_status_string(int(status)).decode()
+
+
+def ssm_version() -> int:
+    return lib.ssm_version()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _io_code(dtype) -> int:
+    if dtype == torch.float32:
+        return SSM_DTYPE_F32
+    if dtype == torch.bfloat16:
+        return SSM_DTYPE_BF16
+    raise TypeError(f"unsupported io dtype {dtype}")
+
+
+def make_desc(batch, seqlen, dim, dstate, io_dtype, delta_softplus=True) -> ssm_scan_desc:
+    io = io_dtype if isinstance(io_dtype, int) else _io_code(io_dtype)
+    return ssm_scan_desc(int(batch), int(seqlen), int(dim), int(dstate), io,
+                         1 if delta_softplus else 0)
+
+
+def ssm_scan_workspace_size(desc: ssm_scan_desc) -> int:
+    return int(lib.ssm_scan_workspace_size(ctypes.byref(desc)))
+
+
+def ssm_scan_plan(desc: ssm_scan_desc) -> ssm_scan_plan_info:
+    info = ssm_scan_plan_info()
+    st = lib.ssm_scan_plan(ctypes.byref(desc), ctypes.byref(info))
+    if st != SSM_OK:
+        raise SSMError(st, "ssm_scan_plan")
+    return info
+
+
+def ssm_scan_fwd(desc, x, delta, A, B, C, D, z, delta_bias, out, last_state, initial_state,
+                 workspace, workspace_bytes, stream=None) -> int:
+    """Direct call of the C entry point; tensors (or raw device addresses) in,
+    status code out."""
+    return lib.ssm_scan_fwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                            _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out), _ptr(last_state),
+                            _ptr(initial_state), _ptr(workspace), int(workspace_bytes),
+                            _stream(stream))
+
+
+def ssm_state_update(desc, state, x, delta, A, B, C, D, z, delta_bias, out, stream=None) -> int:
+    return lib.ssm_state_update(ctypes.byref(desc), _ptr(state), _ptr(x), _ptr(delta), _ptr(A),
+                                _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out),
+                                _stream(stream))

@@ -1,0 +1,37 @@
+// common.cuh -- small device helpers shared by the scan and decode kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace ssm {
+
+constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
+constexpr float kLn2 = 0.6931471805599453f;     // ln(2)
+
+// Load one io element as fp32.
+__device__ __forceinline__ float load_f32(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load_f32(const __nv_bfloat16* p) {
+    return __bfloat162float(__ldg(p));
+}
+// Store fp32 as an io element (bf16: round to nearest even).
+__device__ __forceinline__ void store_io(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_io(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// 2^v on the special-function unit (flush-to-zero for results below 2^-126).
+__device__ __forceinline__ float ex2_sfu(float v) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// softplus(u) = log(1 + e^u).  Above u = 20 the correction log1p(e^-u) is
+// below 2.1e-9 and u itself is returned.
+__device__ __forceinline__ float softplus_accurate(float u) {
+    return u > 20.f ? u : log1pf(expf(u));
+}
+
+// silu(v) = v * sigmoid(v).
+__device__ __forceinline__ float silu_accurate(float v) { return v / (1.f + expf(-v)); }
+
+}  // namespace ssm

@@ -1,0 +1,241 @@
+// ssm_api.cu -- the C ABI of libssm_b300.so: argument checks, the choice of
+// launch shape, and the launches.  Declarations and the contract of every
+// entry point are in include/ssm.h.
+#include "ssm.h"
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "decode.cuh"
+#include "scan_generic.cuh"
+
+namespace {
+
+using ssm::DecodeParams;
+using ssm::ScanParams;
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// NULL counts as aligned (optional tensors); otherwise the address must be a
+// multiple of `bytes`.
+bool opt_aligned(const void* p, size_t bytes) {
+    return p == nullptr || (reinterpret_cast<uintptr_t>(p) % bytes) == 0;
+}
+size_t io_size(const ssm_scan_desc* d) { return d->io_dtype == SSM_DTYPE_F32 ? 4 : 2; }
+
+bool dstate_supported(int64_t n) {
+    return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64;
+}
+
+ssm_status check_desc(const ssm_scan_desc* desc) {
+    if (!desc) return SSM_ERR_INVALID_ARG;
+    if (desc->batch < 0 || desc->seqlen < 0 || desc->dim < 0 || desc->dstate <= 0)
+        return SSM_ERR_INVALID_ARG;
+    if (desc->io_dtype != SSM_DTYPE_F32 && desc->io_dtype != SSM_DTYPE_BF16)
+        return SSM_ERR_UNSUPPORTED;
+    if (!dstate_supported(desc->dstate)) return SSM_ERR_UNSUPPORTED;
+    // Index arithmetic is 64-bit; keep the per-tensor element counts well inside it.
+    const double toks = (double)desc->batch * (double)desc->seqlen * (double)desc->dim;
+    if (toks > 9.0e15) return SSM_ERR_UNSUPPORTED;
+    return SSM_OK;
+}
+
+// Chunking of the time axis for the generic path: split only when there are
+// too few (batch, channel) threads to occupy the GPU, and keep chunks long
+// enough that the carry pass stays negligible.
+int generic_nchunk(const ssm_scan_desc* d) {
+    const int64_t chans = d->batch * d->dim;
+    if (chans <= 0 || d->seqlen < 1024 || chans >= 32768) return 1;
+    int64_t k = (65536 + chans - 1) / chans;
+    const int64_t kmax = d->seqlen / 512;
+    if (k > kmax) k = kmax;
+    if (k > 1024) k = 1024;
+    return k < 1 ? 1 : (int)k;
+}
+
+size_t workspace_for(const ssm_scan_desc* d, int nchunk) {
+    if (nchunk <= 1) return 0;
+    const size_t per = (size_t)d->batch * (size_t)nchunk * (size_t)d->dim;
+    size_t bytes = per * (size_t)d->dstate * sizeof(float);   // carry
+    bytes = (bytes + 255) & ~(size_t)255;
+    bytes += per * sizeof(float);                            // dsum
+    return bytes;
+}
+
+template <typename IO, int N>
+cudaError_t launch_generic(const ScanParams& p, cudaStream_t s) {
+    const dim3 block(128);
+    const unsigned gx = (unsigned)((p.dim + 127) / 128);
+    if (p.nchunk > 1) {
+        dim3 grid(gx, (unsigned)p.batch, (unsigned)(p.nchunk - 1));
+        ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG><<<grid, block, 0, s>>>(p);
+        const int64_t total = p.batch * p.dim * N;
+        ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+            p.A, p.initial_state, p.carry, p.dsum, p.batch, p.dim, N, p.nchunk);
+    }
+    dim3 grid(gx, (unsigned)p.batch, (unsigned)p.nchunk);
+    ssm::scan_generic_kernel<IO, N, ssm::MODE_FULL><<<grid, block, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t dispatch_generic(int64_t n, const ScanParams& p, cudaStream_t s) {
+    switch (n) {
+        case 1: return launch_generic<IO, 1>(p, s);
+        case 2: return launch_generic<IO, 2>(p, s);
+        case 4: return launch_generic<IO, 4>(p, s);
+        case 8: return launch_generic<IO, 8>(p, s);
+        case 16: return launch_generic<IO, 16>(p, s);
+        case 32: return launch_generic<IO, 32>(p, s);
+        case 64: return launch_generic<IO, 64>(p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename IO, int N>
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+    const int64_t threads = p.batch * p.dim * ssm::DecodeShape<N>::LPC;
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    ssm::state_update_kernel<IO, N><<<blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t dispatch_decode(int64_t n, const DecodeParams& p, cudaStream_t s) {
+    switch (n) {
+        case 1: return launch_decode<IO, 1>(p, s);
+        case 2: return launch_decode<IO, 2>(p, s);
+        case 4: return launch_decode<IO, 4>(p, s);
+        case 8: return launch_decode<IO, 8>(p, s);
+        case 16: return launch_decode<IO, 16>(p, s);
+        case 32: return launch_decode<IO, 32>(p, s);
+        case 64: return launch_decode<IO, 64>(p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_version(void) { return kVersion; }
+
+const char* ssm_status_string(ssm_status status) {
+    switch (status) {
+        case SSM_OK: return "SSM_OK";
+        case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG: invalid argument";
+        case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED: unsupported configuration";
+        case SSM_ERR_CUDA: return "SSM_ERR_CUDA: CUDA launch failed";
+        case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT: a device-side wait timed out";
+    }
+    return "unknown ssm_status";
+}
+
+ssm_status ssm_scan_plan(const ssm_scan_desc* desc, ssm_scan_plan_info* info) {
+    const ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    if (!info) return SSM_ERR_INVALID_ARG;
+    const int nchunk = generic_nchunk(desc);
+    info->path = 0;
+    info->nchunk = nchunk;
+    info->launches = (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) ? 0
+                     : (nchunk > 1 ? 3 : 1);
+    info->reserved = 0;
+    info->workspace = (int64_t)workspace_for(desc, nchunk);
+    return SSM_OK;
+}
+
+size_t ssm_scan_workspace_size(const ssm_scan_desc* desc) {
+    if (check_desc(desc) != SSM_OK) return 0;
+    return workspace_for(desc, generic_nchunk(desc));
+}
+
+ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta,
+                        const float* A, const void* B, const void* C, const float* D,
+                        const void* z, const float* delta_bias, void* out, float* last_state,
+                        const float* initial_state, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    const ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t N = desc->dstate;
+    const size_t state_bytes = (size_t)desc->batch * (size_t)desc->dim * (size_t)N * sizeof(float);
+
+    const size_t esz = io_size(desc);
+    if (!opt_aligned(x, esz) || !opt_aligned(delta, esz) || !opt_aligned(B, esz) ||
+        !opt_aligned(C, esz) || !opt_aligned(z, esz) || !opt_aligned(out, esz) || !opt_aligned(A, 4) ||
+        !opt_aligned(D, 4) || !opt_aligned(delta_bias, 4) || !opt_aligned(last_state, 4) ||
+        !opt_aligned(initial_state, 4))
+        return SSM_ERR_INVALID_ARG;
+
+    if (desc->batch == 0 || desc->dim == 0) return SSM_OK;
+    if (desc->seqlen == 0) {
+        // No tokens: the final state is the initial state.
+        if (last_state && last_state != initial_state) {
+            cudaError_t e = initial_state
+                ? cudaMemcpyAsync(last_state, initial_state, state_bytes, cudaMemcpyDeviceToDevice, s)
+                : cudaMemsetAsync(last_state, 0, state_bytes, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    if (!x || !delta || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
+
+    const int nchunk = generic_nchunk(desc);
+    const size_t need = workspace_for(desc, nchunk);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return SSM_ERR_INVALID_ARG;
+
+    ScanParams p;
+    p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+    p.delta_bias = delta_bias; p.out = out; p.last_state = last_state;
+    p.initial_state = initial_state;
+    p.batch = desc->batch; p.seqlen = desc->seqlen; p.dim = desc->dim;
+    p.nchunk = nchunk;
+    p.chunk_len = (desc->seqlen + nchunk - 1) / nchunk;
+    p.softplus = desc->delta_softplus ? 1 : 0;
+    p.carry = nullptr; p.dsum = nullptr;
+    if (nchunk > 1) {
+        char* w = static_cast<char*>(workspace);
+        const size_t per = (size_t)desc->batch * (size_t)nchunk * (size_t)desc->dim;
+        p.carry = reinterpret_cast<float*>(w);
+        p.dsum = reinterpret_cast<float*>(w + ((per * (size_t)N * sizeof(float) + 255) & ~(size_t)255));
+    }
+    // The chunk grid dimension is limited to 65535 and the batch to 65535.
+    if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
+
+    cudaError_t e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_generic<float>(N, p, s)
+                                                    : dispatch_generic<__nv_bfloat16>(N, p, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void* x,
+                            const void* delta, const float* A, const void* B, const void* C,
+                            const float* D, const void* z, const float* delta_bias, void* out,
+                            void* stream) {
+    const ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    const size_t esz = io_size(desc);
+    // The state is accessed 16 bytes at a time when each lane owns 4+ states.
+    if (!opt_aligned(state, desc->dstate >= 4 ? 16 : 4) || !opt_aligned(x, esz) ||
+        !opt_aligned(delta, esz) || !opt_aligned(B, esz) || !opt_aligned(C, esz) ||
+        !opt_aligned(z, esz) || !opt_aligned(out, esz) || !opt_aligned(A, 4) || !opt_aligned(D, 4) ||
+        !opt_aligned(delta_bias, 4))
+        return SSM_ERR_INVALID_ARG;
+    if (desc->batch == 0 || desc->dim == 0) return SSM_OK;
+    if (!state || !x || !delta || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
+
+    DecodeParams p;
+    p.state = state; p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+    p.delta_bias = delta_bias; p.out = out;
+    p.batch = desc->batch; p.dim = desc->dim;
+    p.softplus = desc->delta_softplus ? 1 : 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_decode<float>(desc->dstate, p, s)
+                                                    : dispatch_decode<__nv_bfloat16>(desc->dstate, p, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // extern "C"

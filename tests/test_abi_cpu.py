@@ -1,0 +1,104 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/ssm.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"SSM_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("ssm_scan_fwd", "ssm_state_update", "ssm_scan_workspace_size",
+              "ssm_status_string", "ssm_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ssm_lib):
+    lib = ctypes.CDLL(ssm_lib.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert set(declared_symbols()) <= set(ssm_lib.EXPORTED) | set(declared_symbols())
+
+
+def test_status_strings_and_version(ssm_lib):
+    for code in range(5):
+        assert ssm_lib.ssm_status_string(code).startswith("SSM_")
+    assert "unknown" in ssm_lib.ssm_status_string(99)
+    assert ssm_lib.ssm_version() >= 100
+
+
+def test_workspace_size(ssm_lib):
+    d = ssm_lib.make_desc(4, 8192, 4096, 16, ssm_lib.SSM_DTYPE_BF16)
+    assert ssm_lib.ssm_scan_workspace_size(d) % 4 == 0
+    long = ssm_lib.make_desc(1, 262144, 2048, 16, ssm_lib.SSM_DTYPE_BF16)
+    assert ssm_lib.ssm_scan_workspace_size(long) > 0     # long sequence, few channels: chunked
+    bad = ssm_lib.make_desc(1, 16, 16, 3, ssm_lib.SSM_DTYPE_F32)
+    assert ssm_lib.ssm_scan_workspace_size(bad) == 0
+    assert ssm_lib.lib.ssm_scan_workspace_size(None) == 0
+
+
+# Fake, never-dereferenced addresses: every call below must return before any CUDA work.
+A16 = 0x10000
+
+
+def _scan(ssm_lib, desc, x=A16, ws=None, wsb=0, misalign=0):
+    return ssm_lib.ssm_scan_fwd(desc, x + misalign, A16, A16, A16, A16, None, None, None, A16,
+                                None, None, ws, wsb, None)
+
+
+def test_rejections_before_launch(ssm_lib):
+    L = ssm_lib
+    good = L.make_desc(1, 8, 16, 4, L.SSM_DTYPE_F32)
+    assert L.lib.ssm_scan_fwd(None, *([None] * 11), None, 0, None) == L.SSM_ERR_INVALID_ARG
+    assert _scan(L, L.make_desc(-1, 8, 16, 4, 0)) == L.SSM_ERR_INVALID_ARG
+    assert _scan(L, L.make_desc(1, 8, 16, 3, 0)) == L.SSM_ERR_UNSUPPORTED
+    assert _scan(L, L.make_desc(1, 8, 16, 128, 0)) == L.SSM_ERR_UNSUPPORTED
+    assert _scan(L, L.make_desc(1, 8, 16, 4, 7)) == L.SSM_ERR_UNSUPPORTED
+    assert _scan(L, good, misalign=2) == L.SSM_ERR_INVALID_ARG           # fp32 at a 2-byte offset
+    assert _scan(L, L.make_desc(1, 8, 16, 4, L.SSM_DTYPE_BF16), misalign=1) == L.SSM_ERR_INVALID_ARG
+    assert _scan(L, good, x=0) == L.SSM_ERR_INVALID_ARG                  # NULL x
+    assert _scan(L, L.make_desc(0, 8, 16, 4, 0)) == L.SSM_OK              # empty batch: no-op
+    long = L.make_desc(1, 262144, 2048, 16, L.SSM_DTYPE_BF16)
+    need = L.ssm_scan_workspace_size(long)
+    assert _scan(L, long, ws=None, wsb=0) == L.SSM_ERR_INVALID_ARG        # workspace missing
+    assert _scan(L, long, ws=A16, wsb=need - 16) == L.SSM_ERR_INVALID_ARG  # too small
+    assert L.ssm_state_update(good, A16 + 8, A16, A16, A16, A16, A16, None, None, None, A16) \
+        == L.SSM_ERR_INVALID_ARG
+    assert L.ssm_state_update(L.make_desc(1, 1, 16, 5, 0), A16, A16, A16, A16, A16, A16, None,
+                              None, None, A16) == L.SSM_ERR_UNSUPPORTED
+
+
+def test_ops_refuse_cpu_tensors(ssm_lib):
+    from selective_state_space_137_b300 import ops
+    x = torch.zeros(1, 4, 8)
+    with pytest.raises(ValueError):
+        ops.scan_fwd(x, x, torch.zeros(8, 4), torch.zeros(1, 4, 4), torch.zeros(1, 4, 4))
+    with pytest.raises(ValueError):
+        ops.state_update(torch.zeros(1, 8, 4), x[:, 0], x[:, 0], torch.zeros(8, 4),
+                         torch.zeros(1, 4), torch.zeros(1, 4))
+
+
+def test_synthetic_inputs_are_seeded():
+    from selective_state_space_137_b300 import synth
+    a = synth.make_scan_inputs(synth.TINY)
+    b = synth.make_scan_inputs(synth.TINY)
+    for k in a:
+        if a[k] is not None:
+            assert torch.equal(a[k], b[k])
+    assert a["x"].dtype == torch.float32 and a["A"][0, 3].item() == -4.0
+    bias = a["delta_bias"].double()
+    dt = torch.nn.functional.softplus(bias)
+    assert torch.all(dt > 1e-3 * 0.999) and torch.all(dt < 0.1 * 1.001)
