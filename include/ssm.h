@@ -123,6 +123,39 @@ SSM_API ssm_status ssm_state_update(const ssm_scan_desc *desc, float *state,
                             const void *z, const float *delta_bias,
                             void *out, void *stream);
 
+/* Capacity of the fixed scratch buffer used by ssm_scan_fwd_noalloc. */
+#define SSM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* ssm_scan_fwd for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point: it exists for library users, not
+ * for the method.
+ *
+ * Some callers cannot call cudaMalloc or hand the library a workspace: a
+ * plug-in interface that gives an operator only its input and output
+ * buffers and no allocator, or a latency-bound loop that must not call
+ * cudaMalloc/cudaFree because those may block and synchronise the device.
+ * This variant takes the same arguments as ssm_scan_fwd minus the workspace
+ * and allocates nothing: when the plan needs scratch (a long sequence over
+ * few channels is cut into chunks), it uses one file-scope device array of
+ * SSM_NOALLOC_SCRATCH_BYTES (8 MiB).  Every GPU that loads the library holds
+ * that array until the process exits.
+ *   - Problems that need more scratch than that return SSM_ERR_UNSUPPORTED
+ *     before anything is enqueued (ssm_scan_workspace_size tells the need).
+ *   - The first call on a device looks up the array's device address once
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array, and it keeps the previous call's
+ *     contents.  Every value a call reads from it was written earlier in the
+ *     same call, so nothing has to start at zero; but two calls that overlap
+ *     on the GPU (different streams, or different host threads) race on it
+ *     and give wrong results.  Serialise them. */
+SSM_API ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc *desc,
+                                        const void *x, const void *delta, const float *A,
+                                        const void *B, const void *C, const float *D,
+                                        const void *z, const float *delta_bias,
+                                        void *out, float *last_state,
+                                        const float *initial_state, void *stream);
+
 /* How ssm_scan_fwd will execute `desc` (host-side query, no GPU work).
  *   path        : 0 = general kernel (one thread per channel), 1 = tiled B300 kernel
  *   nchunk      : pieces the time axis is cut into (1 = not cut)

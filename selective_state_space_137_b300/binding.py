@@ -19,7 +19,8 @@ SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 
 # Every symbol include/ssm.h declares; the CPU tests check the library exports them.
 EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
-            "ssm_scan_plan", "ssm_status_string", "ssm_version")
+            "ssm_scan_plan", "ssm_status_string", "ssm_version", "ssm_scan_fwd_noalloc")
+SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class ssm_scan_desc(ctypes.Structure):
@@ -52,6 +53,8 @@ def _load():
     lib.ssm_scan_fwd.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, vp, sz, vp]
     lib.ssm_state_update.restype = ctypes.c_int
     lib.ssm_state_update.argtypes = [dp, fp, vp, vp, fp, vp, vp, fp, vp, fp, vp, vp]
+    lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
+    lib.ssm_scan_fwd_noalloc.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, vp]
     lib.ssm_scan_plan.restype = ctypes.c_int
     lib.ssm_scan_plan.argtypes = [dp, ctypes.POINTER(ssm_scan_plan_info)]
     lib.ssm_status_string.restype = ctypes.c_char_p
@@ -128,3 +131,12 @@ def ssm_state_update(desc, state, x, delta, A, B, C, D, z, delta_bias, out, stre
     return lib.ssm_state_update(ctypes.byref(desc), _ptr(state), _ptr(x), _ptr(delta), _ptr(A),
                                 _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out),
                                 _stream(stream))
+
+
+def ssm_scan_fwd_noalloc(desc, x, delta, A, B, C, D, z, delta_bias, out, last_state,
+                         initial_state, stream=None) -> int:
+    """The scan for callers that cannot allocate: no workspace argument; the
+    library's fixed device scratch array is used instead."""
+    return lib.ssm_scan_fwd_noalloc(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(B),
+                                    _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out),
+                                    _ptr(last_state), _ptr(initial_state), _stream(stream))

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "decode.cuh"
 #include "scan_generic.cuh"
@@ -239,3 +241,52 @@ ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void*
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// ssm_scan_fwd_noalloc: the scan for callers that cannot allocate device
+// memory.  Its chunk-carry scratch is this file-scope device array instead of
+// a caller workspace; see include/ssm.h for the contract.
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[SSM_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoAllocMaxDevices = 256;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device with cudaGetSymbolAddress (that device current) and cached.
+cudaError_t noalloc_scratch_address(void** addr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_addr[dev] = p;
+    }
+    *addr = g_noalloc_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void* x,
+                                           const void* delta, const float* A, const void* B,
+                                           const void* C, const float* D, const void* z,
+                                           const float* delta_bias, void* out,
+                                           float* last_state, const float* initial_state,
+                                           void* stream) {
+    const ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    const size_t need = ssm_scan_workspace_size(desc);
+    if (need > (size_t)SSM_NOALLOC_SCRATCH_BYTES) return SSM_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if (need > 0 && noalloc_scratch_address(&scratch) != cudaSuccess) return SSM_ERR_CUDA;
+    return ssm_scan_fwd(desc, x, delta, A, B, C, D, z, delta_bias, out, last_state,
+                        initial_state, scratch, need, stream);
+}
