@@ -158,6 +158,8 @@ SSM_API ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc *desc,
 
 /* How ssm_scan_fwd will execute `desc` (host-side query, no GPU work).
  *   path        : 0 = general kernel (one thread per channel), 1 = tiled B300 kernel
+ *                 (the tiled kernel is used when the io tensors are 16-byte
+ *                 aligned; the plan reported assumes they are)
  *   nchunk      : pieces the time axis is cut into (1 = not cut)
  *   launches    : kernels one ssm_scan_fwd call enqueues
  *   workspace   : bytes of workspace the call needs (= ssm_scan_workspace_size) */
@@ -170,6 +172,12 @@ typedef struct {
 } ssm_scan_plan_info;
 
 SSM_API ssm_status ssm_scan_plan(const ssm_scan_desc *desc, ssm_scan_plan_info *info);
+
+/* Device-side status of the kernels that ran so far on the current device:
+ * SSM_ERR_TIMEOUT if a bounded wait inside a kernel gave up (that launch's
+ * outputs are then incomplete), SSM_OK otherwise.  Reading it clears it.
+ * Synchronises with the device (it waits for all prior work). */
+SSM_API ssm_status ssm_get_device_status(void);
 
 /* Static description of a status code (never NULL). */
 SSM_API const char *ssm_status_string(ssm_status status);

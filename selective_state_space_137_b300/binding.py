@@ -19,7 +19,8 @@ SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 
 # Every symbol include/ssm.h declares; the CPU tests check the library exports them.
 EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
-            "ssm_scan_plan", "ssm_status_string", "ssm_version", "ssm_scan_fwd_noalloc")
+            "ssm_scan_plan", "ssm_status_string", "ssm_version", "ssm_scan_fwd_noalloc",
+            "ssm_get_device_status")
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -57,6 +58,8 @@ def _load():
     lib.ssm_scan_fwd_noalloc.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, vp]
     lib.ssm_scan_plan.restype = ctypes.c_int
     lib.ssm_scan_plan.argtypes = [dp, ctypes.POINTER(ssm_scan_plan_info)]
+    lib.ssm_get_device_status.restype = ctypes.c_int
+    lib.ssm_get_device_status.argtypes = []
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_status_string.argtypes = [ctypes.c_int]
     lib.ssm_version.restype = ctypes.c_int
@@ -69,6 +72,10 @@ lib = _load()
 
 def ssm_status_string(status: int) -> str:
     return lib.ssm_status_string(int(status)).decode()
+
+
+def ssm_get_device_status() -> int:
+    return lib.ssm_get_device_status()
 
 
 def ssm_version() -> int:

@@ -6,11 +6,15 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include <cstring>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "decode.cuh"
 #include "scan_generic.cuh"
+#include "scan_tiled.cuh"
 
 namespace {
 
@@ -118,6 +122,143 @@ cudaError_t dispatch_decode(int64_t n, const DecodeParams& p, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------------------
+// Tiled path (path 1): TMA-staged tiles, per-token work hoisted out of the
+// state loop.  Chosen for bf16/fp32 I/O with dstate 8, 16 or 32, rows that
+// are 16-byte multiples and 16-byte aligned tensors.
+
+constexpr int kPlanSMs = 148;        // the plan is fixed for a 148-SM B300
+constexpr int kTileT = 32;           // time steps per tile
+constexpr int kStages = 3;           // TMA ring depth
+
+template <typename IO, int N>
+struct TiledFor;   // (KS, DC) per dstate: 8 states per thread, 32-64 threads per CTA
+template <typename IO> struct TiledFor<IO, 8>  { using Cfg = ssm::TiledCfg<IO, 8, 1, 32, kTileT, kStages>; };
+template <typename IO> struct TiledFor<IO, 16> { using Cfg = ssm::TiledCfg<IO, 16, 2, 16, kTileT, kStages>; };
+template <typename IO> struct TiledFor<IO, 32> { using Cfg = ssm::TiledCfg<IO, 32, 4, 16, kTileT, kStages>; };
+
+struct TiledShape { int dc, threads, smem; };
+
+template <typename IO>
+TiledShape tiled_shape_io(int64_t n) {
+    switch (n) {
+        case 8: { using C = typename TiledFor<IO, 8>::Cfg; return {C::DC, C::THREADS, C::SMEM}; }
+        case 16: { using C = typename TiledFor<IO, 16>::Cfg; return {C::DC, C::THREADS, C::SMEM}; }
+        case 32: { using C = typename TiledFor<IO, 32>::Cfg; return {C::DC, C::THREADS, C::SMEM}; }
+    }
+    return {0, 0, 0};
+}
+
+TiledShape tiled_shape(const ssm_scan_desc* d) {
+    return d->io_dtype == SSM_DTYPE_F32 ? tiled_shape_io<float>(d->dstate)
+                                        : tiled_shape_io<__nv_bfloat16>(d->dstate);
+}
+
+// Shape-only eligibility for the tiled path (pointer alignment is checked at call time).
+bool tiled_shape_ok(const ssm_scan_desc* d) {
+    if (tiled_shape(d).dc == 0) return false;
+    const int64_t e = d->io_dtype == SSM_DTYPE_F32 ? 4 : 2;
+    if ((d->dim * e) % 16 != 0 || (d->dstate * e) % 16 != 0) return false;
+    // TMA coordinates are 32-bit and the batch is a grid dimension
+    if (d->seqlen >= (int64_t)1 << 31 || d->dim >= (int64_t)1 << 31 || d->batch > 65535) return false;
+    return true;
+}
+
+// Chunks of the time axis for the tiled path: cut only when the (batch,
+// channel-block) CTAs cannot fill the GPU; chunk lengths are tile multiples.
+void tiled_chunks(const ssm_scan_desc* d, int* nchunk, int64_t* chunk_len) {
+    const TiledShape sh = tiled_shape(d);
+    const int64_t groups = d->batch * ((d->dim + sh.dc - 1) / sh.dc);
+    int per_sm = (228 * 1024) / (sh.smem + 1024);
+    if (per_sm > 2048 / sh.threads) per_sm = 2048 / sh.threads;
+    if (per_sm > 32) per_sm = 32;
+    const int64_t target = (int64_t)kPlanSMs * per_sm;
+    int64_t k = 1;
+    if (groups > 0 && groups * 2 < target) {
+        k = (target + groups - 1) / groups;
+        const int64_t kmax = d->seqlen / (4 * kTileT);
+        if (k > kmax) k = kmax;
+        if (k > 4096) k = 4096;
+        if (k < 1) k = 1;
+    }
+    int64_t len = (d->seqlen + k - 1) / k;
+    len = (len + kTileT - 1) / kTileT * kTileT;
+    if (len < kTileT) len = kTileT;
+    *chunk_len = len;
+    *nchunk = d->seqlen > 0 ? (int)((d->seqlen + len - 1) / len) : 1;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Tensor map of a (batch, rows, cols) row-major tensor, box [box_rows][box_cols].
+bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz, int64_t cols,
+               int64_t rows, int64_t batch, int box_cols, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)(cols * esz), (cuuint64_t)(cols * rows * esz)};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename IO, int N>
+cudaError_t launch_tiled(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
+    using Cfg = typename TiledFor<IO, N>::Cfg;
+    const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    ssm::TiledMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    const int e = (int)sizeof(IO);
+    bool ok = encode_3d(&maps.x, p.x, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+              encode_3d(&maps.delta, p.delta, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+              encode_3d(&maps.B, p.B, dt, e, N, d->seqlen, d->batch, N, Cfg::T) &&
+              encode_3d(&maps.C, p.C, dt, e, N, d->seqlen, d->batch, N, Cfg::T) &&
+              encode_3d(&maps.out, p.out, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+    if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+    if (!ok) return cudaErrorInvalidValue;
+
+    auto kfull = ssm::scan_tiled_kernel<IO, Cfg, ssm::MODE_FULL>;
+    auto kagg = ssm::scan_tiled_kernel<IO, Cfg, ssm::MODE_AGG>;
+    cudaError_t err = cudaFuncSetAttribute(kfull, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(kagg, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (err != cudaSuccess) return err;
+    const unsigned gx = (unsigned)((d->dim + Cfg::DC - 1) / Cfg::DC);
+    if (p.nchunk > 1) {
+        kagg<<<dim3(gx, (unsigned)d->batch, (unsigned)(p.nchunk - 1)), Cfg::THREADS, Cfg::SMEM, s>>>(maps, p);
+        const int64_t total = p.batch * p.dim * N;
+        ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+            p.A, p.initial_state, p.carry, p.dsum, p.batch, p.dim, N, p.nchunk);
+    }
+    kfull<<<dim3(gx, (unsigned)d->batch, (unsigned)p.nchunk), Cfg::THREADS, Cfg::SMEM, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t dispatch_tiled(const ssm_scan_desc* d, const ScanParams& p, cudaStream_t s) {
+    switch (d->dstate) {
+        case 8: return launch_tiled<IO, 8>(d, p, s);
+        case 16: return launch_tiled<IO, 16>(d, p, s);
+        case 32: return launch_tiled<IO, 32>(d, p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 extern "C" {
@@ -139,8 +280,15 @@ ssm_status ssm_scan_plan(const ssm_scan_desc* desc, ssm_scan_plan_info* info) {
     const ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     if (!info) return SSM_ERR_INVALID_ARG;
-    const int nchunk = generic_nchunk(desc);
-    info->path = 0;
+    int nchunk;
+    int64_t chunk_len;
+    const bool tiled = tiled_shape_ok(desc);
+    if (tiled) {
+        tiled_chunks(desc, &nchunk, &chunk_len);
+    } else {
+        nchunk = generic_nchunk(desc);
+    }
+    info->path = tiled ? 1 : 0;
     info->nchunk = nchunk;
     info->launches = (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) ? 0
                      : (nchunk > 1 ? 3 : 1);
@@ -151,7 +299,17 @@ ssm_status ssm_scan_plan(const ssm_scan_desc* desc, ssm_scan_plan_info* info) {
 
 size_t ssm_scan_workspace_size(const ssm_scan_desc* desc) {
     if (check_desc(desc) != SSM_OK) return 0;
-    return workspace_for(desc, generic_nchunk(desc));
+    // Enough for either path: the tiled one is taken only with 16-byte
+    // aligned tensors, which is known at call time.
+    size_t need = workspace_for(desc, generic_nchunk(desc));
+    if (tiled_shape_ok(desc)) {
+        int nchunk;
+        int64_t chunk_len;
+        tiled_chunks(desc, &nchunk, &chunk_len);
+        const size_t t = workspace_for(desc, nchunk);
+        if (t > need) need = t;
+    }
+    return need;
 }
 
 ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta,
@@ -185,7 +343,17 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
     }
     if (!x || !delta || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
 
-    const int nchunk = generic_nchunk(desc);
+    const bool tiled = tiled_shape_ok(desc) && aligned16(x) && aligned16(delta) &&
+                       aligned16(B) && aligned16(C) && aligned16(out) && opt_aligned(z, 16) &&
+                       opt_aligned(last_state, 16);
+    int nchunk;
+    int64_t chunk_len;
+    if (tiled) {
+        tiled_chunks(desc, &nchunk, &chunk_len);
+    } else {
+        nchunk = generic_nchunk(desc);
+        chunk_len = (desc->seqlen + nchunk - 1) / nchunk;
+    }
     const size_t need = workspace_for(desc, nchunk);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
         return SSM_ERR_INVALID_ARG;
@@ -196,7 +364,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
     p.initial_state = initial_state;
     p.batch = desc->batch; p.seqlen = desc->seqlen; p.dim = desc->dim;
     p.nchunk = nchunk;
-    p.chunk_len = (desc->seqlen + nchunk - 1) / nchunk;
+    p.chunk_len = chunk_len;
     p.softplus = desc->delta_softplus ? 1 : 0;
     p.carry = nullptr; p.dsum = nullptr;
     if (nchunk > 1) {
@@ -208,9 +376,25 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
     // The chunk grid dimension is limited to 65535 and the batch to 65535.
     if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
 
-    cudaError_t e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_generic<float>(N, p, s)
-                                                    : dispatch_generic<__nv_bfloat16>(N, p, s);
+    cudaError_t e;
+    if (tiled)
+        e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_tiled<float>(desc, p, s)
+                                            : dispatch_tiled<__nv_bfloat16>(desc, p, s);
+    else
+        e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_generic<float>(N, p, s)
+                                            : dispatch_generic<__nv_bfloat16>(N, p, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_get_device_status(void) {
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, ssm::g_ssm_device_error, sizeof(word)) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (word == 0) return SSM_OK;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(ssm::g_ssm_device_error, &zero, sizeof(zero)) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return SSM_ERR_TIMEOUT;
 }
 
 ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void* x,

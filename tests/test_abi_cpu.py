@@ -72,7 +72,8 @@ def test_rejections_before_launch(ssm_lib):
     assert _scan(L, good, x=0) == L.SSM_ERR_INVALID_ARG                  # NULL x
     assert _scan(L, L.make_desc(0, 8, 16, 4, 0)) == L.SSM_OK              # empty batch: no-op
     long = L.make_desc(1, 262144, 2048, 16, L.SSM_DTYPE_BF16)
-    need = L.ssm_scan_workspace_size(long)
+    need = L.ssm_scan_plan(long).workspace        # the path these aligned addresses take
+    assert 0 < need <= L.ssm_scan_workspace_size(long)
     assert _scan(L, long, ws=None, wsb=0) == L.SSM_ERR_INVALID_ARG        # workspace missing
     assert _scan(L, long, ws=A16, wsb=need - 16) == L.SSM_ERR_INVALID_ARG  # too small
     assert L.ssm_state_update(good, A16 + 8, A16, A16, A16, A16, A16, None, None, None, A16) \
@@ -102,3 +103,15 @@ def test_synthetic_inputs_are_seeded():
     bias = a["delta_bias"].double()
     dt = torch.nn.functional.softplus(bias)
     assert torch.all(dt > 1e-3 * 0.999) and torch.all(dt < 0.1 * 1.001)
+
+
+def test_plan_picks_the_tiled_path(ssm_lib):
+    L = ssm_lib
+    big = L.ssm_scan_plan(L.make_desc(4, 8192, 4096, 16, L.SSM_DTYPE_BF16))
+    assert (big.path, big.nchunk, big.launches, big.workspace) == (1, 1, 1, 0)
+    long = L.ssm_scan_plan(L.make_desc(1, 262144, 2048, 16, L.SSM_DTYPE_BF16))
+    assert long.path == 1 and long.nchunk > 1 and long.launches == 3 and long.workspace > 0
+    assert L.ssm_scan_workspace_size(L.make_desc(1, 262144, 2048, 16, L.SSM_DTYPE_BF16)) >= long.workspace
+    for n, path in ((1, 0), (2, 0), (4, 0), (8, 1), (16, 1), (32, 1), (64, 0)):
+        assert L.ssm_scan_plan(L.make_desc(2, 300, 72, n, L.SSM_DTYPE_BF16)).path == path
+    assert L.ssm_scan_plan(L.make_desc(2, 300, 12, 16, L.SSM_DTYPE_BF16)).path == 0   # 24-byte rows

@@ -150,3 +150,44 @@ def test_full_size_sampled(cuda, w):
         got_last = f64(last[b].index_select(0, idx))
         assert rel_err(got, ref) <= tol, (b, ds, rel_err(got, ref))
         assert rel_err(got_last, ref_last) <= tol, (b, ds, rel_err(got_last, ref_last))
+
+
+def _misaligned_copy(t, cuda):
+    """Same values at an address that is element-aligned but not 16-byte aligned."""
+    e = t.element_size()
+    off = 8 // e
+    buf = torch.empty(t.numel() + off, dtype=t.dtype, device=cuda)
+    v = buf[off:off + t.numel()].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 16 != 0
+    return v
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_general_path_when_not_16_byte_aligned(cuda, io):
+    """Element-aligned but not 16-byte aligned tensors take the general kernel;
+    it must agree with the oracle too (dstate 16, the tiled path's shape)."""
+    w = dataclasses.replace(SMALL, io=io, init_state=True, seed=81)
+    inp = synth.make_scan_inputs(w)
+    dev = to_device(inp, cuda)
+    for k in ("x", "delta", "z"):
+        dev[k] = _misaligned_copy(dev[k], cuda)
+    out = _misaligned_copy(torch.zeros_like(dev["x"]), cuda)
+    out, last = ops.scan_fwd(**dev, out=out)
+    torch.cuda.synchronize()
+    ref, ref_last = oracle_full(inp)
+    tol = TOL[inp["x"].dtype]
+    assert rel_err(f64(out), ref) <= tol and rel_err(f64(last), ref_last) <= tol
+
+
+def test_tiled_and_general_paths_agree(cuda):
+    w = dataclasses.replace(SMALL, seqlen=700, init_state=True, seed=82)
+    dev = to_device(synth.make_scan_inputs(w), cuda)
+    out_t, last_t = ops.scan_fwd(**dev)
+    mis = dict(dev)
+    for k in ("x", "delta", "z"):
+        mis[k] = _misaligned_copy(dev[k], cuda)
+    out_g, last_g = ops.scan_fwd(**mis, out=_misaligned_copy(torch.zeros_like(dev["x"]), cuda))
+    torch.cuda.synchronize()
+    assert rel_err(f64(out_t), f64(out_g)) <= 1e-2
+    assert rel_err(f64(last_t), f64(last_g)) <= 1e-3
