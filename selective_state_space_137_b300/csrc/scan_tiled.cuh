@@ -27,7 +27,16 @@
 #include "scan_generic.cuh"
 #include "tma.cuh"
 
+#ifndef SSM_SCAN_PACKED
+#define SSM_SCAN_PACKED 0     // 1: state pairs in f32x2 registers; 0: scalar fp32
+#endif
+#ifndef SSM_SCAN_UNROLL
+#define SSM_SCAN_UNROLL 2     // time steps unrolled in the scan loop
+#endif
+
 namespace ssm {
+
+constexpr int kScanUnroll = SSM_SCAN_UNROLL;
 
 struct TiledMaps {
     CUtensorMap x, delta, z, B, C, out;
@@ -60,7 +69,7 @@ struct TiledCfg {
     static_assert(N % KS == 0 && NS % 4 == 0, "each thread owns a multiple of 4 states");
     static_assert((DC * ESZ) % 16 == 0 && (N * ESZ) % 16 == 0, "TMA rows are 16-byte multiples");
     static_assert(DC % V == 0 && N % V == 0, "16-byte vectors tile the rows");
-    static_assert(THREADS % (DC / V) == 0, "each thread keeps the same channel vector");
+    static_assert(THREADS % (DC / 2) == 0, "fixed channel pair per thread");
 };
 
 template <typename IO>
@@ -97,6 +106,24 @@ __device__ __forceinline__ uint4 pack<__nv_bfloat16>(const float* f) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Two adjacent io elements as fp32 (one 4- or 8-byte shared load), and back.
+__device__ __forceinline__ float2 load2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 load2(const __nv_bfloat16* p) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ float load1(const float* p) { return *p; }
+__device__ __forceinline__ float load1(const __nv_bfloat16* p) {
+    return __uint_as_float((uint32_t)(*reinterpret_cast<const unsigned short*>(p)) << 16);
+}
+__device__ __forceinline__ void store2(float* p, float lo, float hi) {
+    *reinterpret_cast<float2*>(p) = make_float2(lo, hi);
+}
+__device__ __forceinline__ void store2(__nv_bfloat16* p, float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    *reinterpret_cast<__nv_bfloat162*>(p) = v;
+}
+
 // softplus for the tiled path.  fp32 I/O keeps the accurate libm form; for
 // bf16 I/O: log(1 + e^u) = ln2 * log2(1 + 2^(u log2 e)) on the SFU (relative
 // error of Delta below 1e-3 even where 1 + e^u rounds, far inside the bf16
@@ -107,9 +134,11 @@ template <>
 __device__ __forceinline__ float softplus_tiled<float>(float u) { return softplus_accurate(u); }
 template <>
 __device__ __forceinline__ float softplus_tiled<__nv_bfloat16>(float u) {
+    // softplus(u) >= u, and the formula is exact to fp32 for u <= 80 (the
+    // clamp keeps 2^(u log2 e) finite); above, max() returns u itself.
     float l;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l) : "f"(1.f + ex2_sfu(u * kLog2e)));
-    return u > 20.f ? u : l * kLn2;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l) : "f"(1.f + ex2_sfu(fminf(u, 80.f) * kLog2e)));
+    return fmaxf(u, l * kLn2);
 }
 
 template <typename IO>
@@ -199,14 +228,19 @@ __global__ void __launch_bounds__(Cfg::THREADS)
 #pragma unroll
         for (int j = 0; j < NS; ++j) h[j] = 0.f;
     }
-    // pre/post-pass: this thread always handles the same V channels
-    const int vc = (tid % (DC / V)) * V;
-    float bias[V], dsk[V];
+    // pre- and post-pass: this thread always handles the channel pair `qc`, `qc+1`
+    const int qc = (tid % (DC / 2)) * 2;
+    const float2 bias2 =
+        make_float2((p.delta_bias && d0 + qc < p.dim) ? __ldg(p.delta_bias + d0 + qc) : 0.f,
+                    (p.delta_bias && d0 + qc + 1 < p.dim) ? __ldg(p.delta_bias + d0 + qc + 1) : 0.f);
+    const float2 dsk2 =
+        make_float2((FULL && p.D && d0 + qc < p.dim) ? __ldg(p.D + d0 + qc) : 0.f,
+                    (FULL && p.D && d0 + qc + 1 < p.dim) ? __ldg(p.D + d0 + qc + 1) : 0.f);
+    float2 a2p[NS / 2], hp[NS / 2];
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-        const int dd_ = d0 + vc + i;
-        bias[i] = (p.delta_bias && dd_ < p.dim) ? __ldg(p.delta_bias + dd_) : 0.f;
-        dsk[i] = (FULL && p.D && dd_ < p.dim) ? __ldg(p.D + dd_) : 0.f;
+    for (int q = 0; q < NS / 2; ++q) {
+        a2p[q] = make_float2(a2[2 * q], a2[2 * q + 1]);
+        hp[q] = make_float2(h[2 * q], h[2 * q + 1]);
     }
     float dsum = 0.f;
     int failed = -1;   // tile whose wait gave up
@@ -220,22 +254,22 @@ __global__ void __launch_bounds__(Cfg::THREADS)
         const bool got = mbar_wait_bounded(&bar[st], (uint32_t)((j / S) & 1));
         if (__syncthreads_or(!got)) { failed = j; break; }
 
-        // ---- pre-pass: (Delta, Delta*x) per token, B and C to fp32
+        // ---- pre-pass: (Delta, Delta*x) per token, B and C to fp32.  Lanes take
+        // consecutive channel pairs of a row: conflict-free 16-byte stores.
         const IO* xs = reinterpret_cast<const IO*>(stg + Cfg::OFF_X);
         const IO* ds = reinterpret_cast<const IO*>(stg + Cfg::OFF_DL);
-        for (int g = tid; g < T * DC / V; g += THREADS) {
-            const int t = g / (DC / V);
-            float xv[V], dv[V];
-            unpack<IO>(*reinterpret_cast<const uint4*>(xs + t * DC + vc), xv);
-            unpack<IO>(*reinterpret_cast<const uint4*>(ds + t * DC + vc), dv);
-            float4* out2 = reinterpret_cast<float4*>(dd + t * DC + vc);
-#pragma unroll
-            for (int i = 0; i < V; i += 2) {
-                const float u0 = dv[i] + bias[i], u1 = dv[i + 1] + bias[i + 1];
-                const float t0v = p.softplus ? softplus_tiled<IO>(u0) : u0;
-                const float t1v = p.softplus ? softplus_tiled<IO>(u1) : u1;
-                out2[i / 2] = make_float4(t0v, t0v * xv[i], t1v, t1v * xv[i + 1]);
+#pragma unroll 4
+        for (int g = tid; g < T * DC / 2; g += THREADS) {
+            const int o = (g / (DC / 2)) * DC + qc;
+            const float2 xv = load2(xs + o);
+            const float2 u = __fadd2_rn(load2(ds + o), bias2);
+            float d0v = u.x, d1v = u.y;
+            if (p.softplus) {
+                d0v = softplus_tiled<IO>(d0v);
+                d1v = softplus_tiled<IO>(d1v);
             }
+            const float2 dx = __fmul2_rn(make_float2(d0v, d1v), xv);
+            *reinterpret_cast<float4*>(dd + o) = make_float4(d0v, dx.x, d1v, dx.y);
         }
         {
             const IO* Bs = reinterpret_cast<const IO*>(stg + Cfg::OFF_B);
@@ -255,63 +289,84 @@ __global__ void __launch_bounds__(Cfg::THREADS)
 
         // ---- scan over the tile
         float* ys = yp + s * Cfg::YP_STRIDE;
-#pragma unroll 2
+#pragma unroll kScanUnroll
         for (int t = 0; t < steps; ++t) {
-            const float2 dv = dd[t * DC + c];
-            const float* row = bc + t * 2 * N;
+            const float2 dq = dd[t * DC + c];             // (Delta, Delta*x)
+            const float* row = bc + t * 2 * N + s * NS;
+#if SSM_SCAN_PACKED
+            // pairs of states in float2 registers (f32x2 FMA/MUL)
+            const float2 dl2 = make_float2(dq.x, dq.x);
+            const float2 dx2 = make_float2(dq.y, dq.y);
+            float2 y2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < NS / 2; q += 2) {
+                const float4 b4 = *reinterpret_cast<const float4*>(row + 2 * q);
+                float4 c4;
+                if (FULL) c4 = *reinterpret_cast<const float4*>(row + N + 2 * q);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float2 arg = __fmul2_rn(dl2, a2p[q + r]);
+                    const float2 dA = make_float2(ex2_sfu(arg.x), ex2_sfu(arg.y));
+                    const float2 bb = r ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+                    hp[q + r] = __ffma2_rn(dA, hp[q + r], __fmul2_rn(dx2, bb));
+                    if (FULL) {
+                        const float2 cc = r ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
+                        y2 = __ffma2_rn(cc, hp[q + r], y2);
+                    }
+                }
+            }
+            const float yv = y2.x + y2.y;
+#else
             float Bv[NS], Cv[NS];
 #pragma unroll
             for (int q = 0; q < NS; q += 4) {
-                const float4 b4 = *reinterpret_cast<const float4*>(row + s * NS + q);
+                const float4 b4 = *reinterpret_cast<const float4*>(row + q);
                 Bv[q] = b4.x; Bv[q + 1] = b4.y; Bv[q + 2] = b4.z; Bv[q + 3] = b4.w;
                 if (FULL) {
-                    const float4 c4 = *reinterpret_cast<const float4*>(row + N + s * NS + q);
+                    const float4 c4 = *reinterpret_cast<const float4*>(row + N + q);
                     Cv[q] = c4.x; Cv[q + 1] = c4.y; Cv[q + 2] = c4.z; Cv[q + 3] = c4.w;
                 }
             }
-            float y0 = 0.f, y1 = 0.f;
+            float ya = 0.f, yb = 0.f;
 #pragma unroll
             for (int q = 0; q < NS; ++q) {
-                const float dA = ex2_sfu(dv.x * a2[q]);
-                h[q] = fmaf(dA, h[q], dv.y * Bv[q]);
+                float& hq = (q & 1) ? hp[q / 2].y : hp[q / 2].x;
+                const float a = (q & 1) ? a2p[q / 2].y : a2p[q / 2].x;
+                const float dA = ex2_sfu(dq.x * a);
+                hq = fmaf(dA, hq, dq.y * Bv[q]);
                 if (FULL) {
-                    if (q & 1) y1 = fmaf(Cv[q], h[q], y1);
-                    else y0 = fmaf(Cv[q], h[q], y0);
+                    if (q & 1) yb = fmaf(Cv[q], hq, yb);
+                    else ya = fmaf(Cv[q], hq, ya);
                 }
             }
-            if (FULL) ys[t * DC + c] = y0 + y1;
-            else dsum += dv.x;
+            const float yv = ya + yb;
+#endif
+            if (FULL) ys[t * DC + c] = yv;
+            else dsum += dq.x;
         }
 
         if (FULL) {
             if (tid == 0) bulk_wait_read<1>();   // the store that last used ob[j & 1] has read it
             __syncthreads();
-            // ---- post-pass: skip, gate, cast, into the out tile
+            // ---- post-pass: skip, gate, cast, into the out tile (channel pairs)
             const IO* zs = reinterpret_cast<const IO*>(stg + Cfg::OFF_Z);
             IO* ob = reinterpret_cast<IO*>(smem + Cfg::OFF_OB + (j & 1) * Cfg::TOK_BYTES);
-            for (int g = tid; g < T * DC / V; g += THREADS) {
-                const int t = g / (DC / V);
-                float xv[V], yv[V], zv[V];
-                unpack<IO>(*reinterpret_cast<const uint4*>(xs + t * DC + vc), xv);
-                if (z_on) unpack<IO>(*reinterpret_cast<const uint4*>(zs + t * DC + vc), zv);
+#pragma unroll 2
+            for (int g = tid; g < T * DC / 2; g += THREADS) {
+                const int t = g / (DC / 2);
+                const int o = t * DC + qc;
+                float2 y = *reinterpret_cast<const float2*>(yp + o);
 #pragma unroll
-                for (int i = 0; i < V; i += 4) {
-                    float4 acc = *reinterpret_cast<const float4*>(yp + t * DC + vc + i);
-#pragma unroll
-                    for (int q = 1; q < KS; ++q) {
-                        const float4 o = *reinterpret_cast<const float4*>(
-                            yp + q * Cfg::YP_STRIDE + t * DC + vc + i);
-                        acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
-                    }
-                    yv[i] = acc.x; yv[i + 1] = acc.y; yv[i + 2] = acc.z; yv[i + 3] = acc.w;
+                for (int q = 1; q < KS; ++q)
+                    y = __fadd2_rn(y, *reinterpret_cast<const float2*>(yp + q * Cfg::YP_STRIDE + o));
+                y = __ffma2_rn(dsk2, load2(xs + o), y);
+                float y0 = y.x, y1 = y.y;
+                if (z_on) {
+                    const float2 zv = load2(zs + o);
+                    y0 *= silu_tiled<IO>(zv.x);
+                    y1 *= silu_tiled<IO>(zv.y);
                 }
-#pragma unroll
-                for (int i = 0; i < V; ++i) {
-                    float y = fmaf(dsk[i], xv[i], yv[i]);
-                    if (z_on) y *= silu_tiled<IO>(zv[i]);
-                    yv[i] = y;
-                }
-                *reinterpret_cast<uint4*>(ob + t * DC + vc) = pack<IO>(yv);
+                store2(ob + o, y0, y1);
             }
             fence_proxy_async_smem();
         }
@@ -336,19 +391,17 @@ __global__ void __launch_bounds__(Cfg::THREADS)
     }
 
     if (!dval) return;
+    float* dst = nullptr;
     if (FULL) {
-        if (p.last_state && k == p.nchunk - 1) {
-#pragma unroll
-            for (int q = 0; q < NS; q += 4)
-                *reinterpret_cast<float4*>(p.last_state + chan * N + s * NS + q) =
-                    make_float4(h[q], h[q + 1], h[q + 2], h[q + 3]);
-        }
+        if (p.last_state && k == p.nchunk - 1) dst = p.last_state + chan * N + s * NS;
     } else {
-        float* cend = p.carry + (((int64_t)b * p.nchunk + k) * p.dim + d) * N + s * NS;
-#pragma unroll
-        for (int q = 0; q < NS; q += 4)
-            *reinterpret_cast<float4*>(cend + q) = make_float4(h[q], h[q + 1], h[q + 2], h[q + 3]);
+        dst = p.carry + (((int64_t)b * p.nchunk + k) * p.dim + d) * N + s * NS;
         if (s == 0) p.dsum[((int64_t)b * p.nchunk + k) * p.dim + d] = dsum;
+    }
+    if (dst) {
+#pragma unroll
+        for (int q = 0; q < NS / 2; q += 2)
+            *reinterpret_cast<float4*>(dst + 2 * q) = make_float4(hp[q].x, hp[q].y, hp[q + 1].x, hp[q + 1].y);
     }
 }
 

@@ -128,13 +128,29 @@ cudaError_t dispatch_decode(int64_t n, const DecodeParams& p, cudaStream_t s) {
 // are 16-byte multiples and 16-byte aligned tensors.
 
 constexpr int kPlanSMs = 148;        // the plan is fixed for a 148-SM B300
-constexpr int kTileT = 32;           // time steps per tile
-constexpr int kStages = 3;           // TMA ring depth
+// Tile shape (compile-time; the defaults are the tuned ones).
+#ifndef SSM_TILE_T
+#define SSM_TILE_T 32        // time steps per tile
+#endif
+#ifndef SSM_TILE_STAGES
+#define SSM_TILE_STAGES 3    // TMA ring depth
+#endif
+#ifndef SSM_STAGES16
+#define SSM_STAGES16 2       // TMA ring depth for dstate 16 (keeps 7 CTAs per SM)
+#endif
+#ifndef SSM_KS16
+#define SSM_KS16 4           // state slices per channel for dstate 16
+#endif
+#ifndef SSM_DC16
+#define SSM_DC16 16          // channels per CTA for dstate 16
+#endif
+constexpr int kTileT = SSM_TILE_T;
+constexpr int kStages = SSM_TILE_STAGES;
 
 template <typename IO, int N>
-struct TiledFor;   // (KS, DC) per dstate: 8 states per thread, 32-64 threads per CTA
+struct TiledFor;   // (KS, DC) per dstate
 template <typename IO> struct TiledFor<IO, 8>  { using Cfg = ssm::TiledCfg<IO, 8, 1, 32, kTileT, kStages>; };
-template <typename IO> struct TiledFor<IO, 16> { using Cfg = ssm::TiledCfg<IO, 16, 2, 16, kTileT, kStages>; };
+template <typename IO> struct TiledFor<IO, 16> { using Cfg = ssm::TiledCfg<IO, 16, SSM_KS16, SSM_DC16, kTileT, SSM_STAGES16>; };
 template <typename IO> struct TiledFor<IO, 32> { using Cfg = ssm::TiledCfg<IO, 32, 4, 16, kTileT, kStages>; };
 
 struct TiledShape { int dc, threads, smem; };
