@@ -15,6 +15,7 @@
 #include "decode.cuh"
 #include "scan_generic.cuh"
 #include "scan_tiled.cuh"
+#include "scan_ws.cuh"
 
 namespace {
 
@@ -165,7 +166,31 @@ TiledShape tiled_shape_io(int64_t n) {
     return {0, 0, 0};
 }
 
+// Path 2 (warp-specialised: helper warp for loads and per-token work, scan
+// warp for the recurrence): dstate 16, bf16 or fp32 I/O.
+#ifndef SSM_USE_WS
+#define SSM_USE_WS 1
+#endif
+#ifndef SSM_WS_T
+#define SSM_WS_T 16          // time steps per tile
+#endif
+#ifndef SSM_WS_STAGES
+#define SSM_WS_STAGES 3      // TMA ring depth
+#endif
+#ifndef SSM_WS_SLOTS
+#define SSM_WS_SLOTS 2       // helper <-> scan hand-over slots
+#endif
+template <typename IO>
+using WsConfig = ssm::WsCfg<IO, SSM_WS_T, SSM_WS_STAGES, SSM_WS_SLOTS>;
+
+bool ws_path(const ssm_scan_desc* d) { return SSM_USE_WS && d->dstate == 16; }
+
 TiledShape tiled_shape(const ssm_scan_desc* d) {
+    if (ws_path(d))
+        return d->io_dtype == SSM_DTYPE_F32
+                   ? TiledShape{WsConfig<float>::DC, WsConfig<float>::THREADS, WsConfig<float>::SMEM}
+                   : TiledShape{WsConfig<__nv_bfloat16>::DC, WsConfig<__nv_bfloat16>::THREADS,
+                                WsConfig<__nv_bfloat16>::SMEM};
     return d->io_dtype == SSM_DTYPE_F32 ? tiled_shape_io<float>(d->dstate)
                                         : tiled_shape_io<__nv_bfloat16>(d->dstate);
 }
@@ -266,6 +291,38 @@ cudaError_t launch_tiled(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
 }
 
 template <typename IO>
+cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
+    using Cfg = WsConfig<IO>;
+    const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int e = (int)sizeof(IO);
+    ssm::TiledMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    bool ok = encode_3d(&maps.x, p.x, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+              encode_3d(&maps.delta, p.delta, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+              encode_3d(&maps.B, p.B, dt, e, Cfg::N, d->seqlen, d->batch, Cfg::N, Cfg::T) &&
+              encode_3d(&maps.C, p.C, dt, e, Cfg::N, d->seqlen, d->batch, Cfg::N, Cfg::T) &&
+              encode_3d(&maps.out, p.out, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+    if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+    if (!ok) return cudaErrorInvalidValue;
+    auto kfull = ssm::scan_ws_kernel<IO, Cfg, ssm::MODE_FULL>;
+    auto kagg = ssm::scan_ws_kernel<IO, Cfg, ssm::MODE_AGG>;
+    cudaError_t err = cudaFuncSetAttribute(kfull, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(kagg, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (err != cudaSuccess) return err;
+    const unsigned gx = (unsigned)((d->dim + Cfg::DC - 1) / Cfg::DC);
+    if (p.nchunk > 1) {
+        kagg<<<dim3(gx, (unsigned)d->batch, (unsigned)(p.nchunk - 1)), Cfg::THREADS, Cfg::SMEM, s>>>(maps, p);
+        const int64_t total = p.batch * p.dim * Cfg::N;
+        ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+            p.A, p.initial_state, p.carry, p.dsum, p.batch, p.dim, Cfg::N, p.nchunk);
+    }
+    kfull<<<dim3(gx, (unsigned)d->batch, (unsigned)p.nchunk), Cfg::THREADS, Cfg::SMEM, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+template <typename IO>
 cudaError_t dispatch_tiled(const ssm_scan_desc* d, const ScanParams& p, cudaStream_t s) {
     switch (d->dstate) {
         case 8: return launch_tiled<IO, 8>(d, p, s);
@@ -304,7 +361,7 @@ ssm_status ssm_scan_plan(const ssm_scan_desc* desc, ssm_scan_plan_info* info) {
     } else {
         nchunk = generic_nchunk(desc);
     }
-    info->path = tiled ? 1 : 0;
+    info->path = tiled ? (ws_path(desc) ? 2 : 1) : 0;
     info->nchunk = nchunk;
     info->launches = (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) ? 0
                      : (nchunk > 1 ? 3 : 1);
@@ -393,7 +450,10 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
     if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
 
     cudaError_t e;
-    if (tiled)
+    if (tiled && ws_path(desc))
+        e = desc->io_dtype == SSM_DTYPE_F32 ? launch_ws<float>(desc, p, s)
+                                            : launch_ws<__nv_bfloat16>(desc, p, s);
+    else if (tiled)
         e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_tiled<float>(desc, p, s)
                                             : dispatch_tiled<__nv_bfloat16>(desc, p, s);
     else
