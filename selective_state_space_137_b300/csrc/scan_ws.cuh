@@ -34,6 +34,9 @@
 #ifndef SSM_WS_UNROLL
 #define SSM_WS_UNROLL 4      // time steps unrolled in the scan warp's loop
 #endif
+#ifndef SSM_WS_PIPE
+#define SSM_WS_PIPE 1        // 1: software-pipelined scan loop (decays one step ahead)
+#endif
 
 namespace ssm {
 
@@ -267,6 +270,60 @@ __global__ void __launch_bounds__(64)
         float* ys = reinterpret_cast<float*>(const_cast<unsigned char*>(slot) + Cfg::SL_YP) + s * Cfg::YP_STRIDE;
         const int t0 = (int)(t_begin + (int64_t)j * T);
         const int steps = (int)((t_end - t0) < T ? (t_end - t0) : T);
+#if SSM_WS_PIPE
+        // Software-pipelined: the operands and decays of step t+1 are loaded
+        // and computed (SFU) while step t's state update and readout run.
+        float2 cur_dq = dd[c];
+        float4 cur_b[2], cur_c[2];
+        float2 cur_dA[NS / 2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            cur_b[q] = *reinterpret_cast<const float4*>(bc + s * NS + 4 * q);
+            if (FULL) cur_c[q] = *reinterpret_cast<const float4*>(bc + N + s * NS + 4 * q);
+        }
+#pragma unroll
+        for (int q = 0; q < NS / 2; ++q) {
+            const float2 arg = __fmul2_rn(make_float2(cur_dq.x, cur_dq.x), a2[q]);
+            cur_dA[q] = make_float2(ex2_sfu(arg.x), ex2_sfu(arg.y));
+        }
+#pragma unroll 2
+        for (int t = 0; t < steps; ++t) {
+            const int tn = t + 1 < steps ? t + 1 : t;
+            const float2 nxt_dq = dd[tn * DC + c];
+            float4 nxt_b[2], nxt_c[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                nxt_b[q] = *reinterpret_cast<const float4*>(bc + tn * 2 * N + s * NS + 4 * q);
+                if (FULL) nxt_c[q] = *reinterpret_cast<const float4*>(bc + tn * 2 * N + N + s * NS + 4 * q);
+            }
+            float2 nxt_dA[NS / 2];
+#pragma unroll
+            for (int q = 0; q < NS / 2; ++q) {
+                const float2 arg = __fmul2_rn(make_float2(nxt_dq.x, nxt_dq.x), a2[q]);
+                nxt_dA[q] = make_float2(ex2_sfu(arg.x), ex2_sfu(arg.y));
+            }
+            const float2 dx2 = make_float2(cur_dq.y, cur_dq.y);
+            float2 y2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < NS / 2; ++q) {
+                const float4 b4 = cur_b[q / 2];
+                const float2 bb = (q & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+                h[q] = __ffma2_rn(cur_dA[q], h[q], __fmul2_rn(dx2, bb));
+                if (FULL) {
+                    const float4 c4 = cur_c[q / 2];
+                    const float2 cc = (q & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
+                    y2 = __ffma2_rn(cc, h[q], y2);
+                }
+            }
+            if (FULL) ys[t * DC + c] = y2.x + y2.y;
+            else dsum += cur_dq.x;
+            cur_dq = nxt_dq;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) { cur_b[q] = nxt_b[q]; cur_c[q] = nxt_c[q]; }
+#pragma unroll
+            for (int q = 0; q < NS / 2; ++q) cur_dA[q] = nxt_dA[q];
+        }
+#else
 #pragma unroll kWsUnroll
         for (int t = 0; t < steps; ++t) {
             const float2 dq = dd[t * DC + c];
@@ -298,6 +355,7 @@ __global__ void __launch_bounds__(64)
                 dsum += dq.x;
             }
         }
+#endif
         mbar_arrive(&done[i]);
     }
     if (!ok || !dval) return;

@@ -175,7 +175,7 @@ TiledShape tiled_shape_io(int64_t n) {
 #define SSM_WS_T 16          // time steps per tile
 #endif
 #ifndef SSM_WS_STAGES
-#define SSM_WS_STAGES 3      // TMA ring depth
+#define SSM_WS_STAGES 4      // TMA ring depth
 #endif
 #ifndef SSM_WS_SLOTS
 #define SSM_WS_SLOTS 2       // helper <-> scan hand-over slots
