@@ -9,6 +9,7 @@
 // run of the state with 128-bit accesses (SPL = 4).
 #pragma once
 #include "common.cuh"
+#include "scan_tiled.cuh"   // softplus_tiled / silu_tiled
 
 namespace ssm {
 
@@ -33,17 +34,50 @@ struct DecodeShape {
     static constexpr int SPL = N / LPC;                               // states per lane
 };
 
+// SPL consecutive io elements as fp32 (16-, 8- or 4-byte loads when SPL allows).
+template <int SPL>
+__device__ __forceinline__ void load_vec(const float* p, float* f) {
+    if (SPL % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < SPL; j += 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(p + j));
+            f[j] = v.x; f[j + 1] = v.y; f[j + 2] = v.z; f[j + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) f[j] = __ldg(p + j);
+    }
+}
+template <int SPL>
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f) {
+    if (SPL % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < SPL; j += 4) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(p + j));
+            f[j] = __uint_as_float(v.x << 16); f[j + 1] = __uint_as_float(v.x & 0xffff0000u);
+            f[j + 2] = __uint_as_float(v.y << 16); f[j + 3] = __uint_as_float(v.y & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) f[j] = load_f32(p + j);
+    }
+}
+
+// Grid: x covers the channels of one sequence (LPC lanes per channel, 256
+// threads per block), y is the sequence.  Each thread loads its 16-byte slice
+// of the state, the matching A row slice and B/C slices with vector loads, and
+// the channel's x, delta, z; no integer division is needed to locate them.
 template <typename IO, int N>
-__global__ void __launch_bounds__(256) state_update_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(256, 8) state_update_kernel(DecodeParams p) {
     constexpr int LPC = DecodeShape<N>::LPC;
     constexpr int SPL = DecodeShape<N>::SPL;
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t chan = gid / LPC;            // (b, d) flattened
-    const int sub = (int)(gid % LPC);
-    const bool valid = chan < p.batch * p.dim;
-    const int64_t c = valid ? chan : 0;         // keep whole lane groups alive for the shuffles
-    const int64_t b = c / p.dim;
-    const int64_t d = c % p.dim;
+    const int lin = blockIdx.x * blockDim.x + threadIdx.x;    // lane index within the sequence
+    const int64_t b = blockIdx.y;
+    const int d_raw = lin / LPC;                                // LPC is a power of two
+    const int sub = lin % LPC;
+    const bool valid = d_raw < p.dim;
+    const int d = valid ? d_raw : 0;                            // whole lane groups stay for the shuffles
+    const int64_t ch = b * p.dim + d;
 
     const IO* x = static_cast<const IO*>(p.x);
     const IO* dl = static_cast<const IO*>(p.delta);
@@ -51,8 +85,8 @@ __global__ void __launch_bounds__(256) state_update_kernel(DecodeParams p) {
     const IO* Cm = static_cast<const IO*>(p.C);
     const IO* z = static_cast<const IO*>(p.z);
 
-    float* st = p.state + c * N + sub * SPL;
-    float h[SPL];
+    float h[SPL], a[SPL], bv[SPL], cv[SPL];
+    float* st = p.state + ch * N + sub * SPL;
     if (SPL % 4 == 0) {
 #pragma unroll
         for (int j = 0; j < SPL; j += 4) {
@@ -63,22 +97,25 @@ __global__ void __launch_bounds__(256) state_update_kernel(DecodeParams p) {
 #pragma unroll
         for (int j = 0; j < SPL; ++j) h[j] = st[j];
     }
+    load_vec<SPL>(p.A + (int64_t)d * N + sub * SPL, a);
+    load_vec<SPL>(Bm + b * N + sub * SPL, bv);
+    load_vec<SPL>(Cm + b * N + sub * SPL, cv);
+    const float xv = load_f32(x + ch);
+    const float u = load_f32(dl + ch) + (p.delta_bias ? __ldg(p.delta_bias + d) : 0.f);
+    const float zv = z ? load_f32(z + ch) : 0.f;
+    const float dsk = p.D ? __ldg(p.D + d) : 0.f;
 
-    const float xv = load_f32(x + c);
-    const float u = load_f32(dl + c) + (p.delta_bias ? __ldg(p.delta_bias + d) : 0.f);
-    const float dt = p.softplus ? softplus_accurate(u) : u;
+    const float dt = p.softplus ? softplus_tiled<IO>(u) : u;
     const float dx = dt * xv;
     float y = 0.f;
 #pragma unroll
     for (int j = 0; j < SPL; ++j) {
-        const int n = sub * SPL + j;
-        const float dA = ex2_sfu(dt * (__ldg(p.A + d * N + n) * kLog2e));
-        h[j] = fmaf(dA, h[j], dx * load_f32(Bm + b * N + n));
-        y = fmaf(load_f32(Cm + b * N + n), h[j], y);
+        const float dA = ex2_sfu(dt * (a[j] * kLog2e));
+        h[j] = fmaf(dA, h[j], dx * bv[j]);
+        y = fmaf(cv[j], h[j], y);
     }
 #pragma unroll
     for (int off = LPC / 2; off > 0; off >>= 1) y += __shfl_xor_sync(0xffffffffu, y, off);
-
     if (!valid) return;
     if (SPL % 4 == 0) {
 #pragma unroll
@@ -89,9 +126,9 @@ __global__ void __launch_bounds__(256) state_update_kernel(DecodeParams p) {
         for (int j = 0; j < SPL; ++j) st[j] = h[j];
     }
     if (sub == 0) {
-        y = fmaf(p.D ? __ldg(p.D + d) : 0.f, xv, y);
-        if (z) y *= silu_accurate(load_f32(z + c));
-        store_io(static_cast<IO*>(p.out) + c, y);
+        y = fmaf(dsk, xv, y);
+        if (z) y *= silu_tiled<IO>(zv);
+        store_io(static_cast<IO*>(p.out) + ch, y);
     }
 }
 

@@ -103,9 +103,9 @@ cudaError_t dispatch_generic(int64_t n, const ScanParams& p, cudaStream_t s) {
 
 template <typename IO, int N>
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
-    const int64_t threads = p.batch * p.dim * ssm::DecodeShape<N>::LPC;
-    const unsigned blocks = (unsigned)((threads + 255) / 256);
-    ssm::state_update_kernel<IO, N><<<blocks, 256, 0, s>>>(p);
+    const int64_t lanes = p.dim * ssm::DecodeShape<N>::LPC;   // per sequence
+    const dim3 grid((unsigned)((lanes + 255) / 256), (unsigned)p.batch);
+    ssm::state_update_kernel<IO, N><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -488,6 +488,8 @@ ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void*
         return SSM_ERR_INVALID_ARG;
     if (desc->batch == 0 || desc->dim == 0) return SSM_OK;
     if (!state || !x || !delta || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
+    // grid: y = sequence (<= 65535), x = channel lanes (32-bit lane index)
+    if (desc->batch > 65535 || desc->dim * 64 >= ((int64_t)1 << 31)) return SSM_ERR_UNSUPPORTED;
 
     DecodeParams p;
     p.state = state; p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
