@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target wall time of the oracle sample")
+    ap.add_argument("--only", choices=["all", "scan", "decode"], default="all",
+                    help="run only the prefill scan part or only the decode part (profiling)")
     return ap.parse_args()
 
 
@@ -182,13 +184,21 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(v, world, device):
+def max_over_ranks(v, world, device=None):
+    """Max of a per-rank scalar over all ranks (timing: the job takes as long
+    as its slowest rank).  A scalar all-reduce, not a data-path collective."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device=device)
+    t = torch.tensor([v], dtype=torch.float64, device=device if device is not None else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank_step, steps, max_total_ms):
+    """Weak scaling: every rank processes its own batch, so the job's
+    throughput is all ranks' units over the slowest rank's time."""
+    return world * units_per_rank_step * steps / (max_total_ms * 1e-3)
 
 
 # ----------------------------------------------------------------------------- oracle sample
@@ -277,6 +287,12 @@ def run_ours(args, world, rank, local):
 
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
+    if args.only == "decode":
+        peak, peak_kind = peaks()
+        line = {"decode": run_decode(args, dev, peak, peak_kind), "source_hash": kernel_source_hash()}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     w = workload_by_name(args.workload)
     import dataclasses
     wr = dataclasses.replace(w, seed=w.seed + 1000 * rank) if rank else w
@@ -314,7 +330,7 @@ def run_ours(args, world, rank, local):
     total_ms = ev[0].elapsed_time(ev[-1])
     total_ms = max_over_ranks(total_ms, world, dev)
     ms = total_ms / args.steps
-    value = world * w.tokens * args.steps / (total_ms * 1e-3)
+    value = whole_job_rate(world, w.tokens, args.steps, total_ms)
 
     peak, peak_kind = peaks()
     kernel_ms = float(np.mean(per))
@@ -345,7 +361,7 @@ def run_ours(args, world, rank, local):
 
     if not args.no_e2e:
         line["e2e"] = run_e2e(args, w, inp, desc, plan, dev, world, binding)
-    if not args.no_decode:
+    if not args.no_decode and args.only == "all":
         line["decode"] = run_decode(args, dev, peak, peak_kind)
     if rank == 0 and world == 1 and not args.no_cpu:
         val, dt, nchan, cores = time_oracle(inp, w, args.cpu_seconds)
@@ -397,7 +413,7 @@ def run_e2e(args, w, inp, desc, plan, dev, world, binding):
     b.record(stream)
     torch.cuda.synchronize(dev)
     total = max_over_ranks(a.elapsed_time(b), world, dev)
-    return {"value": world * w.tokens * steps / (total * 1e-3), "unit": UNIT,
+    return {"value": whole_job_rate(world, w.tokens, steps, total), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": total / steps}
 

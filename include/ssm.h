@@ -180,6 +180,13 @@ SSM_API ssm_status ssm_scan_plan(const ssm_scan_desc *desc, ssm_scan_plan_info *
  * Synchronises with the device (it waits for all prior work). */
 SSM_API ssm_status ssm_get_device_status(void);
 
+/* Test hook for the timeout path: launches one warp that waits, for at most
+ * `limit_ns` nanoseconds (1e3 .. 5e9), on a shared-memory barrier that nothing
+ * completes.  The wait gives up, the kernel returns normally, and the next
+ * ssm_get_device_status() reports SSM_ERR_TIMEOUT.  No GPU fault or hang is
+ * involved.  The pages have no counterpart to this entry point. */
+SSM_API ssm_status ssm_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
 /* Static description of a status code (never NULL). */
 SSM_API const char *ssm_status_string(ssm_status status);
 

@@ -20,7 +20,7 @@ SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 # Every symbol include/ssm.h declares; the CPU tests check the library exports them.
 EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
             "ssm_scan_plan", "ssm_status_string", "ssm_version", "ssm_scan_fwd_noalloc",
-            "ssm_get_device_status")
+            "ssm_get_device_status", "ssm_selftest_wait_timeout")
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -58,6 +58,8 @@ def _load():
     lib.ssm_scan_fwd_noalloc.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, vp]
     lib.ssm_scan_plan.restype = ctypes.c_int
     lib.ssm_scan_plan.argtypes = [dp, ctypes.POINTER(ssm_scan_plan_info)]
+    lib.ssm_selftest_wait_timeout.restype = ctypes.c_int
+    lib.ssm_selftest_wait_timeout.argtypes = [ctypes.c_int64, vp]
     lib.ssm_get_device_status.restype = ctypes.c_int
     lib.ssm_get_device_status.argtypes = []
     lib.ssm_status_string.restype = ctypes.c_char_p
@@ -76,6 +78,10 @@ def ssm_status_string(status: int) -> str:
 
 def ssm_get_device_status() -> int:
     return lib.ssm_get_device_status()
+
+
+def ssm_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return lib.ssm_selftest_wait_timeout(int(limit_ns), _stream(stream))
 
 
 def ssm_version() -> int:

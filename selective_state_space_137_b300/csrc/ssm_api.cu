@@ -16,6 +16,7 @@
 #include "scan_generic.cuh"
 #include "scan_tiled.cuh"
 #include "scan_ws.cuh"
+#include "selftest.cuh"
 
 namespace {
 
@@ -460,6 +461,12 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
         e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_generic<float>(N, p, s)
                                             : dispatch_generic<__nv_bfloat16>(N, p, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+    if (limit_ns < 1000 || limit_ns > 5000000000LL) return SSM_ERR_INVALID_ARG;
+    ssm::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>((uint64_t)limit_ns);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status ssm_get_device_status(void) {
