@@ -37,6 +37,12 @@
 #ifndef SSM_WS_PIPE
 #define SSM_WS_PIPE 1        // 1: software-pipelined scan loop (decays one step ahead)
 #endif
+#ifndef SSM_WS_FULLUNROLL
+#define SSM_WS_FULLUNROLL 1  // 1: full tiles run a fully unrolled scan (constant offsets)
+#endif
+#ifndef SSM_WS_MINBLOCKS
+#define SSM_WS_MINBLOCKS 7   // resident CTAs per SM the register budget must allow
+#endif
 
 namespace ssm {
 
@@ -69,7 +75,7 @@ struct WsCfg {
 };
 
 template <typename IO, typename Cfg, int MODE>
-__global__ void __launch_bounds__(64)
+__global__ void __launch_bounds__(64, SSM_WS_MINBLOCKS)
     scan_ws_kernel(const __grid_constant__ TiledMaps maps, const ScanParams p) {
     constexpr int N = Cfg::N, NS = Cfg::NS, DC = Cfg::DC, T = Cfg::T, S = Cfg::S, R = Cfg::R;
     constexpr bool FULL = (MODE == MODE_FULL);
@@ -215,6 +221,7 @@ __global__ void __launch_bounds__(64)
                 const IO* Bs = reinterpret_cast<const IO*>(stg + Cfg::OFF_B);
                 const IO* Cs = reinterpret_cast<const IO*>(stg + Cfg::OFF_C);
                 constexpr int V = 16 / Cfg::ESZ;
+#pragma unroll
                 for (int g = lane; g < T * N / V * (FULL ? 2 : 1); g += 32) {
                     const int which = g / (T * N / V);
                     const int e = (g % (T * N / V)) * V;
@@ -270,6 +277,42 @@ __global__ void __launch_bounds__(64)
         float* ys = reinterpret_cast<float*>(const_cast<unsigned char*>(slot) + Cfg::SL_YP) + s * Cfg::YP_STRIDE;
         const int t0 = (int)(t_begin + (int64_t)j * T);
         const int steps = (int)((t_end - t0) < T ? (t_end - t0) : T);
+        // One time step of the recurrence for this lane's 8 states.
+        auto step = [&](int t) {
+            const float2 dq = dd[t * DC + c];
+            const float* row = bc + t * 2 * N + s * NS;
+            const float2 dl2 = make_float2(dq.x, dq.x);
+            const float2 dx2 = make_float2(dq.y, dq.y);
+            float2 y2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < NS / 2; q += 2) {
+                const float4 b4 = *reinterpret_cast<const float4*>(row + 2 * q);
+                float4 c4;
+                if (FULL) c4 = *reinterpret_cast<const float4*>(row + N + 2 * q);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float2 arg = __fmul2_rn(dl2, a2[q + r]);
+                    const float2 dA = make_float2(ex2_sfu(arg.x), ex2_sfu(arg.y));
+                    const float2 bb = r ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
+                    h[q + r] = __ffma2_rn(dA, h[q + r], __fmul2_rn(dx2, bb));
+                    if (FULL) {
+                        const float2 cc = r ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
+                        y2 = __ffma2_rn(cc, h[q + r], y2);
+                    }
+                }
+            }
+            if (FULL) ys[t * DC + c] = y2.x + y2.y;
+            else dsum += dq.x;
+        };
+#if SSM_WS_FULLUNROLL
+        if (steps == T) {
+            // full tile: every offset is a compile-time constant
+#pragma unroll
+            for (int t = 0; t < T; ++t) step(t);
+        } else {
+            for (int t = 0; t < steps; ++t) step(t);
+        }
+#else
 #if SSM_WS_PIPE
         // Software-pipelined: the operands and decays of step t+1 are loaded
         // and computed (SFU) while step t's state update and readout run.
@@ -355,6 +398,7 @@ __global__ void __launch_bounds__(64)
                 dsum += dq.x;
             }
         }
+#endif
 #endif
         mbar_arrive(&done[i]);
     }
