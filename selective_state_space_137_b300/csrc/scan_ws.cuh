@@ -1,26 +1,30 @@
 // scan_ws.cuh -- warp-specialised selective scan (path 2; bf16 or fp32 I/O,
 // dstate 16).
 //
-// A CTA owns 16 channels of one sequence and two warps:
-//   helper warp: issues the TMA loads of x, delta, z, B, C tiles (T steps),
-//     computes per token (Delta, Delta*x) and widens B, C to fp32 (pre-pass),
-//     then, once the scan has produced a tile's partial readouts, applies
-//     skip + silu gate, casts, and TMA-stores the output tile (post-pass);
-//   scan warp: lane (c, s) = (lane % 16, lane / 16) keeps states
-//     [8s, 8s+8) of channel c in registers and runs, step after step,
+// A CTA owns 16 channels of one sequence and three warps:
+//   warp 0, scan: lane (c, s) = (lane % 16, lane / 16) keeps states [8s, 8s+8)
+//     of channel c in registers and runs, step after step,
 //       dA = 2^(Delta * A[n] log2 e)   h = dA h + (Delta x) B[n]   y_s = sum C[n] h
-//     with no block-wide barrier: it only waits for "tile ready" and
-//     signals "readout written" on shared-memory mbarriers.
-// The two warps hand tiles over through a ring of R slots (per slot: the
-// (Delta, Delta*x) tile, the fp32 B/C tile, and the two partial readouts).
-// The per-token work (softplus, skip, gate, conversions) thereby runs beside
-// the recurrence instead of between its tiles.
+//     with f32x2 arithmetic.  It never meets a block-wide barrier: per tile
+//     it waits for "tile ready" and signals "readouts written";
+//   warp 1, pre-pass: per token (Delta, Delta*x) with Delta = softplus(delta +
+//     bias), and B, C widened to fp32, into a ring slot;
+//   warp 2, post-pass: y = (sum of the two partial readouts + D x) silu(z),
+//     cast, TMA store of the output tile; as the last reader of a TMA stage it
+//     also issues the TMA load that refills it.
+// The per-token work (softplus, skip, gate, conversions) thus runs beside the
+// recurrence, on its own warps, instead of between its tiles.
 //
-// Ordering of the ring (slot i = j % R for tile j):
-//   helper: pre(j) -> arrive ready[i] ... wait done[i'] (tile j-1) -> post(j-1)
-//   scan:   wait ready[i] -> scan tile j -> arrive done[i]
-// The helper writes slot i for tile j only after its own post(j-R), which
-// waited for done of tile j-R, so the scan has finished with the slot.
+// Buffers: S TMA stages (x, delta, z, B, C tiles of T steps) and R ring slots
+// (dd = (Delta, Delta*x) tile, fp32 B|C tile, two partial-readout tiles).
+// mbarriers, tile j, stage j % S, slot i = j % R:
+//   full[st]    TMA bytes landed             (post-pass issued the load)
+//   ready[i]    pre-pass wrote slot i         (32 arrivals, warp 1)
+//   done[i]     scan finished with slot i     (32 arrivals, warp 0)
+//   posted[i]   post-pass finished with slot i (32 arrivals, warp 2)
+// The pre-pass writes slot i for tile j only after posted for tile j - R, and
+// the post-pass refills stage st only after its own post(j), the last read of
+// that stage; every wait is on a phase that cannot be overtaken before it.
 //
 // This is the recurrent mode of the selective SSM (stage 2 in
 // "Mamba的三大创新") with the gate and skip of the Mamba block fused in; the
@@ -31,27 +35,16 @@
 #include "scan_tiled.cuh"
 #include "tma.cuh"
 
-#ifndef SSM_WS_UNROLL
-#define SSM_WS_UNROLL 4      // time steps unrolled in the scan warp's loop
-#endif
-#ifndef SSM_WS_PIPE
-#define SSM_WS_PIPE 1        // 1: software-pipelined scan loop (decays one step ahead)
-#endif
-#ifndef SSM_WS_FULLUNROLL
-#define SSM_WS_FULLUNROLL 1  // 1: full tiles run a fully unrolled scan (constant offsets)
-#endif
 #ifndef SSM_WS_MINBLOCKS
 #define SSM_WS_MINBLOCKS 7   // resident CTAs per SM the register budget must allow
 #endif
 
 namespace ssm {
 
-constexpr int kWsUnroll = SSM_WS_UNROLL;
-
 template <typename IO, int T_, int S_, int R_>
 struct WsCfg {
     static constexpr int N = 16, DC = 16, KS = 2, NS = 8, T = T_, S = S_, R = R_;
-    static constexpr int THREADS = 64;
+    static constexpr int THREADS = 96;   // warp 0 scan, warp 1 pre-pass, warp 2 post-pass
     static constexpr int ESZ = (int)sizeof(IO);
     static constexpr int TOK_BYTES = T * DC * ESZ;
     static constexpr int BC_BYTES = T * N * ESZ;
@@ -70,12 +63,11 @@ struct WsCfg {
     static constexpr int OFF_RING = S * STAGE;
     static constexpr int OFF_OB = round_up(OFF_RING + R * SLOT, 128);
     static constexpr int OFF_BAR = round_up(OFF_OB + 2 * TOK_BYTES, 128);
-    // barriers: full[S] (TMA), ready[R] (pre-pass done), done[R] (scan done)
-    static constexpr int SMEM = OFF_BAR + (S + 2 * R) * 8;
+    static constexpr int SMEM = OFF_BAR + (S + 3 * R) * 8;
 };
 
 template <typename IO, typename Cfg, int MODE>
-__global__ void __launch_bounds__(64, SSM_WS_MINBLOCKS)
+__global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
     scan_ws_kernel(const __grid_constant__ TiledMaps maps, const ScanParams p) {
     constexpr int N = Cfg::N, NS = Cfg::NS, DC = Cfg::DC, T = Cfg::T, S = Cfg::S, R = Cfg::R;
     constexpr bool FULL = (MODE == MODE_FULL);
@@ -83,6 +75,7 @@ __global__ void __launch_bounds__(64, SSM_WS_MINBLOCKS)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* ready = full + S;
     uint64_t* done = ready + R;
+    uint64_t* posted = done + R;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -94,47 +87,95 @@ __global__ void __launch_bounds__(64, SSM_WS_MINBLOCKS)
     if (t_end > p.seqlen) t_end = p.seqlen;
     const int ntiles = t_end > t_begin ? (int)((t_end - t_begin + T - 1) / T) : 0;
     const bool z_on = FULL && p.z != nullptr;
+    const uint32_t stage_tx = (uint32_t)(Cfg::TOK_BYTES * (z_on ? 3 : 2) +
+                                         Cfg::BC_BYTES * (FULL ? 2 : 1));
+    auto slot_ptr = [&](int i) { return smem + Cfg::OFF_RING + i * Cfg::SLOT; };
+    auto stage_ptr = [&](int j) { return smem + (j % S) * Cfg::STAGE; };
+    auto issue = [&](int j) {   // TMA loads of tile j into stage j % S (one thread)
+        unsigned char* st = stage_ptr(j);
+        const int t0 = (int)(t_begin + (int64_t)j * T);
+        mbar_arrive_expect_tx(&full[j % S], stage_tx);
+        tma_load_3d(st + Cfg::OFF_X, &maps.x, &full[j % S], d0, t0, b);
+        tma_load_3d(st + Cfg::OFF_DL, &maps.delta, &full[j % S], d0, t0, b);
+        if (z_on) tma_load_3d(st + Cfg::OFF_Z, &maps.z, &full[j % S], d0, t0, b);
+        tma_load_3d(st + Cfg::OFF_B, &maps.B, &full[j % S], 0, t0, b);
+        if (FULL) tma_load_3d(st + Cfg::OFF_C, &maps.C, &full[j % S], 0, t0, b);
+    };
 
-    // Role choice.  An SM issues from four sub-partitions, and a warp's
-    // sub-partition follows its hardware slot (%warpid mod 4).  A two-warp CTA
-    // gets two consecutive slots, so a fixed "warp 1 scans" would put every
-    // scan warp of the SM on two of the four sub-partitions.  Instead the CTA
-    // picks its scan warp from warp 0's slot so that successive CTAs alternate
-    // between the sub-partitions (slot pairs 0-1, 2-3, 4-5, 6-7 scan on 0, 2,
-    // 1, 3).  The rule names exactly one warp whatever the slots are; only the
-    // speed depends on the slot layout.
-    __shared__ unsigned slot_of[2];
-    if (lane == 0) {
-        unsigned wid;
-        asm volatile("mov.u32 %0, %%warpid;" : "=r"(wid));
-        slot_of[warp] = wid;
-    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
         for (int r = 0; r < R; ++r) {
             mbar_init(&ready[r], 32);
             mbar_init(&done[r], 32);
+            mbar_init(&posted[r], 32);
         }
         fence_barrier_init();
     }
     __syncthreads();
-    const unsigned w0 = slot_of[0];
-    const int scan_warp = ((w0 & 1u) == ((w0 >> 2) & 1u)) ? 0 : 1;
+    // Three-warp CTAs take three consecutive hardware warp slots, so warp 0
+    // of successive CTAs falls on successive SM sub-partitions: the scan warps
+    // of an SM spread over all four.
 
-    if (warp != scan_warp) {
-        // ================= helper warp =================
-        const uint32_t stage_tx = (uint32_t)(Cfg::TOK_BYTES * (z_on ? 3 : 2) +
-                                             Cfg::BC_BYTES * (FULL ? 2 : 1));
-        auto issue = [&](int j) {
-            unsigned char* st = smem + (j % S) * Cfg::STAGE;
-            const int t0 = (int)(t_begin + (int64_t)j * T);
-            mbar_arrive_expect_tx(&full[j % S], stage_tx);
-            tma_load_3d(st + Cfg::OFF_X, &maps.x, &full[j % S], d0, t0, b);
-            tma_load_3d(st + Cfg::OFF_DL, &maps.delta, &full[j % S], d0, t0, b);
-            if (z_on) tma_load_3d(st + Cfg::OFF_Z, &maps.z, &full[j % S], d0, t0, b);
-            tma_load_3d(st + Cfg::OFF_B, &maps.B, &full[j % S], 0, t0, b);
-            if (FULL) tma_load_3d(st + Cfg::OFF_C, &maps.C, &full[j % S], 0, t0, b);
-        };
+    // the pre- and post-pass lanes handle the channel pair qc, qc + 1
+    const int qc = (lane % (DC / 2)) * 2;
+
+    if (warp == 1) {
+        // ================= pre-pass warp =================
+        const float2 bias2 = make_float2(
+            (p.delta_bias && d0 + qc < p.dim) ? __ldg(p.delta_bias + d0 + qc) : 0.f,
+            (p.delta_bias && d0 + qc + 1 < p.dim) ? __ldg(p.delta_bias + d0 + qc + 1) : 0.f);
+        for (int j = 0; j < ntiles; ++j) {
+            const int i = j % R;
+            if (j >= R && !mbar_wait_bounded(&posted[i], (uint32_t)(((j - R) / R) & 1))) return;
+            if (!mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1))) return;
+            const unsigned char* stg = stage_ptr(j);
+            unsigned char* slot = slot_ptr(i);
+            float2* dd = reinterpret_cast<float2*>(slot + Cfg::SL_DD);
+            float* bc = reinterpret_cast<float*>(slot + Cfg::SL_BC);
+            const IO* xs = reinterpret_cast<const IO*>(stg + Cfg::OFF_X);
+            const IO* ds = reinterpret_cast<const IO*>(stg + Cfg::OFF_DL);
+#pragma unroll
+            for (int gi = lane; gi < T * DC / 2; gi += 32) {
+                const int o = (gi / (DC / 2)) * DC + qc;
+                const float2 xv = load2(xs + o);
+                const float2 u = __fadd2_rn(load2(ds + o), bias2);
+                float e0 = u.x, e1 = u.y;
+                if (p.softplus) {
+                    e0 = softplus_tiled<IO>(e0);
+                    e1 = softplus_tiled<IO>(e1);
+                }
+                const float2 dx = __fmul2_rn(make_float2(e0, e1), xv);
+                *reinterpret_cast<float4*>(dd + o) = make_float4(e0, dx.x, e1, dx.y);
+            }
+            // B and C widened to fp32 rows [B0..B15 | C0..C15]; lane u writes the
+            // 16-byte chunk u, so a warp store covers 512 consecutive bytes.
+            const IO* Bs = reinterpret_cast<const IO*>(stg + Cfg::OFF_B);
+            const IO* Cs = reinterpret_cast<const IO*>(stg + Cfg::OFF_C);
+            constexpr int CHUNKS = T * 2 * N / 4;
+#pragma unroll
+            for (int u = lane; u < CHUNKS; u += 32) {
+                const int t = u / (2 * N / 4);
+                const int kk = (u % (2 * N / 4)) * 4;
+                if (!FULL && kk >= N) continue;
+                const IO* src = (kk < N ? Bs : Cs) + t * N + (kk % N);
+                float f[4];
+                if (sizeof(IO) == 2) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(src);
+                    f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xffff0000u);
+                    f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xffff0000u);
+                } else {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+                }
+                *reinterpret_cast<float4*>(bc + u * 4) = make_float4(f[0], f[1], f[2], f[3]);
+            }
+            mbar_arrive(&ready[i]);
+        }
+        return;
+    }
+
+    if (warp == 2) {
+        // ================= post-pass warp (and TMA issue) =================
         if (lane == 0) {
             prefetch_tmap(&maps.x);
             prefetch_tmap(&maps.delta);
@@ -146,29 +187,24 @@ __global__ void __launch_bounds__(64, SSM_WS_MINBLOCKS)
             }
             for (int j = 0; j < S && j < ntiles; ++j) issue(j);
         }
-        const int qc = (lane % (DC / 2)) * 2;
-        const float2 bias2 = make_float2(
-            (p.delta_bias && d0 + qc < p.dim) ? __ldg(p.delta_bias + d0 + qc) : 0.f,
-            (p.delta_bias && d0 + qc + 1 < p.dim) ? __ldg(p.delta_bias + d0 + qc + 1) : 0.f);
         const float2 dsk2 =
             make_float2((FULL && p.D && d0 + qc < p.dim) ? __ldg(p.D + d0 + qc) : 0.f,
                         (FULL && p.D && d0 + qc + 1 < p.dim) ? __ldg(p.D + d0 + qc + 1) : 0.f);
+        int issued = ntiles < S ? ntiles : S;
         bool ok = true;
-
-        // post-pass of tile j: skip + gate + cast + TMA store; frees stage j % S
-        auto post = [&](int j) {
+        for (int j = 0; j < ntiles; ++j) {
             const int i = j % R;
-            ok = ok && mbar_wait_bounded(&done[i], (uint32_t)((j / R) & 1));
-            const unsigned char* stg = smem + (j % S) * Cfg::STAGE;
-            const int t0 = (int)(t_begin + (int64_t)j * T);
-            if (FULL && ok) {
-                const float* yp = reinterpret_cast<const float*>(smem + Cfg::OFF_RING + i * Cfg::SLOT + Cfg::SL_YP);
+            if (!mbar_wait_bounded(&done[i], (uint32_t)((j / R) & 1))) { ok = false; break; }
+            if (FULL) {
+                const unsigned char* stg = stage_ptr(j);
+                const int t0 = (int)(t_begin + (int64_t)j * T);
+                const float* yp = reinterpret_cast<const float*>(slot_ptr(i) + Cfg::SL_YP);
                 const IO* xs = reinterpret_cast<const IO*>(stg + Cfg::OFF_X);
                 const IO* zs = reinterpret_cast<const IO*>(stg + Cfg::OFF_Z);
                 IO* ob = reinterpret_cast<IO*>(smem + Cfg::OFF_OB + (j & 1) * Cfg::TOK_BYTES);
                 if (lane == 0) bulk_wait_read<1>();   // the store that last used ob[j & 1]
                 __syncwarp();
-#pragma unroll 4
+#pragma unroll
                 for (int gi = lane; gi < T * DC / 2; gi += 32) {
                     const int o = (gi / (DC / 2)) * DC + qc;
                     float2 y = __fadd2_rn(*reinterpret_cast<const float2*>(yp + o),
@@ -189,58 +225,18 @@ __global__ void __launch_bounds__(64, SSM_WS_MINBLOCKS)
                     bulk_commit();
                 }
             }
+            mbar_arrive(&posted[i]);
             __syncwarp();
-            if (lane == 0 && ok && j + S < ntiles) issue(j + S);   // stage j % S is free again
-        };
-
-        for (int j = 0; j < ntiles && ok; ++j) {
-            const int i = j % R;
-            // the slot's previous tile (j - R) was posted before this point
-            ok = ok && mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1));
-            if (!ok) break;
-            const unsigned char* stg = smem + (j % S) * Cfg::STAGE;
-            unsigned char* slot = smem + Cfg::OFF_RING + i * Cfg::SLOT;
-            float2* dd = reinterpret_cast<float2*>(slot + Cfg::SL_DD);
-            float* bc = reinterpret_cast<float*>(slot + Cfg::SL_BC);
-            const IO* xs = reinterpret_cast<const IO*>(stg + Cfg::OFF_X);
-            const IO* ds = reinterpret_cast<const IO*>(stg + Cfg::OFF_DL);
-#pragma unroll 4
-            for (int gi = lane; gi < T * DC / 2; gi += 32) {
-                const int o = (gi / (DC / 2)) * DC + qc;
-                const float2 xv = load2(xs + o);
-                const float2 u = __fadd2_rn(load2(ds + o), bias2);
-                float e0 = u.x, e1 = u.y;
-                if (p.softplus) {
-                    e0 = softplus_tiled<IO>(e0);
-                    e1 = softplus_tiled<IO>(e1);
-                }
-                const float2 dx = __fmul2_rn(make_float2(e0, e1), xv);
-                *reinterpret_cast<float4*>(dd + o) = make_float4(e0, dx.x, e1, dx.y);
-            }
-            {
-                const IO* Bs = reinterpret_cast<const IO*>(stg + Cfg::OFF_B);
-                const IO* Cs = reinterpret_cast<const IO*>(stg + Cfg::OFF_C);
-                constexpr int V = 16 / Cfg::ESZ;
-#pragma unroll
-                for (int g = lane; g < T * N / V * (FULL ? 2 : 1); g += 32) {
-                    const int which = g / (T * N / V);
-                    const int e = (g % (T * N / V)) * V;
-                    float f[V];
-                    unpack<IO>(*reinterpret_cast<const uint4*>((which ? Cs : Bs) + e), f);
-                    float4* o4 = reinterpret_cast<float4*>(bc + (e / N) * 2 * N + which * N + e % N);
-#pragma unroll
-                    for (int v = 0; v < V; v += 4) o4[v / 4] = make_float4(f[v], f[v + 1], f[v + 2], f[v + 3]);
-                }
-            }
-            mbar_arrive(&ready[i]);          // every helper lane: its writes are published
-            if (j >= 1) post(j - 1);
+            if (lane == 0 && j + S < ntiles) issue(j + S);   // stage j % S is read by no one now
+            if (j + S < ntiles) issued = j + S + 1;
         }
-        if (ok && ntiles > 0) post(ntiles - 1);
-        if (lane == 0) bulk_wait<0>();
-        if (!ok) {
-            // let the loads that were issued land before the CTA's smem goes away
-            if (lane == 0)
-                for (int j = 0; j < ntiles; ++j) mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), 50000000ull);
+        if (lane == 0) {
+            bulk_wait<0>();
+            if (!ok) {
+                // let the last loads issued land before the CTA's shared memory is released
+                for (int j = issued - S > 0 ? issued - S : 0; j < issued; ++j)
+                    mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), 100000000ull);
+            }
         }
         return;
     }
@@ -267,11 +263,10 @@ __global__ void __launch_bounds__(64, SSM_WS_MINBLOCKS)
         h[q] = h0;
     }
     float dsum = 0.f;
-    bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
         const int i = j % R;
-        if (!mbar_wait_bounded(&ready[i], (uint32_t)((j / R) & 1))) { ok = false; break; }
-        const unsigned char* slot = smem + Cfg::OFF_RING + i * Cfg::SLOT;
+        if (!mbar_wait_bounded(&ready[i], (uint32_t)((j / R) & 1))) return;
+        const unsigned char* slot = slot_ptr(i);
         const float2* dd = reinterpret_cast<const float2*>(slot + Cfg::SL_DD);
         const float* bc = reinterpret_cast<const float*>(slot + Cfg::SL_BC);
         float* ys = reinterpret_cast<float*>(const_cast<unsigned char*>(slot) + Cfg::SL_YP) + s * Cfg::YP_STRIDE;
@@ -304,105 +299,16 @@ __global__ void __launch_bounds__(64, SSM_WS_MINBLOCKS)
             if (FULL) ys[t * DC + c] = y2.x + y2.y;
             else dsum += dq.x;
         };
-#if SSM_WS_FULLUNROLL
         if (steps == T) {
-            // full tile: every offset is a compile-time constant
+            // full tile: every shared-memory offset is a compile-time constant
 #pragma unroll
             for (int t = 0; t < T; ++t) step(t);
         } else {
             for (int t = 0; t < steps; ++t) step(t);
         }
-#else
-#if SSM_WS_PIPE
-        // Software-pipelined: the operands and decays of step t+1 are loaded
-        // and computed (SFU) while step t's state update and readout run.
-        float2 cur_dq = dd[c];
-        float4 cur_b[2], cur_c[2];
-        float2 cur_dA[NS / 2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            cur_b[q] = *reinterpret_cast<const float4*>(bc + s * NS + 4 * q);
-            if (FULL) cur_c[q] = *reinterpret_cast<const float4*>(bc + N + s * NS + 4 * q);
-        }
-#pragma unroll
-        for (int q = 0; q < NS / 2; ++q) {
-            const float2 arg = __fmul2_rn(make_float2(cur_dq.x, cur_dq.x), a2[q]);
-            cur_dA[q] = make_float2(ex2_sfu(arg.x), ex2_sfu(arg.y));
-        }
-#pragma unroll 2
-        for (int t = 0; t < steps; ++t) {
-            const int tn = t + 1 < steps ? t + 1 : t;
-            const float2 nxt_dq = dd[tn * DC + c];
-            float4 nxt_b[2], nxt_c[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                nxt_b[q] = *reinterpret_cast<const float4*>(bc + tn * 2 * N + s * NS + 4 * q);
-                if (FULL) nxt_c[q] = *reinterpret_cast<const float4*>(bc + tn * 2 * N + N + s * NS + 4 * q);
-            }
-            float2 nxt_dA[NS / 2];
-#pragma unroll
-            for (int q = 0; q < NS / 2; ++q) {
-                const float2 arg = __fmul2_rn(make_float2(nxt_dq.x, nxt_dq.x), a2[q]);
-                nxt_dA[q] = make_float2(ex2_sfu(arg.x), ex2_sfu(arg.y));
-            }
-            const float2 dx2 = make_float2(cur_dq.y, cur_dq.y);
-            float2 y2 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int q = 0; q < NS / 2; ++q) {
-                const float4 b4 = cur_b[q / 2];
-                const float2 bb = (q & 1) ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
-                h[q] = __ffma2_rn(cur_dA[q], h[q], __fmul2_rn(dx2, bb));
-                if (FULL) {
-                    const float4 c4 = cur_c[q / 2];
-                    const float2 cc = (q & 1) ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
-                    y2 = __ffma2_rn(cc, h[q], y2);
-                }
-            }
-            if (FULL) ys[t * DC + c] = y2.x + y2.y;
-            else dsum += cur_dq.x;
-            cur_dq = nxt_dq;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) { cur_b[q] = nxt_b[q]; cur_c[q] = nxt_c[q]; }
-#pragma unroll
-            for (int q = 0; q < NS / 2; ++q) cur_dA[q] = nxt_dA[q];
-        }
-#else
-#pragma unroll kWsUnroll
-        for (int t = 0; t < steps; ++t) {
-            const float2 dq = dd[t * DC + c];
-            const float* row = bc + t * 2 * N + s * NS;
-            const float2 dl2 = make_float2(dq.x, dq.x);
-            const float2 dx2 = make_float2(dq.y, dq.y);
-            float2 yacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // two short chains
-#pragma unroll
-            for (int q = 0; q < NS / 2; q += 2) {
-                const float4 b4 = *reinterpret_cast<const float4*>(row + 2 * q);
-                float4 c4;
-                if (FULL) c4 = *reinterpret_cast<const float4*>(row + N + 2 * q);
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float2 arg = __fmul2_rn(dl2, a2[q + r]);
-                    const float2 dA = make_float2(ex2_sfu(arg.x), ex2_sfu(arg.y));
-                    const float2 bb = r ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
-                    h[q + r] = __ffma2_rn(dA, h[q + r], __fmul2_rn(dx2, bb));
-                    if (FULL) {
-                        const float2 cc = r ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
-                        yacc[r] = __ffma2_rn(cc, h[q + r], yacc[r]);
-                    }
-                }
-            }
-            if (FULL) {
-                const float2 y2 = __fadd2_rn(yacc[0], yacc[1]);
-                ys[t * DC + c] = y2.x + y2.y;
-            } else {
-                dsum += dq.x;
-            }
-        }
-#endif
-#endif
         mbar_arrive(&done[i]);
     }
-    if (!ok || !dval) return;
+    if (!dval) return;
     float* dst = nullptr;
     if (FULL) {
         if (p.last_state && k == p.nchunk - 1) dst = p.last_state + ((int64_t)b * p.dim + d) * N + s * NS;
