@@ -35,6 +35,9 @@
 #include "scan_tiled.cuh"
 #include "tma.cuh"
 
+#ifndef SSM_HELPER_WAIT
+#define SSM_HELPER_WAIT mbar_wait_bounded_idle   // helper warps sleep while they wait
+#endif
 #ifndef SSM_WS_MINBLOCKS
 #define SSM_WS_MINBLOCKS 7   // resident CTAs per SM the register budget must allow
 #endif
@@ -126,8 +129,8 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
             (p.delta_bias && d0 + qc + 1 < p.dim) ? __ldg(p.delta_bias + d0 + qc + 1) : 0.f);
         for (int j = 0; j < ntiles; ++j) {
             const int i = j % R;
-            if (j >= R && !mbar_wait_bounded(&posted[i], (uint32_t)(((j - R) / R) & 1))) return;
-            if (!mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1))) return;
+            if (j >= R && !SSM_HELPER_WAIT(&posted[i], (uint32_t)(((j - R) / R) & 1))) return;
+            if (!SSM_HELPER_WAIT(&full[j % S], (uint32_t)((j / S) & 1))) return;
             const unsigned char* stg = stage_ptr(j);
             unsigned char* slot = slot_ptr(i);
             float2* dd = reinterpret_cast<float2*>(slot + Cfg::SL_DD);
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int i = j % R;
-            if (!mbar_wait_bounded(&done[i], (uint32_t)((j / R) & 1))) { ok = false; break; }
+            if (!SSM_HELPER_WAIT(&done[i], (uint32_t)((j / R) & 1))) { ok = false; break; }
             if (FULL) {
                 const unsigned char* stg = stage_ptr(j);
                 const int t0 = (int)(t_begin + (int64_t)j * T);

@@ -64,13 +64,49 @@ __device__ __forceinline__ uint64_t global_ns() {
 // kDevErrTimeout here; the host reads it with ssm_get_device_status().
 static __device__ unsigned g_ssm_device_error = 0;
 
+// try_wait with a suspend-time hint: the thread may sleep in hardware for up
+// to `hint_ns` until the phase completes, instead of spinning (a spinning
+// waiter takes issue slots from the warps that do the work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` for at most `limit_ns` nanoseconds of
 // wall time.  Returns false on timeout (and latches kDevErrTimeout).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+        if (global_ns() - t0 > limit_ns) {
+            atomicExch(&g_ssm_device_error, kDevErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// The same bounded wait for warps whose waits are long and whose latency
+// does not matter (the helper warps): between polls the warp sleeps with a
+// growing back-off (32 ns .. 512 ns), so a waiting warp takes almost no issue
+// slots from the warps that compute.
+__device__ __forceinline__ bool mbar_wait_bounded_idle(uint64_t* bar, uint32_t parity,
+                                                       uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    uint32_t nap = 32;
     while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(nap);
+        if (nap < 512) nap <<= 1;
         if (global_ns() - t0 > limit_ns) {
             atomicExch(&g_ssm_device_error, kDevErrTimeout);
             return false;
