@@ -68,6 +68,8 @@ def _bind(lib):
                                                                        ctypes.c_int]
     lib.oracle_state_update.restype = ctypes.c_int
     lib.oracle_state_update.argtypes = [ctypes.c_int64] * 3 + [_dp] * 9 + [ctypes.c_int, _dp]
+    lib.oracle_conv1d_fwd.restype = ctypes.c_int
+    lib.oracle_conv1d_fwd.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int] + [_dp] * 6
     lib.oracle_softplus_scalar.restype = ctypes.c_double
     lib.oracle_softplus_scalar.argtypes = [ctypes.c_double]
     lib.oracle_silu_scalar.restype = ctypes.c_double
@@ -151,6 +153,29 @@ def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, delt
                                              _ptr(out))
     if rc != 0:
         raise ValueError("oracle_state_update rejected its arguments")
+    return out, st
+
+
+def conv1d_fwd(x, w, bias=None, conv_state=None, activation=True, lib=None):
+    """Causal depthwise conv1d (+ SiLU) in fp64.  x: (batch, seqlen, dim);
+    w: (dim, width); bias: (dim,); conv_state: (batch, dim, width-1) inputs
+    before t = 0 (oldest first) or None for zeros.
+    Returns ``(out, conv_state_out)``."""
+    x = _f64(x)
+    bsz, seqlen, dim = x.shape
+    w = _f64(w)
+    width = w.shape[1]
+    if w.shape[0] != dim:
+        raise ValueError("w must be (dim, width)")
+    bias = _f64(bias, (dim,))
+    conv_state = _f64(conv_state, (bsz, dim, width - 1))
+    out = np.empty((bsz, seqlen, dim), dtype=np.float64)
+    st = np.empty((bsz, dim, width - 1), dtype=np.float64)
+    rc = (lib or load()).oracle_conv1d_fwd(bsz, seqlen, dim, width, int(bool(activation)),
+                                           _ptr(x), _ptr(w), _ptr(bias), _ptr(conv_state),
+                                           _ptr(out), _ptr(st))
+    if rc != 0:
+        raise ValueError("oracle_conv1d_fwd rejected its arguments")
     return out, st
 
 

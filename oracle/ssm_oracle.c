@@ -148,6 +148,60 @@ int oracle_state_update(int64_t batch, int64_t dim, int64_t dstate, double *stat
     return 0;
 }
 
+/* Causal depthwise convolution over time, per channel, followed by an
+ * optional SiLU: the local-context convolution the Mamba block applies to x
+ * before the selective SSM ("Mamba的三大创新", section on the simplified
+ * architecture, "为什么SSM前面有个卷积": each token sees its neighbours
+ * before the SSM; the unite.ai overview: a causal Conv1d layer in the block).
+ * Width K, taps w[d][0..K-1] with w[d][K-1] on the current token:
+ *   pre[t, d] = bias[d] + sum_{k=0..K-1} w[d][k] * x[t - (K-1) + k, d]
+ *   out[t, d] = activation ? silu(pre) : pre
+ * Inputs before t = 0 come from conv_state_in[b][d][0..K-2] (oldest first),
+ * or are zero when it is NULL.  conv_state_out receives the last K-1 inputs
+ * of the sequence (oldest first), continuing the state when L < K-1.
+ * Layouts: x, out (batch, seqlen, dim); w (dim, K); bias (dim);
+ * states (batch, dim, K-1). */
+int oracle_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width,
+                      int activation, const double *x, const double *w, const double *bias,
+                      const double *conv_state_in, double *out, double *conv_state_out)
+{
+    if (batch < 0 || seqlen < 0 || dim < 0 || width < 1 || width > 64)
+        return -1;
+    if (!w || (seqlen > 0 && (!x || !out)))
+        return -1;
+    const int64_t H = width - 1;   /* history length */
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            /* the input at time t, for t in [-H, seqlen) */
+            for (int64_t t = 0; t < seqlen; ++t) {
+                double acc = bias ? bias[d] : 0.0;
+                for (int64_t k = 0; k < width; ++k) {
+                    const int64_t tt = t - H + k;
+                    double v;
+                    if (tt >= 0)
+                        v = x[(b * seqlen + tt) * dim + d];
+                    else
+                        v = conv_state_in ? conv_state_in[(b * dim + d) * H + (H + tt)] : 0.0;
+                    acc += w[d * width + k] * v;
+                }
+                out[(b * seqlen + t) * dim + d] = activation ? oracle_silu(acc) : acc;
+            }
+            if (conv_state_out) {
+                for (int64_t k = 0; k < H; ++k) {
+                    const int64_t tt = seqlen - H + k;   /* time of state slot k */
+                    double v;
+                    if (tt >= 0)
+                        v = x[(b * seqlen + tt) * dim + d];
+                    else
+                        v = conv_state_in ? conv_state_in[(b * dim + d) * H + (H + tt)] : 0.0;
+                    conv_state_out[(b * dim + d) * H + k] = v;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
 /* Scalar helpers exposed for the pins on the nonlinearities. */
 double oracle_softplus_scalar(double u) { return oracle_softplus(u); }
 double oracle_silu_scalar(double v) { return oracle_silu(v); }

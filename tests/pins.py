@@ -232,6 +232,59 @@ def pin_nonlinearities(lib):
     assert oracle.softplus(800.0, lib=lib) == 800.0
 
 
+# ---- causal depthwise conv1d (+ SiLU) in front of the scan
+
+def _conv_problem(seed, bsz=2, L=11, dim=3, K=4):
+    r = np.random.default_rng(seed)
+    return (r.standard_normal((bsz, L, dim)), r.standard_normal((dim, K)), r.standard_normal(dim),
+            r.standard_normal((bsz, dim, K - 1)))
+
+
+# C1 -- numpy's direct convolution: out[:, d] = act(np.convolve(x[:, d], w[d][::-1])[:L] + b),
+#       with the K-1 earlier inputs (the state) prepended.
+def pin_conv_numpy(lib):
+    x, w, b, st = _conv_problem(11)
+    out, st_out = oracle.conv1d_fwd(x, w, b, st, lib=lib)
+    bsz, L, dim = x.shape
+    K = w.shape[1]
+    for bb in range(bsz):
+        for d in range(dim):
+            seq = np.concatenate([st[bb, d], x[bb, :, d]])
+            full = np.convolve(seq, w[d][::-1])[K - 1:K - 1 + L]
+            assert np.max(np.abs(out[bb, :, d] - silu_ref(full + b[d]))) < 1e-13
+            assert np.array_equal(st_out[bb, d], seq[-(K - 1):])
+    out0, _ = oracle.conv1d_fwd(x, w, b, None, activation=False, lib=lib)
+    d = 1
+    ref0 = np.convolve(x[0, :, d], w[d][::-1])[:L] + b[d]           # zero history
+    assert np.max(np.abs(out0[0, :, d] - ref0)) < 1e-13
+
+
+# C2 -- special taps: identity (w = e_{K-1}) gives act(x + b); a pure delay
+#       (w = e_0) gives act(x[t-K+1] + b) with the history before t = 0.
+def pin_conv_taps(lib):
+    x, w, b, st = _conv_problem(12, K=3)
+    K = 3
+    ident = np.zeros_like(w); ident[:, K - 1] = 1.0
+    out, _ = oracle.conv1d_fwd(x, ident, b, st, lib=lib)
+    assert np.max(np.abs(out - silu_ref(x + b))) < 1e-15
+    delay = np.zeros_like(w); delay[:, 0] = 1.0
+    out, _ = oracle.conv1d_fwd(x, delay, None, st, activation=False, lib=lib)
+    assert np.array_equal(out[:, K - 1:], x[:, :-(K - 1)])
+    assert np.array_equal(out[:, :K - 1], np.transpose(st, (0, 2, 1)))
+
+
+# C3 -- split + state carry: [0, L1) then [L1, L) from the first part's final
+#       state equals the unsplit call (bit for bit), also when L1 < K - 1.
+def pin_conv_split(lib):
+    x, w, b, st = _conv_problem(13, L=10, K=5)
+    out, st_out = oracle.conv1d_fwd(x, w, b, st, lib=lib)
+    for L1 in (2, 6):
+        o1, s1 = oracle.conv1d_fwd(x[:, :L1], w, b, st, lib=lib)
+        o2, s2 = oracle.conv1d_fwd(x[:, L1:], w, b, s1, lib=lib)
+        assert np.array_equal(np.concatenate([o1, o2], 1), out)
+        assert np.array_equal(s2, st_out)
+
+
 ALL_PINS = [pin_closed_form, pin_prefix_sum, pin_lti_convolution, pin_small_delta,
             pin_large_delta, pin_split_carry, pin_decode_equals_scan, pin_first_order_iir,
-            pin_worked_example, pin_nonlinearities]
+            pin_worked_example, pin_nonlinearities, pin_conv_numpy, pin_conv_taps, pin_conv_split]

@@ -32,6 +32,14 @@ MUTATIONS = {
     "initial_state_ignored": ("h[n] = initial_state ? initial_state[(b * dim + d) * dstate + n] : 0.0;",
                               "h[n] = 0.0;"),
     "silu_sign": ("return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
+    "conv_anticausal": ("const int64_t tt = t - H + k;\n                    double v;\n                    if (tt >= 0)\n                        v = x[(b * seqlen + tt) * dim + d];",
+                        "const int64_t tt = t + k;\n                    double v;\n                    if (tt >= 0 && tt < seqlen)\n                        v = x[(b * seqlen + tt) * dim + d];"),
+    "conv_off_by_one": ("const int64_t tt = t - H + k;\n                    double v;\n                    if (tt >= 0)\n                        v = x[(b * seqlen + tt) * dim + d];",
+                        "const int64_t tt = t - H + k - 1;\n                    double v;\n                    if (tt >= 0)\n                        v = x[(b * seqlen + tt) * dim + d];"),
+    "conv_bias_dropped": ("double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
+    "conv_state_ignored": ("v = conv_state_in ? conv_state_in[(b * dim + d) * H + (H + tt)] : 0.0;\n                    acc +=",
+                           "v = 0.0;\n                    acc +="),
+    "conv_taps_reversed": ("acc += w[d * width + k] * v;", "acc += w[d * width + (width - 1 - k)] * v;"),
 }
 
 
