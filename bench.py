@@ -17,6 +17,9 @@ needed).  Prints ONE JSON line (rank 0):
                buffers, host->device and device->host copies inside the timing
   cpu_baseline the fp64 oracle on the host cores, on a bounded sample
   decode       the one-token state update (256 x 5120 x 16, 128 chained steps)
+  conv_scan    the Mamba block's causal conv (width 4, SiLU) in front of the
+               same scan: fused (ssm_conv_scan_fwd, one pass) against the two
+               separate calls (ssm_conv1d_fwd writing x_conv, then ssm_scan_fwd)
 
 With --impl reference the fp64 CPU oracle is timed instead (the reference arm),
 on a bounded sample of the same workload per step.
@@ -62,9 +65,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-conv", action="store_true")
+    ap.add_argument("--conv-width", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target wall time of the oracle sample")
-    ap.add_argument("--only", choices=["all", "scan", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "scan", "decode", "conv"], default="all",
                     help="run only the prefill scan part or only the decode part (profiling)")
     return ap.parse_args()
 
@@ -293,6 +298,15 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps(line), flush=True)
         return
+    if args.only == "conv":
+        peak, peak_kind = peaks()
+        w = workload_by_name(args.workload)
+        inp = synth.make_scan_inputs(w, device=str(dev))
+        line = {"conv_scan": run_conv(args, w, inp, dev, peak, peak_kind),
+                "source_hash": kernel_source_hash()}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     w = workload_by_name(args.workload)
     import dataclasses
     wr = dataclasses.replace(w, seed=w.seed + 1000 * rank) if rank else w
@@ -363,6 +377,8 @@ def run_ours(args, world, rank, local):
         line["e2e"] = run_e2e(args, w, inp, desc, plan, dev, world, binding)
     if not args.no_decode and args.only == "all":
         line["decode"] = run_decode(args, dev, peak, peak_kind)
+    if not args.no_conv and args.only == "all":
+        line["conv_scan"] = run_conv(args, w, inp, dev, peak, peak_kind)
     if rank == 0 and world == 1 and not args.no_cpu:
         val, dt, nchan, cores = time_oracle(inp, w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -416,6 +432,81 @@ def run_e2e(args, w, inp, desc, plan, dev, world, binding):
     return {"value": whole_job_rate(world, w.tokens, steps, total), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": total / steps}
+
+
+def run_conv(args, w, inp, dev, peak, peak_kind):
+    """The causal conv (width K, SiLU, fp32 taps and bias) in front of the scan
+    of workload w: fused conv+scan against conv1d then scan, CUDA events per
+    call on the launching stream, inputs far larger than L2."""
+    from selective_state_space_137_b300 import binding
+    K = args.conv_width
+    conv = synth.make_conv_inputs(w.batch, w.dim, K, seed=w.seed + 500, device=str(dev))
+    out = torch.empty_like(inp["x"])
+    xc = torch.empty_like(inp["x"])
+    last = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device=dev)
+    cst = torch.empty((w.batch, w.dim, K - 1), dtype=torch.float32, device=dev)
+    desc = binding.make_desc(w.batch, w.seqlen, w.dim, w.dstate, inp["x"].dtype)
+    cdesc = binding.make_conv_desc(K, True)
+    plan = binding.ssm_scan_plan(desc)
+    ws = torch.empty(max(plan.workspace, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fused():
+        st = binding.ssm_conv_scan_fwd(desc, cdesc, inp["x"], conv["conv_w"], conv["conv_bias"],
+                                       None, cst, inp["delta"], inp["A"], inp["B"], inp["C"],
+                                       inp["D"], inp["z"], inp["delta_bias"], out, last, None,
+                                       ws, ws.numel(), stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_conv_scan_fwd")
+
+    def conv1d():
+        st = binding.ssm_conv1d_fwd(desc, cdesc, inp["x"], conv["conv_w"], conv["conv_bias"],
+                                    None, xc, cst, stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_conv1d_fwd")
+
+    def scan():
+        st = binding.ssm_scan_fwd(desc, xc, inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                  inp["z"], inp["delta_bias"], out, last, None, ws, ws.numel(),
+                                  stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_scan_fwd")
+
+    def timed(fns, steps):
+        for _ in range(3):
+            for f in fns:
+                f()
+        torch.cuda.synchronize(dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+              for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record(stream)
+            for j, f in enumerate(fns):
+                f()
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)]))
+                for j in range(len(fns))]
+
+    steps = max(3, min(args.steps, 20))
+    (fused_ms,) = timed([fused], steps)
+    conv_ms, scan_ms = timed([conv1d, scan], steps)
+    e = inp["x"].element_size()
+    state_bytes = w.batch * w.dim * (K - 1) * 4
+    conv_bytes = 2 * w.tokens * e + state_bytes + w.dim * (K + 1) * 4   # x in, x_conv out
+    fused_bytes = w.io_bytes() + state_bytes + w.dim * (K + 1) * 4
+    conv_gbs = conv_bytes / (conv_ms * 1e-3) / 1e9
+    return {"width": K, "activation": "silu",
+            "fused": {"ms": fused_ms, "elements_per_s": w.tokens / (fused_ms * 1e-3),
+                      "gb_per_s": fused_bytes / (fused_ms * 1e-3) / 1e9,
+                      "algorithmic_bytes_per_launch": fused_bytes},
+            "separate": {"conv1d_ms": conv_ms, "scan_ms": scan_ms, "ms": conv_ms + scan_ms,
+                         "elements_per_s": w.tokens / ((conv_ms + scan_ms) * 1e-3)},
+            "fused_speedup": (conv_ms + scan_ms) / fused_ms,
+            "conv1d_roofline": {"bound": "hbm", "achieved": conv_gbs, "peak": peak, "unit": "GB/s",
+                                "frac": conv_gbs / peak, "peak_kind": peak_kind,
+                                "algorithmic_bytes_per_launch": conv_bytes,
+                                "traffic": profiled_traffic("conv1d_fwd_" + w.name)}}
 
 
 def run_decode(args, dev, peak, peak_kind):

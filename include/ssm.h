@@ -123,6 +123,57 @@ SSM_API ssm_status ssm_state_update(const ssm_scan_desc *desc, float *state,
                             const void *z, const float *delta_bias,
                             void *out, void *stream);
 
+/* Causal depthwise convolution applied to x before the SSM in the Mamba block
+ * ("Mamba的三大创新", simplified-architecture section: a convolution gives each
+ * token its neighbours before the SSM; the unite.ai overview: a causal Conv1d
+ * layer).  Width K = `width` (1..8), taps w[d][0..K-1] with w[d][K-1] on the
+ * current token:
+ *   x_conv[t, d] = act(bias[d] + sum_k w[d][k] * x[t - (K-1) + k, d])
+ * act = SiLU when `activation` is 1, identity when 0.  Inputs before t = 0
+ * come from a conv state (batch, dim, K-1) fp32, oldest first, or are zero
+ * when that pointer is NULL; the final state holds the last K-1 inputs. */
+typedef struct {
+    int32_t width;
+    int32_t activation;
+} ssm_conv_desc;
+
+/* x_conv = act(causal depthwise conv(x) + bias), standalone.
+ *   x, out          : (batch, seqlen, dim) io (desc->io_dtype); out must not alias x
+ *   w               : (dim, width) fp32;  bias: (dim) fp32 or NULL
+ *   conv_state_in   : (batch, dim, width-1) fp32 or NULL (zeros)
+ *   conv_state_out  : (batch, dim, width-1) fp32 or NULL; may not alias conv_state_in
+ * desc->dstate and desc->delta_softplus are ignored. */
+SSM_API ssm_status ssm_conv1d_fwd(const ssm_scan_desc *desc, const ssm_conv_desc *conv,
+                                  const void *x, const float *w, const float *bias,
+                                  const float *conv_state_in, void *out,
+                                  float *conv_state_out, void *stream);
+
+/* The conv above fused in front of the selective scan: equal to
+ * ssm_conv1d_fwd(x) followed by ssm_scan_fwd with x = x_conv (both the input
+ * term Delta*x_conv*B and the skip D*x_conv use it), without writing x_conv
+ * to memory.  `x` is the raw (pre-conv) input; the other arguments are those
+ * of ssm_scan_fwd, with the same workspace size (ssm_scan_workspace_size).
+ * conv_state_out may not alias conv_state_in. */
+SSM_API ssm_status ssm_conv_scan_fwd(const ssm_scan_desc *desc, const ssm_conv_desc *conv,
+                                     const void *x, const float *conv_w, const float *conv_bias,
+                                     const float *conv_state_in, float *conv_state_out,
+                                     const void *delta, const float *A, const void *B,
+                                     const void *C, const float *D, const void *z,
+                                     const float *delta_bias, void *out, float *last_state,
+                                     const float *initial_state, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/* One decode step with the conv in front: x_conv from conv_state and the new
+ * raw x, conv_state shifted in place (oldest input dropped, x appended), then
+ * ssm_state_update with x = x_conv.  conv_state: (batch, dim, width-1) fp32
+ * (may be NULL only when width == 1); the rest as in ssm_state_update. */
+SSM_API ssm_status ssm_conv_state_update(const ssm_scan_desc *desc, const ssm_conv_desc *conv,
+                                         float *conv_state, const float *conv_w,
+                                         const float *conv_bias, float *state, const void *x,
+                                         const void *delta, const float *A, const void *B,
+                                         const void *C, const float *D, const void *z,
+                                         const float *delta_bias, void *out, void *stream);
+
 /* Capacity of the fixed scratch buffer used by ssm_scan_fwd_noalloc. */
 #define SSM_NOALLOC_SCRATCH_BYTES (8u << 20)
 

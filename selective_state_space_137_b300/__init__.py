@@ -1,7 +1,10 @@
 """B300-native selective state-space scan (Mamba S6).
 
-Prefill (``scan_fwd``) and decode (``state_update``) run in hand-written CUDA
-kernels for sm_103a behind the C ABI of ``include/ssm.h`` (libssm_b300.so).
+Prefill (``scan_fwd``) and decode (``state_update``), and the same two with
+the Mamba block's causal conv fused in front (``conv_scan_fwd``,
+``conv_state_update``; ``conv1d_fwd`` is the conv alone), run in hand-written
+CUDA kernels for sm_103a behind the C ABI of ``include/ssm.h``
+(libssm_b300.so).
 PyTorch supplies device memory and streams only.
 
 The CUDA library is loaded on first use of an op: importing the package
@@ -12,11 +15,12 @@ from __future__ import annotations
 
 import importlib
 
-__all__ = ["scan_fwd", "state_update", "binding", "synth", "ops"]
+_OPS = ("scan_fwd", "state_update", "conv1d_fwd", "conv_scan_fwd", "conv_state_update")
+__all__ = list(_OPS) + ["binding", "synth", "ops"]
 
 
 def __getattr__(name):
-    if name in ("scan_fwd", "state_update"):
+    if name in _OPS:
         return getattr(importlib.import_module(__name__ + ".ops"), name)
     if name in ("binding", "synth", "ops"):
         return importlib.import_module(__name__ + "." + name)

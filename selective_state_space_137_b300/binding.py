@@ -20,7 +20,8 @@ SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 # Every symbol include/ssm.h declares; the CPU tests check the library exports them.
 EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
             "ssm_scan_plan", "ssm_status_string", "ssm_version", "ssm_scan_fwd_noalloc",
-            "ssm_get_device_status", "ssm_selftest_wait_timeout")
+            "ssm_get_device_status", "ssm_selftest_wait_timeout", "ssm_conv1d_fwd",
+            "ssm_conv_scan_fwd", "ssm_conv_state_update")
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -28,6 +29,10 @@ class ssm_scan_desc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("dim", ctypes.c_int64),
                 ("dstate", ctypes.c_int64), ("io_dtype", ctypes.c_int32),
                 ("delta_softplus", ctypes.c_int32)]
+
+
+class ssm_conv_desc(ctypes.Structure):
+    _fields_ = [("width", ctypes.c_int32), ("activation", ctypes.c_int32)]
 
 
 class ssm_scan_plan_info(ctypes.Structure):
@@ -56,6 +61,15 @@ def _load():
     lib.ssm_state_update.argtypes = [dp, fp, vp, vp, fp, vp, vp, fp, vp, fp, vp, vp]
     lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
     lib.ssm_scan_fwd_noalloc.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, vp]
+    cp = ctypes.POINTER(ssm_conv_desc)
+    lib.ssm_conv1d_fwd.restype = ctypes.c_int
+    lib.ssm_conv1d_fwd.argtypes = [dp, cp, vp, fp, fp, fp, vp, fp, vp]
+    lib.ssm_conv_scan_fwd.restype = ctypes.c_int
+    lib.ssm_conv_scan_fwd.argtypes = [dp, cp, vp, fp, fp, fp, fp, vp, fp, vp, vp, fp, vp, fp, vp,
+                                      fp, fp, vp, sz, vp]
+    lib.ssm_conv_state_update.restype = ctypes.c_int
+    lib.ssm_conv_state_update.argtypes = [dp, cp, fp, fp, fp, fp, vp, vp, fp, vp, vp, fp, vp, fp,
+                                          vp, vp]
     lib.ssm_scan_plan.restype = ctypes.c_int
     lib.ssm_scan_plan.argtypes = [dp, ctypes.POINTER(ssm_scan_plan_info)]
     lib.ssm_selftest_wait_timeout.restype = ctypes.c_int
@@ -153,3 +167,34 @@ def ssm_scan_fwd_noalloc(desc, x, delta, A, B, C, D, z, delta_bias, out, last_st
     return lib.ssm_scan_fwd_noalloc(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(B),
                                     _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out),
                                     _ptr(last_state), _ptr(initial_state), _stream(stream))
+
+
+def make_conv_desc(width, activation=True) -> ssm_conv_desc:
+    return ssm_conv_desc(int(width), 1 if activation else 0)
+
+
+def ssm_conv1d_fwd(desc, conv, x, w, bias, conv_state_in, out, conv_state_out, stream=None) -> int:
+    """Causal depthwise conv (+ SiLU) of x, standalone; status code out."""
+    return lib.ssm_conv1d_fwd(ctypes.byref(desc), ctypes.byref(conv), _ptr(x), _ptr(w), _ptr(bias),
+                              _ptr(conv_state_in), _ptr(out), _ptr(conv_state_out), _stream(stream))
+
+
+def ssm_conv_scan_fwd(desc, conv, x, conv_w, conv_bias, conv_state_in, conv_state_out, delta, A,
+                      B, C, D, z, delta_bias, out, last_state, initial_state, workspace,
+                      workspace_bytes, stream=None) -> int:
+    """The conv fused in front of the scan (x is the raw, pre-conv input)."""
+    return lib.ssm_conv_scan_fwd(ctypes.byref(desc), ctypes.byref(conv), _ptr(x), _ptr(conv_w),
+                                 _ptr(conv_bias), _ptr(conv_state_in), _ptr(conv_state_out),
+                                 _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                 _ptr(delta_bias), _ptr(out), _ptr(last_state),
+                                 _ptr(initial_state), _ptr(workspace), int(workspace_bytes),
+                                 _stream(stream))
+
+
+def ssm_conv_state_update(desc, conv, conv_state, conv_w, conv_bias, state, x, delta, A, B, C, D,
+                          z, delta_bias, out, stream=None) -> int:
+    """One decode step with the conv in front; conv_state and state in place."""
+    return lib.ssm_conv_state_update(ctypes.byref(desc), ctypes.byref(conv), _ptr(conv_state),
+                                     _ptr(conv_w), _ptr(conv_bias), _ptr(state), _ptr(x),
+                                     _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                     _ptr(delta_bias), _ptr(out), _stream(stream))

@@ -26,6 +26,12 @@ struct DecodeParams {
     void* out;
     int64_t batch, dim;
     int softplus;
+    // causal conv in front (read only by kernels instantiated with CONV)
+    float* conv_state = nullptr;            // (batch, dim, conv_width - 1), shifted in place
+    const float* conv_w = nullptr;          // (dim, conv_width)
+    const float* conv_bias = nullptr;       // (dim) or NULL
+    int conv_width = 1;
+    int conv_act = 0;
 };
 
 template <int N>
@@ -67,8 +73,8 @@ __device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f) {
 // threads per block), y is the sequence.  Each thread loads its 16-byte slice
 // of the state, the matching A row slice and B/C slices with vector loads, and
 // the channel's x, delta, z; no integer division is needed to locate them.
-template <typename IO, int N>
-__global__ void __launch_bounds__(256, 8) state_update_kernel(DecodeParams p) {
+template <typename IO, int N, bool CONV = false>
+__global__ void __launch_bounds__(256, CONV ? 4 : 8) state_update_kernel(DecodeParams p) {
     constexpr int LPC = DecodeShape<N>::LPC;
     constexpr int SPL = DecodeShape<N>::SPL;
     const int lin = blockIdx.x * blockDim.x + threadIdx.x;    // lane index within the sequence
@@ -100,7 +106,23 @@ __global__ void __launch_bounds__(256, 8) state_update_kernel(DecodeParams p) {
     load_vec<SPL>(p.A + (int64_t)d * N + sub * SPL, a);
     load_vec<SPL>(Bm + b * N + sub * SPL, bv);
     load_vec<SPL>(Cm + b * N + sub * SPL, cv);
-    const float xv = load_f32(x + ch);
+    float xv = load_f32(x + ch);
+    if (CONV) {
+        // x_conv from the K-1 stored inputs and the new one; the state shift is
+        // written below by the channel's first lane (all lanes read it first)
+        const int H = p.conv_width - 1;
+        float acc = p.conv_bias ? __ldg(p.conv_bias + d) : 0.f;
+        for (int q = 0; q < H; ++q)
+            acc = fmaf(__ldg(p.conv_w + (int64_t)d * p.conv_width + q), p.conv_state[ch * H + q], acc);
+        acc = fmaf(__ldg(p.conv_w + (int64_t)d * p.conv_width + H), xv, acc);
+        const float raw = xv;
+        xv = p.conv_act ? silu_tiled<IO>(acc) : acc;
+        __syncwarp();   // every lane of the warp has read the state before it is shifted
+        if (valid && sub == 0) {
+            for (int q = 0; q + 1 < H; ++q) p.conv_state[ch * H + q] = p.conv_state[ch * H + q + 1];
+            if (H > 0) p.conv_state[ch * H + H - 1] = raw;
+        }
+    }
     const float u = load_f32(dl + ch) + (p.delta_bias ? __ldg(p.delta_bias + d) : 0.f);
     const float zv = z ? load_f32(z + ch) : 0.f;
     const float dsk = p.D ? __ldg(p.D + d) : 0.f;

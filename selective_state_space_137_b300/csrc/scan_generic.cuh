@@ -31,13 +31,22 @@ struct ScanParams {
     int64_t chunk_len;
     int nchunk;
     int softplus;
+    // causal conv in front of the scan (read only by kernels instantiated with CONV)
+    const float* conv_w = nullptr;          // (dim, conv_width)
+    const float* conv_bias = nullptr;       // (dim) or NULL
+    const float* conv_state_in = nullptr;   // (batch, dim, conv_width - 1) or NULL
+    float* conv_state_out = nullptr;        // (batch, dim, conv_width - 1) or NULL
+    int conv_width = 1;
+    int conv_act = 0;
 };
+
+constexpr int kMaxConvWidth = 8;
 
 // MODE_FULL: outputs for tokens of one chunk, from its start state.
 // MODE_AGG : chunk end-state from a zero start, plus the chunk's sum of Delta.
 enum { MODE_FULL = 0, MODE_AGG = 1 };
 
-template <typename IO, int N, int MODE>
+template <typename IO, int N, int MODE, bool CONV = false>
 __global__ void __launch_bounds__(128) scan_generic_kernel(ScanParams p) {
     const int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t b = blockIdx.y;
@@ -76,11 +85,43 @@ __global__ void __launch_bounds__(128) scan_generic_kernel(ScanParams p) {
     const float bias = p.delta_bias ? __ldg(p.delta_bias + d) : 0.f;
     const float dskip = p.D ? __ldg(p.D + d) : 0.f;
 
+    // conv: window of the K-1 raw inputs before t0 (state or zeros before t = 0)
+    const int H = CONV ? p.conv_width - 1 : 0;
+    float cw[kMaxConvWidth], wnd[kMaxConvWidth];
+    const float cbias = (CONV && p.conv_bias) ? __ldg(p.conv_bias + d) : 0.f;
+    if (CONV) {
+#pragma unroll
+        for (int q = 0; q < kMaxConvWidth; ++q) {
+            cw[q] = q < p.conv_width ? __ldg(p.conv_w + d * p.conv_width + q) : 0.f;
+            wnd[q] = 0.f;
+            if (q < H) {
+                const int64_t tt = t0 - H + q;
+                if (tt >= 0) wnd[q] = load_f32(x + (b * p.seqlen + tt) * p.dim + d);
+                else if (p.conv_state_in) wnd[q] = __ldg(p.conv_state_in + chan * H + (H + tt));
+            }
+        }
+    }
+
     float dsum = 0.f;
     for (int64_t t = t0; t < t1; ++t) {
         const int64_t tok = (b * p.seqlen + t) * p.dim + d;
         const int64_t row = (b * p.seqlen + t) * N;
-        const float xv = load_f32(x + tok);
+        float xv = load_f32(x + tok);
+        if (CONV) {
+            // taps 0..H-1 on the window, tap H on the current input (static
+            // register indices only: H is a runtime width)
+            const float raw = xv;
+            float acc = cbias;
+#pragma unroll
+            for (int q = 0; q < kMaxConvWidth; ++q) {
+                if (q < H) acc = fmaf(cw[q], wnd[q], acc);
+                else if (q == H) acc = fmaf(cw[q], raw, acc);
+            }
+#pragma unroll
+            for (int q = 0; q < kMaxConvWidth - 1; ++q)
+                wnd[q] = (q + 1 < H) ? wnd[q + 1] : ((q + 1 == H) ? raw : wnd[q]);
+            xv = p.conv_act ? silu_accurate(acc) : acc;
+        }
         const float u = load_f32(dl + tok) + bias;
         const float dt = p.softplus ? softplus_accurate(u) : u;
         const float dx = dt * xv;
@@ -105,9 +146,16 @@ __global__ void __launch_bounds__(128) scan_generic_kernel(ScanParams p) {
 #pragma unroll
         for (int n = 0; n < N; ++n) cend[n] = h[n];
         p.dsum[(b * p.nchunk + k) * p.dim + d] = dsum;
-    } else if (p.last_state && k == p.nchunk - 1) {
+    } else if (k == p.nchunk - 1) {
+        if (p.last_state) {
 #pragma unroll
-        for (int n = 0; n < N; ++n) p.last_state[chan * N + n] = h[n];
+            for (int n = 0; n < N; ++n) p.last_state[chan * N + n] = h[n];
+        }
+        if (CONV && p.conv_state_out) {
+#pragma unroll
+            for (int q = 0; q < kMaxConvWidth - 1; ++q)
+                if (q < H) p.conv_state_out[chan * H + q] = wnd[q];
+        }
     }
 }
 

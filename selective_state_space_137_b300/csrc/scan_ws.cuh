@@ -44,15 +44,20 @@
 
 namespace ssm {
 
-template <typename IO, int T_, int S_, int R_>
+template <typename IO, int T_, int S_, int R_, int CK_ = 0>
 struct WsCfg {
     static constexpr int N = 16, DC = 16, KS = 2, NS = 8, T = T_, S = S_, R = R_;
+    static constexpr int CK = CK_;               // causal conv width in front (0: none)
+    static constexpr bool CONV = CK > 0;
+    static constexpr int HALO = CONV ? CK - 1 : 0;   // raw x rows before the tile
+    static_assert(CK >= 0 && CK <= kMaxConvWidth, "conv width");
+    static_assert(!CONV || T == 16, "the conv pre-pass maps 4 lanes x 4 tokens onto a tile");
     static constexpr int THREADS = 96;   // warp 0 scan, warp 1 pre-pass, warp 2 post-pass
     static constexpr int ESZ = (int)sizeof(IO);
     static constexpr int TOK_BYTES = T * DC * ESZ;
     static constexpr int BC_BYTES = T * N * ESZ;
-    static constexpr int OFF_X = 0;
-    static constexpr int OFF_DL = round_up(OFF_X + TOK_BYTES, 128);
+    static constexpr int OFF_X = 0;   // [HALO + T][16]: with the conv the box starts K-1 rows early
+    static constexpr int OFF_DL = round_up(OFF_X + (T + HALO) * DC * ESZ, 128);
     static constexpr int OFF_Z = round_up(OFF_DL + TOK_BYTES, 128);
     static constexpr int OFF_B = round_up(OFF_Z + TOK_BYTES, 128);
     static constexpr int OFF_C = round_up(OFF_B + BC_BYTES, 128);
@@ -62,7 +67,8 @@ struct WsCfg {
     static constexpr int SL_DD = 0;
     static constexpr int SL_BC = round_up(SL_DD + T * DC * 8, 128);
     static constexpr int SL_YP = round_up(SL_BC + T * 2 * N * 4, 128);
-    static constexpr int SLOT = round_up(SL_YP + KS * YP_STRIDE * 4, 128);
+    static constexpr int SL_XC = round_up(SL_YP + KS * YP_STRIDE * 4, 128);  // fp32 x_conv [T][16]
+    static constexpr int SLOT = round_up(SL_XC + (CONV ? T * DC * 4 : 0), 128);
     static constexpr int OFF_RING = S * STAGE;
     static constexpr int OFF_OB = round_up(OFF_RING + R * SLOT, 128);
     static constexpr int OFF_BAR = round_up(OFF_OB + 2 * TOK_BYTES, 128);
@@ -90,7 +96,9 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
     if (t_end > p.seqlen) t_end = p.seqlen;
     const int ntiles = t_end > t_begin ? (int)((t_end - t_begin + T - 1) / T) : 0;
     const bool z_on = FULL && p.z != nullptr;
-    const uint32_t stage_tx = (uint32_t)(Cfg::TOK_BYTES * (z_on ? 3 : 2) +
+    constexpr bool CONV = Cfg::CONV;
+    constexpr int H = Cfg::HALO;                      // conv history rows in front of the tile
+    const uint32_t stage_tx = (uint32_t)(Cfg::TOK_BYTES * (z_on ? 3 : 2) + H * DC * Cfg::ESZ +
                                          Cfg::BC_BYTES * (FULL ? 2 : 1));
     auto slot_ptr = [&](int i) { return smem + Cfg::OFF_RING + i * Cfg::SLOT; };
     auto stage_ptr = [&](int j) { return smem + (j % S) * Cfg::STAGE; };
@@ -98,7 +106,8 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
         unsigned char* st = stage_ptr(j);
         const int t0 = (int)(t_begin + (int64_t)j * T);
         mbar_arrive_expect_tx(&full[j % S], stage_tx);
-        tma_load_3d(st + Cfg::OFF_X, &maps.x, &full[j % S], d0, t0, b);
+        // with the conv the x box starts H rows early (negative rows read zeros)
+        tma_load_3d(st + Cfg::OFF_X, &maps.x, &full[j % S], d0, t0 - H, b);
         tma_load_3d(st + Cfg::OFF_DL, &maps.delta, &full[j % S], d0, t0, b);
         if (z_on) tma_load_3d(st + Cfg::OFF_Z, &maps.z, &full[j % S], d0, t0, b);
         tma_load_3d(st + Cfg::OFF_B, &maps.B, &full[j % S], 0, t0, b);
@@ -127,6 +136,18 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
         const float2 bias2 = make_float2(
             (p.delta_bias && d0 + qc < p.dim) ? __ldg(p.delta_bias + d0 + qc) : 0.f,
             (p.delta_bias && d0 + qc + 1 < p.dim) ? __ldg(p.delta_bias + d0 + qc + 1) : 0.f);
+        constexpr int CKW = CONV ? Cfg::CK : 1;
+        float2 cw2[CKW], cbias2 = make_float2(0.f, 0.f);
+        if constexpr (CONV) {
+            const bool v0 = d0 + qc < p.dim, v1 = d0 + qc + 1 < p.dim;
+#pragma unroll
+            for (int q = 0; q < CKW; ++q)
+                cw2[q] = make_float2(v0 ? __ldg(p.conv_w + (int64_t)(d0 + qc) * CKW + q) : 0.f,
+                                     v1 ? __ldg(p.conv_w + (int64_t)(d0 + qc + 1) * CKW + q) : 0.f);
+            if (p.conv_bias)
+                cbias2 = make_float2(v0 ? __ldg(p.conv_bias + d0 + qc) : 0.f,
+                                     v1 ? __ldg(p.conv_bias + d0 + qc + 1) : 0.f);
+        }
         for (int j = 0; j < ntiles; ++j) {
             const int i = j % R;
             if (j >= R && !SSM_HELPER_WAIT(&posted[i], (uint32_t)(((j - R) / R) & 1))) return;
@@ -137,6 +158,51 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
             float* bc = reinterpret_cast<float*>(slot + Cfg::SL_BC);
             const IO* xs = reinterpret_cast<const IO*>(stg + Cfg::OFF_X);
             const IO* ds = reinterpret_cast<const IO*>(stg + Cfg::OFF_DL);
+            const int t0 = (int)(t_begin + (int64_t)j * T);
+            if constexpr (CONV) {
+                // lane (pair qc, group g) takes the 4 consecutive tokens 4g .. 4g+3 and
+                // slides over stage rows 4g .. 4g+3+H (stage row r is time t0 - H + r):
+                // each raw input is loaded once per lane instead of once per tap
+                float* xc = reinterpret_cast<float*>(slot + Cfg::SL_XC);
+                const int g = lane >> 3;
+                float2 win[4 + H];
+#pragma unroll
+                for (int r = 0; r < 4 + H; ++r) win[r] = load2(xs + (4 * g + r) * DC + qc);
+                if (t0 < H) {
+                    // first tile of the sequence: history before t = 0 from the conv state
+#pragma unroll
+                    for (int r = 0; r < 4 + H; ++r) {
+                        const int tt = t0 - H + 4 * g + r;
+                        if (tt < 0) {
+                            float2 v = make_float2(0.f, 0.f);
+                            if (p.conv_state_in) {
+                                const int64_t ch = (int64_t)b * p.dim + d0 + qc;
+                                if (d0 + qc < p.dim) v.x = p.conv_state_in[ch * H + H + tt];
+                                if (d0 + qc + 1 < p.dim) v.y = p.conv_state_in[(ch + 1) * H + H + tt];
+                            }
+                            win[r] = v;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int o = (4 * g + m) * DC + qc;
+                    float2 acc = cbias2;
+#pragma unroll
+                    for (int q = 0; q <= H; ++q) acc = __ffma2_rn(cw2[q], win[m + q], acc);
+                    const float2 xv = p.conv_act
+                        ? make_float2(silu_tiled<IO>(acc.x), silu_tiled<IO>(acc.y)) : acc;
+                    *reinterpret_cast<float2*>(xc + o) = xv;
+                    const float2 u = __fadd2_rn(load2(ds + o), bias2);
+                    float e0 = u.x, e1 = u.y;
+                    if (p.softplus) {
+                        e0 = softplus_tiled<IO>(e0);
+                        e1 = softplus_tiled<IO>(e1);
+                    }
+                    const float2 dx = __fmul2_rn(make_float2(e0, e1), xv);
+                    *reinterpret_cast<float4*>(dd + o) = make_float4(e0, dx.x, e1, dx.y);
+                }
+            } else {
 #pragma unroll
             for (int gi = lane; gi < T * DC / 2; gi += 32) {
                 const int o = (gi / (DC / 2)) * DC + qc;
@@ -149,6 +215,7 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
                 }
                 const float2 dx = __fmul2_rn(make_float2(e0, e1), xv);
                 *reinterpret_cast<float4*>(dd + o) = make_float4(e0, dx.x, e1, dx.y);
+            }
             }
             // B and C widened to fp32 rows [B0..B15 | C0..C15]; lane u writes the
             // 16-byte chunk u, so a warp store covers 512 consecutive bytes.
@@ -171,6 +238,21 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
                     f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
                 }
                 *reinterpret_cast<float4*>(bc + u * 4) = make_float4(f[0], f[1], f[2], f[3]);
+            }
+            if constexpr (CONV && H > 0) if (FULL && p.conv_state_out && k == p.nchunk - 1 && j == ntiles - 1) {
+                // the last H raw inputs (times L-H .. L-1), oldest first
+                const int last = (int)(t_end - t0);          // rows of this tile that exist
+                for (int e = lane; e < DC * H; e += 32) {
+                    const int cc = e / H, q = e % H;
+                    if (d0 + cc >= p.dim) continue;
+                    const int r = last + q;                      // stage row of time L - H + q
+                    float v;
+                    if (t0 - H + r < 0)
+                        v = p.conv_state_in ? p.conv_state_in[((int64_t)b * p.dim + d0 + cc) * H + H + (t0 - H + r)] : 0.f;
+                    else
+                        v = load1(xs + r * DC + cc);
+                    p.conv_state_out[((int64_t)b * p.dim + d0 + cc) * H + q] = v;
+                }
             }
             mbar_arrive(&ready[i]);
         }
@@ -212,7 +294,10 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
                     const int o = (gi / (DC / 2)) * DC + qc;
                     float2 y = __fadd2_rn(*reinterpret_cast<const float2*>(yp + o),
                                           *reinterpret_cast<const float2*>(yp + Cfg::YP_STRIDE + o));
-                    y = __ffma2_rn(dsk2, load2(xs + o), y);
+                    const float2 xv = CONV ? *reinterpret_cast<const float2*>(
+                                                 slot_ptr(i) + Cfg::SL_XC + o * sizeof(float))
+                                           : load2(xs + o);
+                    y = __ffma2_rn(dsk2, xv, y);
                     float y0 = y.x, y1 = y.y;
                     if (z_on) {
                         const float2 zv = load2(zs + o);

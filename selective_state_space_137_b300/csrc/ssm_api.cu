@@ -12,6 +12,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "conv.cuh"
 #include "decode.cuh"
 #include "scan_generic.cuh"
 #include "scan_tiled.cuh"
@@ -72,54 +73,54 @@ size_t workspace_for(const ssm_scan_desc* d, int nchunk) {
     return bytes;
 }
 
-template <typename IO, int N>
+template <typename IO, int N, bool CONV = false>
 cudaError_t launch_generic(const ScanParams& p, cudaStream_t s) {
     const dim3 block(128);
     const unsigned gx = (unsigned)((p.dim + 127) / 128);
     if (p.nchunk > 1) {
         dim3 grid(gx, (unsigned)p.batch, (unsigned)(p.nchunk - 1));
-        ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG><<<grid, block, 0, s>>>(p);
+        ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG, CONV><<<grid, block, 0, s>>>(p);
         const int64_t total = p.batch * p.dim * N;
         ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
             p.A, p.initial_state, p.carry, p.dsum, p.batch, p.dim, N, p.nchunk);
     }
     dim3 grid(gx, (unsigned)p.batch, (unsigned)p.nchunk);
-    ssm::scan_generic_kernel<IO, N, ssm::MODE_FULL><<<grid, block, 0, s>>>(p);
+    ssm::scan_generic_kernel<IO, N, ssm::MODE_FULL, CONV><<<grid, block, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <typename IO>
+template <typename IO, bool CONV = false>
 cudaError_t dispatch_generic(int64_t n, const ScanParams& p, cudaStream_t s) {
     switch (n) {
-        case 1: return launch_generic<IO, 1>(p, s);
-        case 2: return launch_generic<IO, 2>(p, s);
-        case 4: return launch_generic<IO, 4>(p, s);
-        case 8: return launch_generic<IO, 8>(p, s);
-        case 16: return launch_generic<IO, 16>(p, s);
-        case 32: return launch_generic<IO, 32>(p, s);
-        case 64: return launch_generic<IO, 64>(p, s);
+        case 1: return launch_generic<IO, 1, CONV>(p, s);
+        case 2: return launch_generic<IO, 2, CONV>(p, s);
+        case 4: return launch_generic<IO, 4, CONV>(p, s);
+        case 8: return launch_generic<IO, 8, CONV>(p, s);
+        case 16: return launch_generic<IO, 16, CONV>(p, s);
+        case 32: return launch_generic<IO, 32, CONV>(p, s);
+        case 64: return launch_generic<IO, 64, CONV>(p, s);
     }
     return cudaErrorInvalidValue;
 }
 
-template <typename IO, int N>
+template <typename IO, int N, bool CONV = false>
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
     const int64_t lanes = p.dim * ssm::DecodeShape<N>::LPC;   // per sequence
     const dim3 grid((unsigned)((lanes + 255) / 256), (unsigned)p.batch);
-    ssm::state_update_kernel<IO, N><<<grid, 256, 0, s>>>(p);
+    ssm::state_update_kernel<IO, N, CONV><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <typename IO>
+template <typename IO, bool CONV = false>
 cudaError_t dispatch_decode(int64_t n, const DecodeParams& p, cudaStream_t s) {
     switch (n) {
-        case 1: return launch_decode<IO, 1>(p, s);
-        case 2: return launch_decode<IO, 2>(p, s);
-        case 4: return launch_decode<IO, 4>(p, s);
-        case 8: return launch_decode<IO, 8>(p, s);
-        case 16: return launch_decode<IO, 16>(p, s);
-        case 32: return launch_decode<IO, 32>(p, s);
-        case 64: return launch_decode<IO, 64>(p, s);
+        case 1: return launch_decode<IO, 1, CONV>(p, s);
+        case 2: return launch_decode<IO, 2, CONV>(p, s);
+        case 4: return launch_decode<IO, 4, CONV>(p, s);
+        case 8: return launch_decode<IO, 8, CONV>(p, s);
+        case 16: return launch_decode<IO, 16, CONV>(p, s);
+        case 32: return launch_decode<IO, 32, CONV>(p, s);
+        case 64: return launch_decode<IO, 64, CONV>(p, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -181,8 +182,11 @@ TiledShape tiled_shape_io(int64_t n) {
 #ifndef SSM_WS_SLOTS
 #define SSM_WS_SLOTS 2       // helper <-> scan hand-over slots
 #endif
-template <typename IO>
-using WsConfig = ssm::WsCfg<IO, SSM_WS_T, SSM_WS_STAGES, SSM_WS_SLOTS>;
+template <typename IO, int CK = 0>
+using WsConfig = ssm::WsCfg<IO, SSM_WS_T, SSM_WS_STAGES, SSM_WS_SLOTS, CK>;
+// Conv widths fused into the warp-specialised kernel (compile-time width);
+// wider convs take the generic kernel.
+constexpr int kWsMaxConvWidth = 4;
 
 bool ws_path(const ssm_scan_desc* d) { return SSM_USE_WS && d->dstate == 16; }
 
@@ -291,15 +295,17 @@ cudaError_t launch_tiled(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <typename IO>
+template <typename IO, int CK = 0>
 cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
-    using Cfg = WsConfig<IO>;
+    using Cfg = WsConfig<IO, CK>;
     const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int e = (int)sizeof(IO);
     ssm::TiledMaps maps;
     memset(&maps, 0, sizeof(maps));
-    bool ok = encode_3d(&maps.x, p.x, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+    // with the conv, the x box also holds the K-1 raw inputs before the tile
+    const int x_rows = Cfg::T + Cfg::HALO;
+    bool ok = encode_3d(&maps.x, p.x, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, x_rows) &&
               encode_3d(&maps.delta, p.delta, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
               encode_3d(&maps.B, p.B, dt, e, Cfg::N, d->seqlen, d->batch, Cfg::N, Cfg::T) &&
               encode_3d(&maps.C, p.C, dt, e, Cfg::N, d->seqlen, d->batch, Cfg::N, Cfg::T) &&
@@ -321,6 +327,18 @@ cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
     }
     kfull<<<dim3(gx, (unsigned)d->batch, (unsigned)p.nchunk), Cfg::THREADS, Cfg::SMEM, s>>>(maps, p);
     return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_ws_conv(const ssm_scan_desc* d, const ScanParams& p, cudaStream_t s) {
+    static_assert(kWsMaxConvWidth == 4, "one case per fused width");
+    switch (p.conv_width) {
+        case 1: return launch_ws<IO, 1>(d, p, s);
+        case 2: return launch_ws<IO, 2>(d, p, s);
+        case 3: return launch_ws<IO, 3>(d, p, s);
+        case 4: return launch_ws<IO, 4>(d, p, s);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <typename IO>
@@ -506,6 +524,234 @@ ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_decode<float>(desc->dstate, p, s)
                                                     : dispatch_decode<__nv_bfloat16>(desc->dstate, p, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The causal depthwise conv in front of the scan: standalone, fused into the
+// scan, and fused into the decode step.
+namespace {
+
+ssm_status check_conv(const ssm_conv_desc* c) {
+    if (!c) return SSM_ERR_INVALID_ARG;
+    if (c->width < 1 || c->width > ssm::kMaxConvWidth) return SSM_ERR_UNSUPPORTED;
+    if (c->activation != 0 && c->activation != 1) return SSM_ERR_INVALID_ARG;
+    return SSM_OK;
+}
+
+// True when the byte ranges [a, a + n) and [b, b + n) intersect.
+bool overlaps(const void* a, const void* b, size_t n) {
+    if (!a || !b || n == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + n && y < x + n;
+}
+
+// Time steps per thread of the standalone conv: enough threads to cover the
+// GPU a few times over, and chunks long enough that the K-1 rows re-read at
+// each chunk start stay a small fraction.
+int64_t conv_chunk(int64_t seqlen, int64_t threads_per_step) {
+    const int64_t target = (int64_t)kPlanSMs * 2048 * 2;
+    int64_t nch = threads_per_step > 0 ? (target + threads_per_step - 1) / threads_per_step : 1;
+    const int64_t most = seqlen / 64 > 1 ? seqlen / 64 : 1;
+    if (nch > most) nch = most;
+    if (nch > 65535) nch = 65535;
+    if (nch < 1) nch = 1;
+    return (seqlen + nch - 1) / nch;
+}
+
+template <typename IO, int VEC>
+cudaError_t launch_conv(const ssm::ConvParams& p, cudaStream_t s) {
+    const int64_t vecs = p.dim / VEC;
+    const dim3 grid((unsigned)((vecs + 127) / 128), (unsigned)((p.seqlen + p.chunk - 1) / p.chunk),
+                    (unsigned)p.batch);
+    switch (p.width) {
+        case 1: ssm::conv1d_kernel<IO, VEC, 1><<<grid, 128, 0, s>>>(p); break;
+        case 2: ssm::conv1d_kernel<IO, VEC, 2><<<grid, 128, 0, s>>>(p); break;
+        case 3: ssm::conv1d_kernel<IO, VEC, 3><<<grid, 128, 0, s>>>(p); break;
+        case 4: ssm::conv1d_kernel<IO, VEC, 4><<<grid, 128, 0, s>>>(p); break;
+        case 5: ssm::conv1d_kernel<IO, VEC, 5><<<grid, 128, 0, s>>>(p); break;
+        case 6: ssm::conv1d_kernel<IO, VEC, 6><<<grid, 128, 0, s>>>(p); break;
+        case 7: ssm::conv1d_kernel<IO, VEC, 7><<<grid, 128, 0, s>>>(p); break;
+        case 8: ssm::conv1d_kernel<IO, VEC, 8><<<grid, 128, 0, s>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+// Copy (or zero) the conv state when there are no tokens to push through it.
+cudaError_t conv_state_passthrough(float* out, const float* in, size_t bytes, cudaStream_t s) {
+    if (!out || out == in || bytes == 0) return cudaSuccess;
+    return in ? cudaMemcpyAsync(out, in, bytes, cudaMemcpyDeviceToDevice, s)
+              : cudaMemsetAsync(out, 0, bytes, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_conv1d_fwd(const ssm_scan_desc* desc, const ssm_conv_desc* conv, const void* x,
+                          const float* w, const float* bias, const float* conv_state_in,
+                          void* out, float* conv_state_out, void* stream) {
+    if (!desc) return SSM_ERR_INVALID_ARG;
+    if (desc->batch < 0 || desc->seqlen < 0 || desc->dim < 0) return SSM_ERR_INVALID_ARG;
+    if (desc->io_dtype != SSM_DTYPE_F32 && desc->io_dtype != SSM_DTYPE_BF16)
+        return SSM_ERR_UNSUPPORTED;
+    ssm_status st = check_conv(conv);
+    if (st != SSM_OK) return st;
+    const size_t esz = io_size(desc);
+    if (!opt_aligned(x, esz) || !opt_aligned(out, esz) || !opt_aligned(w, 4) ||
+        !opt_aligned(bias, 4) || !opt_aligned(conv_state_in, 4) || !opt_aligned(conv_state_out, 4))
+        return SSM_ERR_INVALID_ARG;
+    const int H = conv->width - 1;
+    const size_t state_bytes = (size_t)desc->batch * (size_t)desc->dim * (size_t)H * sizeof(float);
+    if (overlaps(conv_state_in, conv_state_out, state_bytes)) return SSM_ERR_INVALID_ARG;
+    if (desc->batch == 0 || desc->dim == 0) return SSM_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (desc->seqlen == 0)
+        return conv_state_passthrough(conv_state_out, conv_state_in, state_bytes, s) == cudaSuccess
+                   ? SSM_OK : SSM_ERR_CUDA;
+    if (!x || !w || !out) return SSM_ERR_INVALID_ARG;
+    const size_t io_bytes = (size_t)desc->batch * (size_t)desc->seqlen * (size_t)desc->dim * esz;
+    if (overlaps(x, out, io_bytes)) return SSM_ERR_INVALID_ARG;
+    if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
+
+    const int vec = (int)(16 / esz);
+    const bool wide = desc->dim % vec == 0 && aligned16(x) && aligned16(out);
+    ssm::ConvParams p;
+    p.x = x; p.w = w; p.bias = bias; p.state_in = conv_state_in; p.out = out;
+    p.state_out = conv_state_out;
+    p.batch = desc->batch; p.seqlen = desc->seqlen; p.dim = desc->dim;
+    p.width = conv->width; p.act = conv->activation;
+    p.chunk = conv_chunk(desc->seqlen, wide ? desc->dim / vec : desc->dim);
+    if (((desc->dim / (wide ? vec : 1)) + 127) / 128 > 0x7fffffff) return SSM_ERR_UNSUPPORTED;
+    cudaError_t e;
+    if (desc->io_dtype == SSM_DTYPE_F32)
+        e = wide ? launch_conv<float, 4>(p, s) : launch_conv<float, 1>(p, s);
+    else
+        e = wide ? launch_conv<__nv_bfloat16, 8>(p, s) : launch_conv<__nv_bfloat16, 1>(p, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_conv_scan_fwd(const ssm_scan_desc* desc, const ssm_conv_desc* conv,
+                             const void* x, const float* conv_w, const float* conv_bias,
+                             const float* conv_state_in, float* conv_state_out,
+                             const void* delta, const float* A, const void* B, const void* C,
+                             const float* D, const void* z, const float* delta_bias, void* out,
+                             float* last_state, const float* initial_state, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    st = check_conv(conv);
+    if (st != SSM_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t N = desc->dstate;
+    const size_t state_bytes = (size_t)desc->batch * (size_t)desc->dim * (size_t)N * sizeof(float);
+    const int H = conv->width - 1;
+    const size_t cstate_bytes = (size_t)desc->batch * (size_t)desc->dim * (size_t)H * sizeof(float);
+
+    const size_t esz = io_size(desc);
+    if (!opt_aligned(x, esz) || !opt_aligned(delta, esz) || !opt_aligned(B, esz) ||
+        !opt_aligned(C, esz) || !opt_aligned(z, esz) || !opt_aligned(out, esz) || !opt_aligned(A, 4) ||
+        !opt_aligned(D, 4) || !opt_aligned(delta_bias, 4) || !opt_aligned(last_state, 4) ||
+        !opt_aligned(initial_state, 4) || !opt_aligned(conv_w, 4) || !opt_aligned(conv_bias, 4) ||
+        !opt_aligned(conv_state_in, 4) || !opt_aligned(conv_state_out, 4))
+        return SSM_ERR_INVALID_ARG;
+    if (overlaps(conv_state_in, conv_state_out, cstate_bytes)) return SSM_ERR_INVALID_ARG;
+
+    if (desc->batch == 0 || desc->dim == 0) return SSM_OK;
+    if (desc->seqlen == 0) {
+        cudaError_t e = conv_state_passthrough(conv_state_out, conv_state_in, cstate_bytes, s);
+        if (e == cudaSuccess && last_state && last_state != initial_state)
+            e = initial_state
+                ? cudaMemcpyAsync(last_state, initial_state, state_bytes, cudaMemcpyDeviceToDevice, s)
+                : cudaMemsetAsync(last_state, 0, state_bytes, s);
+        return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    }
+    if (!x || !delta || !A || !B || !C || !out || !conv_w) return SSM_ERR_INVALID_ARG;
+
+    const bool tiled = tiled_shape_ok(desc) && aligned16(x) && aligned16(delta) &&
+                       aligned16(B) && aligned16(C) && aligned16(out) && opt_aligned(z, 16) &&
+                       opt_aligned(last_state, 16);
+    // The conv is fused into the warp-specialised kernel (dstate 16, width up
+    // to kWsMaxConvWidth) and into the generic one, which takes the rest.
+    const bool ws = tiled && ws_path(desc) && conv->width <= kWsMaxConvWidth;
+    int nchunk;
+    int64_t chunk_len;
+    if (ws) {
+        tiled_chunks(desc, &nchunk, &chunk_len);
+    } else {
+        nchunk = generic_nchunk(desc);
+        chunk_len = (desc->seqlen + nchunk - 1) / nchunk;
+    }
+    const size_t need = workspace_for(desc, nchunk);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return SSM_ERR_INVALID_ARG;
+    if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
+
+    ScanParams p;
+    p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+    p.delta_bias = delta_bias; p.out = out; p.last_state = last_state;
+    p.initial_state = initial_state;
+    p.batch = desc->batch; p.seqlen = desc->seqlen; p.dim = desc->dim;
+    p.nchunk = nchunk;
+    p.chunk_len = chunk_len;
+    p.softplus = desc->delta_softplus ? 1 : 0;
+    p.carry = nullptr; p.dsum = nullptr;
+    if (nchunk > 1) {
+        char* w = static_cast<char*>(workspace);
+        const size_t per = (size_t)desc->batch * (size_t)nchunk * (size_t)desc->dim;
+        p.carry = reinterpret_cast<float*>(w);
+        p.dsum = reinterpret_cast<float*>(w + ((per * (size_t)N * sizeof(float) + 255) & ~(size_t)255));
+    }
+    p.conv_w = conv_w; p.conv_bias = conv_bias;
+    p.conv_state_in = H > 0 ? conv_state_in : nullptr;
+    p.conv_state_out = H > 0 ? conv_state_out : nullptr;
+    p.conv_width = conv->width; p.conv_act = conv->activation;
+
+    cudaError_t e;
+    if (ws)
+        e = desc->io_dtype == SSM_DTYPE_F32 ? launch_ws_conv<float>(desc, p, s)
+                                            : launch_ws_conv<__nv_bfloat16>(desc, p, s);
+    else
+        e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_generic<float, true>(N, p, s)
+                                            : dispatch_generic<__nv_bfloat16, true>(N, p, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_conv_state_update(const ssm_scan_desc* desc, const ssm_conv_desc* conv,
+                                 float* conv_state, const float* conv_w, const float* conv_bias,
+                                 float* state, const void* x, const void* delta, const float* A,
+                                 const void* B, const void* C, const float* D, const void* z,
+                                 const float* delta_bias, void* out, void* stream) {
+    ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    st = check_conv(conv);
+    if (st != SSM_OK) return st;
+    const size_t esz = io_size(desc);
+    if (!opt_aligned(state, desc->dstate >= 4 ? 16 : 4) || !opt_aligned(x, esz) ||
+        !opt_aligned(delta, esz) || !opt_aligned(B, esz) || !opt_aligned(C, esz) ||
+        !opt_aligned(z, esz) || !opt_aligned(out, esz) || !opt_aligned(A, 4) || !opt_aligned(D, 4) ||
+        !opt_aligned(delta_bias, 4) || !opt_aligned(conv_state, 4) || !opt_aligned(conv_w, 4) ||
+        !opt_aligned(conv_bias, 4))
+        return SSM_ERR_INVALID_ARG;
+    if (desc->batch == 0 || desc->dim == 0) return SSM_OK;
+    if (!state || !x || !delta || !A || !B || !C || !out || !conv_w) return SSM_ERR_INVALID_ARG;
+    if (conv->width > 1 && !conv_state) return SSM_ERR_INVALID_ARG;
+    if (desc->batch > 65535 || desc->dim * 64 >= ((int64_t)1 << 31)) return SSM_ERR_UNSUPPORTED;
+
+    DecodeParams p;
+    p.state = state; p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+    p.delta_bias = delta_bias; p.out = out;
+    p.batch = desc->batch; p.dim = desc->dim;
+    p.softplus = desc->delta_softplus ? 1 : 0;
+    p.conv_state = conv_state; p.conv_w = conv_w; p.conv_bias = conv_bias;
+    p.conv_width = conv->width; p.conv_act = conv->activation;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = desc->io_dtype == SSM_DTYPE_F32
+                        ? dispatch_decode<float, true>(desc->dstate, p, s)
+                        : dispatch_decode<__nv_bfloat16, true>(desc->dstate, p, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

@@ -1,8 +1,9 @@
 """Tensor-level entry points over the C ABI.
 
-``scan_fwd`` and ``state_update`` check shapes, allocate outputs (and the
-scan workspace) with torch on the inputs' device, and call the library.  They
-add no arithmetic of their own.
+``scan_fwd``, ``state_update`` and the conv variants (``conv1d_fwd``,
+``conv_scan_fwd``, ``conv_state_update``) check shapes, allocate outputs (and
+the scan workspace) with torch on the inputs' device, and call the library.
+They add no arithmetic of their own.
 """
 from __future__ import annotations
 
@@ -82,4 +83,112 @@ def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, delt
     st = _b.ssm_state_update(desc, state, x, delta, A, B, C, D, z, delta_bias, out, stream)
     if st != _b.SSM_OK:
         raise _b.SSMError(st, "ssm_state_update")
+    return out
+
+
+def _conv_state_shape(bsz, dim, width):
+    return (bsz, dim, width - 1)
+
+
+def conv1d_fwd(x, w, bias=None, conv_state=None, activation=True, out=None,
+               conv_state_out=None, stream=None):
+    """Causal depthwise conv of x (batch, seqlen, dim) with taps w (dim, width)
+    fp32, optional bias (dim,), optional history conv_state (batch, dim,
+    width-1) fp32.  Returns ``(x_conv, conv_state_out)``."""
+    if not x.is_cuda:
+        raise ValueError("conv1d_fwd runs on a CUDA device only")
+    bsz, seqlen, dim = x.shape
+    width = w.shape[1]
+    dev = x.device
+    _check(w, "w", (dim, width), torch.float32, dev)
+    _check(bias, "bias", (dim,), torch.float32, dev)
+    _check(conv_state, "conv_state", _conv_state_shape(bsz, dim, width), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    if conv_state_out is None:
+        conv_state_out = torch.empty(_conv_state_shape(bsz, dim, width), dtype=torch.float32,
+                                     device=dev)
+    desc = _b.make_desc(bsz, seqlen, dim, 1, x.dtype, False)
+    st = _b.ssm_conv1d_fwd(desc, _b.make_conv_desc(width, activation), x, w, bias, conv_state,
+                           out, conv_state_out, stream)
+    if st != _b.SSM_OK:
+        raise _b.SSMError(st, "ssm_conv1d_fwd")
+    return out, conv_state_out
+
+
+def conv_scan_fwd(x, conv_w, delta, A, B, C, D=None, z=None, delta_bias=None, conv_bias=None,
+                  conv_state=None, initial_state=None, activation=True, delta_softplus=True,
+                  out=None, last_state=None, conv_state_out=None, workspace=None, stream=None):
+    """The Mamba block's conv + selective scan in one pass: x is the raw
+    (pre-conv) input; the scan uses x_conv = act(conv(x) + conv_bias) for both
+    the input and the skip term.  Returns ``(out, last_state, conv_state_out)``."""
+    if not x.is_cuda:
+        raise ValueError("conv_scan_fwd runs on a CUDA device only")
+    bsz, seqlen, dim = x.shape
+    dstate = A.shape[1]
+    width = conv_w.shape[1]
+    dev, io = x.device, x.dtype
+    _check(delta, "delta", x.shape, io, dev)
+    _check(z, "z", x.shape, io, dev)
+    _check(B, "B", (bsz, seqlen, dstate), io, dev)
+    _check(C, "C", (bsz, seqlen, dstate), io, dev)
+    _check(A, "A", (dim, dstate), torch.float32, dev)
+    _check(D, "D", (dim,), torch.float32, dev)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    _check(initial_state, "initial_state", (bsz, dim, dstate), torch.float32, dev)
+    _check(conv_w, "conv_w", (dim, width), torch.float32, dev)
+    _check(conv_bias, "conv_bias", (dim,), torch.float32, dev)
+    _check(conv_state, "conv_state", _conv_state_shape(bsz, dim, width), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    if last_state is None:
+        last_state = torch.empty((bsz, dim, dstate), dtype=torch.float32, device=dev)
+    if conv_state_out is None:
+        conv_state_out = torch.empty(_conv_state_shape(bsz, dim, width), dtype=torch.float32,
+                                     device=dev)
+    desc = _b.make_desc(bsz, seqlen, dim, dstate, io, delta_softplus)
+    need = _b.ssm_scan_workspace_size(desc)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _b.ssm_conv_scan_fwd(desc, _b.make_conv_desc(width, activation), x, conv_w, conv_bias,
+                              conv_state, conv_state_out, delta, A, B, C, D, z, delta_bias, out,
+                              last_state, initial_state, workspace if need else None,
+                              wbytes if need else 0, stream)
+    if st != _b.SSM_OK:
+        raise _b.SSMError(st, "ssm_conv_scan_fwd")
+    return out, last_state, conv_state_out
+
+
+def conv_state_update(conv_state, conv_w, state, x, delta, A, B, C, D=None, z=None,
+                      delta_bias=None, conv_bias=None, activation=True, delta_softplus=True,
+                      out=None, stream=None):
+    """One decode step with the conv in front: conv_state (batch, dim,
+    width-1) and state (batch, dim, dstate) are updated in place.  Returns
+    ``out``."""
+    if not state.is_cuda:
+        raise ValueError("conv_state_update runs on a CUDA device only")
+    bsz, dim, dstate = state.shape
+    width = conv_w.shape[1]
+    dev, io = x.device, x.dtype
+    _check(state, "state", (bsz, dim, dstate), torch.float32, dev)
+    _check(conv_state, "conv_state", _conv_state_shape(bsz, dim, width), torch.float32, dev)
+    _check(conv_w, "conv_w", (dim, width), torch.float32, dev)
+    _check(conv_bias, "conv_bias", (dim,), torch.float32, dev)
+    _check(x, "x", (bsz, dim), io, dev)
+    _check(delta, "delta", (bsz, dim), io, dev)
+    _check(z, "z", (bsz, dim), io, dev)
+    _check(B, "B", (bsz, dstate), io, dev)
+    _check(C, "C", (bsz, dstate), io, dev)
+    _check(A, "A", (dim, dstate), torch.float32, dev)
+    _check(D, "D", (dim,), torch.float32, dev)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    desc = _b.make_desc(bsz, 1, dim, dstate, io, delta_softplus)
+    st = _b.ssm_conv_state_update(desc, _b.make_conv_desc(width, activation), conv_state, conv_w,
+                                  conv_bias, state, x, delta, A, B, C, D, z, delta_bias, out,
+                                  stream)
+    if st != _b.SSM_OK:
+        raise _b.SSMError(st, "ssm_conv_state_update")
     return out

@@ -16,6 +16,12 @@ Recipe (per workload; draws are fp32, then cast to the I/O dtype):
 Draw order: x, z, delta_raw, bias uniform, B, C, D.  A, D and delta_bias are
 always fp32; x, delta, z, B, C follow the I/O dtype.
 
+Causal conv in front of the scan (own seeded stream, all fp32), the default
+initialisation of a depthwise Conv1d layer with K taps (fan-in K):
+  conv_w[d, k]    ~ U[-1/sqrt(K), 1/sqrt(K)]       shape (dim, K)
+  conv_bias[d]    ~ U[-1/sqrt(K), 1/sqrt(K)]       shape (dim,)
+  conv_state      ~ N(0, 1)                        shape (batch, dim, K-1)
+
 On ``device="cpu"`` the draws come from numpy's PCG64 stream (bit-identical on
 every machine).  On a CUDA device they come from torch's device generator,
 which is much faster for the multi-GB workloads; both are seeded.
@@ -164,3 +170,16 @@ def make_decode_inputs(w: DecodeWorkload, device: str = "cpu") -> dict:
     A = (-torch.exp(a_log)).to(torch.float32).contiguous()
     state = g.normal((w.batch, w.dim, w.dstate))
     return dict(state=state, x=x, delta=delta, z=z, A=A, B=Bm, C=Cm, D=D, delta_bias=bias)
+
+
+def make_conv_inputs(batch: int, dim: int, width: int, seed: int, device: str = "cpu",
+                     with_bias: bool = True, with_state: bool = False) -> dict:
+    """Draw the causal conv's parameters (and optionally its history):
+    conv_w (dim, width), conv_bias (dim,) or None, conv_state (batch, dim,
+    width-1) or None; all fp32."""
+    g = _Draw(seed, device)
+    bound = 1.0 / float(width) ** 0.5
+    w = g.uniform((dim, width), -bound, bound).to(torch.float32).contiguous()
+    bias = g.uniform((dim,), -bound, bound).to(torch.float32) if with_bias else None
+    state = g.normal((batch, dim, width - 1)).contiguous() if with_state else None
+    return dict(conv_w=w, conv_bias=bias, conv_state=state)

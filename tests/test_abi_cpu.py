@@ -116,3 +116,42 @@ def test_plan_picks_the_tiled_path(ssm_lib):
         assert L.ssm_scan_plan(L.make_desc(2, 300, 72, n, L.SSM_DTYPE_BF16)).path == path
     assert L.ssm_scan_plan(L.make_desc(2, 300, 72, 16, L.SSM_DTYPE_F32)).path == 2
     assert L.ssm_scan_plan(L.make_desc(2, 300, 12, 16, L.SSM_DTYPE_BF16)).path == 0   # 24-byte rows
+
+
+def test_conv_rejections_before_launch(ssm_lib):
+    """The conv entry points check the conv descriptor, alignment and aliasing
+    before any CUDA call (fake addresses again)."""
+    L = ssm_lib
+    d = L.make_desc(2, 8, 16, 16, L.SSM_DTYPE_F32)
+    ok_conv = L.make_conv_desc(4, True)
+
+    def conv1d(conv, x=A16, w=A16, s_in=None, out=A16 + 4096, s_out=None, desc=d):
+        return L.ssm_conv1d_fwd(desc, conv, x, w, None, s_in, out, s_out, None)
+
+    assert L.lib.ssm_conv1d_fwd(ctypes.byref(d), None, *([None] * 7)) == L.SSM_ERR_INVALID_ARG
+    assert conv1d(L.make_conv_desc(0)) == L.SSM_ERR_UNSUPPORTED            # width 0
+    assert conv1d(L.make_conv_desc(9)) == L.SSM_ERR_UNSUPPORTED            # width > 8
+    assert conv1d(L.ssm_conv_desc(4, 2)) == L.SSM_ERR_INVALID_ARG          # activation not 0/1
+    assert conv1d(ok_conv, x=A16 + 2) == L.SSM_ERR_INVALID_ARG             # fp32 at 2-byte offset
+    assert conv1d(ok_conv, s_in=A16, s_out=A16 + 8) == L.SSM_ERR_INVALID_ARG   # states overlap
+    assert conv1d(ok_conv, x=0) == L.SSM_ERR_INVALID_ARG                   # NULL x
+    assert conv1d(ok_conv, out=A16 + 64) == L.SSM_ERR_INVALID_ARG          # out overlaps x
+    assert conv1d(ok_conv, desc=L.make_desc(0, 8, 16, 1, 0)) == L.SSM_OK   # empty batch: no-op
+
+    def fused(conv, w=A16, s_in=None, s_out=None, desc=d):
+        return L.ssm_conv_scan_fwd(desc, conv, A16, w, None, s_in, s_out, A16, A16, A16, A16,
+                                   None, None, None, A16, None, None, None, 0, None)
+
+    assert fused(L.make_conv_desc(9)) == L.SSM_ERR_UNSUPPORTED
+    assert fused(ok_conv, w=0) == L.SSM_ERR_INVALID_ARG                    # taps missing
+    assert fused(ok_conv, s_in=A16, s_out=A16) == L.SSM_ERR_INVALID_ARG    # in-place conv state
+    assert fused(ok_conv, desc=L.make_desc(1, 8, 16, 3, 0)) == L.SSM_ERR_UNSUPPORTED
+
+    def step(conv, cs=A16, w=A16):
+        return L.ssm_conv_state_update(d, conv, cs, w, None, A16, A16, A16, A16, A16, A16, None,
+                                       None, None, A16, None)
+
+    assert step(L.make_conv_desc(4), cs=None) == L.SSM_ERR_INVALID_ARG      # width 4 needs a state
+    assert step(L.make_conv_desc(4), w=None) == L.SSM_ERR_INVALID_ARG
+    assert step(L.ssm_conv_desc(4, -1)) == L.SSM_ERR_INVALID_ARG
+    assert step(L.make_conv_desc(4), cs=A16 + 2) == L.SSM_ERR_INVALID_ARG   # misaligned state
