@@ -16,6 +16,9 @@
 #ifndef SSM_CONV_UNROLL
 #define SSM_CONV_UNROLL 4    // rows loaded ahead per thread
 #endif
+#ifndef SSM_CONV_MINBLOCKS
+#define SSM_CONV_MINBLOCKS 1 // resident 128-thread blocks per SM the registers must allow
+#endif
 
 namespace ssm {
 
@@ -32,21 +35,46 @@ struct ConvParams {
     int act;
 };
 
+// VEC consecutive io elements as fp32: one 16- or 8-byte load when the
+// vector has that size, else element by element; and back.
 template <typename IO, int VEC>
 __device__ __forceinline__ void load_row(const IO* p, float* f) {
-    if (VEC == 1) {
-        f[0] = load_f32(p);
-    } else {
+    constexpr int BYTES = VEC * (int)sizeof(IO);
+    if constexpr (BYTES == 16) {
         unpack<IO>(__ldg(reinterpret_cast<const uint4*>(p)), f);
+    } else if constexpr (BYTES == 8 || BYTES == 4) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (BYTES == 8) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+            w.x = v.x; w.y = v.y;
+        } else {
+            w.x = __ldg(reinterpret_cast<const unsigned*>(p));
+        }
+        float g[8];
+        unpack<IO>(w, g);
+#pragma unroll
+        for (int v2 = 0; v2 < VEC; ++v2) f[v2] = g[v2];
+    } else {
+#pragma unroll
+        for (int v2 = 0; v2 < VEC; ++v2) f[v2] = load_f32(p + v2);
     }
 }
 
 template <typename IO, int VEC>
 __device__ __forceinline__ void store_row(IO* p, const float* f) {
-    if (VEC == 1) {
-        store_io(p, f[0]);
-    } else {
+    constexpr int BYTES = VEC * (int)sizeof(IO);
+    if constexpr (BYTES == 16) {
         *reinterpret_cast<uint4*>(p) = pack<IO>(f);
+    } else if constexpr (BYTES == 8 || BYTES == 4) {
+        float g[8] = {};
+#pragma unroll
+        for (int v2 = 0; v2 < VEC; ++v2) g[v2] = f[v2];
+        const uint4 v = pack<IO>(g);
+        if constexpr (BYTES == 8) *reinterpret_cast<uint2*>(p) = make_uint2(v.x, v.y);
+        else *reinterpret_cast<unsigned*>(p) = v.x;
+    } else {
+#pragma unroll
+        for (int v2 = 0; v2 < VEC; ++v2) store_io(p + v2, f[v2]);
     }
 }
 
@@ -54,7 +82,7 @@ __device__ __forceinline__ void store_row(IO* p, const float* f) {
 // registers; the time loop is unrolled by U with the U row loads issued before
 // the arithmetic, so each thread keeps U 16-byte loads in flight.
 template <typename IO, int VEC, int K>
-__global__ void __launch_bounds__(128) conv1d_kernel(ConvParams p) {
+__global__ void __launch_bounds__(128, SSM_CONV_MINBLOCKS) conv1d_kernel(ConvParams p) {
     constexpr int H = K - 1;
     constexpr int HW = H > 0 ? H : 1;   // window array extent
     constexpr int U = SSM_CONV_UNROLL;

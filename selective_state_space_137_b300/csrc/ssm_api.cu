@@ -548,13 +548,20 @@ bool overlaps(const void* a, const void* b, size_t n) {
     return x < y + n && y < x + n;
 }
 
+#ifndef SSM_CONV_VEC16
+#define SSM_CONV_VEC16 4     // bf16 channels per thread of the standalone conv (8-byte rows)
+#endif
+#ifndef SSM_CONV_MINCHUNK
+#define SSM_CONV_MINCHUNK 64 // shortest time chunk per thread
+#endif
+
 // Time steps per thread of the standalone conv: enough threads to cover the
 // GPU a few times over, and chunks long enough that the K-1 rows re-read at
 // each chunk start stay a small fraction.
 int64_t conv_chunk(int64_t seqlen, int64_t threads_per_step) {
     const int64_t target = (int64_t)kPlanSMs * 2048 * 2;
     int64_t nch = threads_per_step > 0 ? (target + threads_per_step - 1) / threads_per_step : 1;
-    const int64_t most = seqlen / 64 > 1 ? seqlen / 64 : 1;
+    const int64_t most = seqlen / SSM_CONV_MINCHUNK > 1 ? seqlen / SSM_CONV_MINCHUNK : 1;
     if (nch > most) nch = most;
     if (nch > 65535) nch = 65535;
     if (nch < 1) nch = 1;
@@ -617,8 +624,8 @@ ssm_status ssm_conv1d_fwd(const ssm_scan_desc* desc, const ssm_conv_desc* conv, 
     if (overlaps(x, out, io_bytes)) return SSM_ERR_INVALID_ARG;
     if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
 
-    const int vec = (int)(16 / esz);
-    const bool wide = desc->dim % vec == 0 && aligned16(x) && aligned16(out);
+    const int vec = desc->io_dtype == SSM_DTYPE_F32 ? 4 : SSM_CONV_VEC16;
+    const bool wide = desc->dim % vec == 0 && aligned16(x) && aligned16(out);   // vector rows
     ssm::ConvParams p;
     p.x = x; p.w = w; p.bias = bias; p.state_in = conv_state_in; p.out = out;
     p.state_out = conv_state_out;
@@ -630,7 +637,7 @@ ssm_status ssm_conv1d_fwd(const ssm_scan_desc* desc, const ssm_conv_desc* conv, 
     if (desc->io_dtype == SSM_DTYPE_F32)
         e = wide ? launch_conv<float, 4>(p, s) : launch_conv<float, 1>(p, s);
     else
-        e = wide ? launch_conv<__nv_bfloat16, 8>(p, s) : launch_conv<__nv_bfloat16, 1>(p, s);
+        e = wide ? launch_conv<__nv_bfloat16, SSM_CONV_VEC16>(p, s) : launch_conv<__nv_bfloat16, 1>(p, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
