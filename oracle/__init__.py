@@ -12,7 +12,9 @@ This module only marshals numpy arrays into fp64 buffers for it.
 
 Definitions followed (see the header of ``ssm_oracle.c`` for the passages):
 the recurrence h_t = exp(Delta_t A) * h_{t-1} + Delta_t B_t x_t, the readout
-y_t = C_t . h_t + D x_t, the gate silu(z_t), and Delta = softplus(raw + bias).
+y_t = C_t . h_t + D x_t, the gate silu(z_t), and Delta = softplus(raw + bias);
+the causal depthwise conv in front of it; and the gradients of the scan
+(``scan_bwd``: the same loop differentiated in reverse mode).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 identities and closed forms that are independent of this code.
@@ -68,6 +70,9 @@ def _bind(lib):
                                                                        ctypes.c_int]
     lib.oracle_state_update.restype = ctypes.c_int
     lib.oracle_state_update.argtypes = [ctypes.c_int64] * 3 + [_dp] * 9 + [ctypes.c_int, _dp]
+    lib.oracle_scan_bwd.restype = ctypes.c_int
+    lib.oracle_scan_bwd.argtypes = ([ctypes.c_int64] * 4 + [_dp] * 8 + [ctypes.c_int] + [_dp] * 12
+                                    + [ctypes.c_int])
     lib.oracle_conv1d_fwd.restype = ctypes.c_int
     lib.oracle_conv1d_fwd.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int] + [_dp] * 6
     lib.oracle_softplus_scalar.restype = ctypes.c_double
@@ -130,6 +135,43 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
     if rc != 0:
         raise ValueError("oracle_scan_fwd rejected its arguments")
     return out, last
+
+
+def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, delta_bias=None, delta_softplus=True,
+             initial_state=None, dlast_state=None, nthreads=0, lib=None):
+    """Gradients of ``scan_fwd`` in fp64, given dout = dL/dout (batch, seqlen,
+    dim) and optionally dlast_state = dL/dlast_state (batch, dim, dstate).
+    Returns a dict with dx, ddelta, dA, dB, dC, dD, dz (None without z),
+    ddelta_bias and dinitial_state (gradients w.r.t. D, the bias and the
+    initial state are returned whether or not those inputs were given: they
+    are the gradients at zero)."""
+    x = _f64(x)
+    bsz, seqlen, dim = x.shape
+    A = _f64(A)
+    dstate = A.shape[1]
+    delta = _f64(delta, x.shape)
+    B = _f64(B, (bsz, seqlen, dstate))
+    C = _f64(C, (bsz, seqlen, dstate))
+    D = _f64(D, (dim,))
+    z = _f64(z, x.shape)
+    delta_bias = _f64(delta_bias, (dim,))
+    initial_state = _f64(initial_state, (bsz, dim, dstate))
+    dout = _f64(dout, x.shape)
+    dlast_state = _f64(dlast_state, (bsz, dim, dstate))
+    g = {k: np.empty(sh, dtype=np.float64) for k, sh in (
+        ("dx", x.shape), ("ddelta", x.shape), ("dA", (dim, dstate)), ("dB", B.shape),
+        ("dC", C.shape), ("dD", (dim,)), ("ddelta_bias", (dim,)),
+        ("dinitial_state", (bsz, dim, dstate)))}
+    g["dz"] = np.empty(x.shape, dtype=np.float64) if z is not None else None
+    rc = (lib or load()).oracle_scan_bwd(
+        bsz, seqlen, dim, dstate, _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+        _ptr(z), _ptr(delta_bias), int(bool(delta_softplus)), _ptr(initial_state), _ptr(dout),
+        _ptr(dlast_state), _ptr(g["dx"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]),
+        _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]),
+        _ptr(g["dinitial_state"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_scan_bwd rejected its arguments")
+    return g
 
 
 def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,

@@ -41,6 +41,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -199,6 +200,174 @@ int oracle_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width,
             }
         }
     }
+    return 0;
+}
+
+/* Gradients of oracle_scan_fwd: the loop of that function differentiated
+ * by hand in reverse mode (the backward half of training the selective SSM:
+ * "Mamba的三大创新", stage 2, the parallel training of the recurrence; the
+ * gradients of the same recurrence, run backwards in time).
+ *
+ * Given dout = dL/dout (batch, seqlen, dim) and optionally
+ * dlast = dL/dlast_state (batch, dim, dstate), with, per (b, d) and time t,
+ *   u_t = delta + bias,  Delta_t = softplus(u_t) (or u_t),
+ *   dA_{t,n} = exp(Delta_t A_n),  h_{t,n} = dA_{t,n} h_{t-1,n} + Delta_t B_{t,n} x_t,
+ *   yc_t = sum_n C_{t,n} h_{t,n} + D x_t,  out_t = yc_t silu(z_t),
+ * time runs backwards carrying g_n = dL/dh_{t,n} (starting from dlast):
+ *   dyc = dout_t silu(z_t);     dz_t = dout_t yc_t silu'(z_t)
+ *   g_n += dyc C_{t,n};         dC_{t,n} += dyc h_{t,n};  dD += dyc x_t;  dx_t = dyc D
+ *   dDelta_t = sum_n g_n (B_{t,n} x_t + A_n dA_{t,n} h_{t-1,n})
+ *   dA_n += g_n Delta_t dA_{t,n} h_{t-1,n};   dB_{t,n} += g_n Delta_t x_t
+ *   dx_t += Delta_t sum_n g_n B_{t,n};        g_n *= dA_{t,n}   (now dL/dh_{t-1,n})
+ *   du_t = dDelta_t sigmoid(u_t) (or dDelta_t);  ddelta_t = du_t;  dbias += du_t
+ * and after t = 0, dinitial_state = g.  silu'(z) = s (1 + z (1 - s)), s = sigmoid(z).
+ *
+ * Outputs are written, not accumulated: dx, ddelta (batch, seqlen, dim);
+ * dA (dim, dstate); dB, dC (batch, seqlen, dstate); dD, ddelta_bias (dim);
+ * dz (batch, seqlen, dim); dinitial_state (batch, dim, dstate).  Any output
+ * pointer may be NULL (not computed); dz must be NULL when z is.
+ * Sums over channels (dB, dC) and over sequences (dA, dD, ddelta_bias) are
+ * formed per thread over a fixed range of channels, then added in thread order. */
+int oracle_scan_bwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                    const double *x, const double *delta, const double *A,
+                    const double *B, const double *C, const double *D,
+                    const double *z, const double *delta_bias, int delta_softplus,
+                    const double *initial_state, const double *dout, const double *dlast,
+                    double *dx, double *ddelta, double *dA, double *dB, double *dC,
+                    double *dD, double *dz, double *ddelta_bias, double *dinitial_state,
+                    int nthreads)
+{
+    if (batch < 0 || seqlen < 0 || dim < 0 || dstate <= 0 || dstate > 4096)
+        return -1;
+    if (!x || !delta || !A || !B || !C || !dout || (dz && !z))
+        return -1;
+    const int64_t nchan = batch * dim;
+    const int64_t nbc = batch * seqlen * dstate;     /* elements of dB (and dC) */
+    int nt = 1;
+#ifdef _OPENMP
+    nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#endif
+    if (nt < 1)
+        nt = 1;
+    if ((int64_t)nt > nchan && nchan > 0)
+        nt = (int)nchan;
+    /* per-thread partial sums: dB, dC | dA | dD | dbias */
+    const int64_t per = 2 * nbc + dim * dstate + 2 * dim;
+    double *part = (double *)calloc((size_t)nt * (size_t)per, sizeof(double));
+    double *hist = (double *)malloc((size_t)nt * (size_t)(seqlen + 1) * (size_t)dstate * sizeof(double));
+    if (!part || !hist) {
+        free(part);
+        free(hist);
+        return -1;
+    }
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nt)
+#endif
+    {
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        double *pB = part + (int64_t)tid * per;
+        double *pC = pB + nbc;
+        double *pA = pC + nbc;
+        double *pD = pA + dim * dstate;
+        double *pbias = pD + dim;
+        /* h_{t,n} for t = -1 .. seqlen-1 at hs[(t + 1) * dstate + n] */
+        double *hs = hist + (int64_t)tid * (seqlen + 1) * dstate;
+        double g[4096];
+        const int64_t lo = nchan * tid / nt, hi = nchan * (tid + 1) / nt;
+        for (int64_t ch = lo; ch < hi; ++ch) {
+            const int64_t b = ch / dim;
+            const int64_t d = ch % dim;
+            const double bias = delta_bias ? delta_bias[d] : 0.0;
+            /* forward again, keeping every state */
+            for (int64_t n = 0; n < dstate; ++n)
+                hs[n] = initial_state ? initial_state[(b * dim + d) * dstate + n] : 0.0;
+            for (int64_t t = 0; t < seqlen; ++t) {
+                const int64_t tok = (b * seqlen + t) * dim + d;
+                const int64_t row = (b * seqlen + t) * dstate;
+                const double u = delta[tok] + bias;
+                const double dt = delta_softplus ? oracle_softplus(u) : u;
+                for (int64_t n = 0; n < dstate; ++n)
+                    hs[(t + 1) * dstate + n] = exp(dt * A[d * dstate + n]) * hs[t * dstate + n]
+                                               + dt * B[row + n] * x[tok];
+            }
+            /* backwards in time */
+            for (int64_t n = 0; n < dstate; ++n)
+                g[n] = dlast ? dlast[(b * dim + d) * dstate + n] : 0.0;
+            for (int64_t t = seqlen - 1; t >= 0; --t) {
+                const int64_t tok = (b * seqlen + t) * dim + d;
+                const int64_t row = (b * seqlen + t) * dstate;
+                const double *h = hs + (t + 1) * dstate;      /* h_t */
+                const double *hp = hs + t * dstate;           /* h_{t-1} */
+                const double xv = x[tok];
+                const double u = delta[tok] + bias;
+                const double dt = delta_softplus ? oracle_softplus(u) : u;
+                double yc = D ? D[d] * xv : 0.0;
+                for (int64_t n = 0; n < dstate; ++n)
+                    yc += C[row + n] * h[n];
+                double dyc = dout[tok];
+                if (z) {
+                    const double s = 1.0 / (1.0 + exp(-z[tok]));
+                    dyc = dout[tok] * z[tok] * s;
+                    if (dz)
+                        dz[tok] = dout[tok] * yc * s * (1.0 + z[tok] * (1.0 - s));
+                }
+                pD[d] += dyc * xv;
+                double dxv = dyc * (D ? D[d] : 0.0);
+                double ddt = 0.0;
+                for (int64_t n = 0; n < dstate; ++n) {
+                    const double a = A[d * dstate + n];
+                    const double dAn = exp(dt * a);
+                    g[n] += dyc * C[row + n];
+                    pC[row + n] += dyc * h[n];
+                    ddt += g[n] * (B[row + n] * xv + a * dAn * hp[n]);
+                    pA[d * dstate + n] += g[n] * dt * dAn * hp[n];
+                    pB[row + n] += g[n] * dt * xv;
+                    dxv += dt * g[n] * B[row + n];
+                    g[n] *= dAn;
+                }
+                const double du = delta_softplus ? ddt / (1.0 + exp(-u)) : ddt;
+                if (dx)
+                    dx[tok] = dxv;
+                if (ddelta)
+                    ddelta[tok] = du;
+                pbias[d] += du;
+            }
+            if (dinitial_state)
+                for (int64_t n = 0; n < dstate; ++n)
+                    dinitial_state[(b * dim + d) * dstate + n] = g[n];
+        }
+    }
+    /* add the per-thread partial sums in thread order */
+    for (int64_t i = 0; i < nbc; ++i) {
+        double sb = 0.0, sc = 0.0;
+        for (int tid = 0; tid < nt; ++tid) {
+            sb += part[(int64_t)tid * per + i];
+            sc += part[(int64_t)tid * per + nbc + i];
+        }
+        if (dB)
+            dB[i] = sb;
+        if (dC)
+            dC[i] = sc;
+    }
+    for (int64_t i = 0; i < dim * dstate + 2 * dim; ++i) {
+        double s = 0.0;
+        for (int tid = 0; tid < nt; ++tid)
+            s += part[(int64_t)tid * per + 2 * nbc + i];
+        if (i < dim * dstate) {
+            if (dA)
+                dA[i] = s;
+        } else if (i < dim * dstate + dim) {
+            if (dD)
+                dD[i - dim * dstate] = s;
+        } else if (ddelta_bias) {
+            ddelta_bias[i - dim * dstate - dim] = s;
+        }
+    }
+    free(part);
+    free(hist);
     return 0;
 }
 

@@ -285,6 +285,113 @@ def pin_conv_split(lib):
         assert np.array_equal(s2, st_out)
 
 
+# ------------------------------------------------------------------ backward
+# The gradients of the scan (oracle.scan_bwd) are pinned by differentiating
+# the forward numerically and by torch's autograd on an fp64 loop of its own.
+
+_BWD_KEYS = (("x", "dx"), ("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC"),
+             ("D", "dD"), ("z", "dz"), ("delta_bias", "ddelta_bias"),
+             ("initial_state", "dinitial_state"))
+
+
+def _bwd_problem(seed, bsz=2, L=5, dim=3, N=4, **kw):
+    p = rand_problem(seed, bsz=bsz, L=L, dim=dim, N=N)
+    r = np.random.default_rng(seed + 1)
+    dout = r.standard_normal((bsz, L, dim))
+    dlast = r.standard_normal((bsz, dim, N))
+    for k, v in kw.items():
+        p[k] = v
+    return p, dout, dlast
+
+
+def _loss(lib, p, dout, dlast, softplus=True):
+    out, last = oracle.scan_fwd(lib=lib, delta_softplus=softplus, **p)
+    return float(np.sum(out * dout) + (np.sum(last * dlast) if dlast is not None else 0.0))
+
+
+# G1 -- central differences of the forward, coordinate by coordinate
+#       (error O(eps^2) + roundoff/eps, about 1e-9 here)
+def pin_bwd_finite_differences(lib):
+    for case in range(3):
+        if case == 0:
+            p, dout, dlast = _bwd_problem(31)
+            softplus = True
+        elif case == 1:     # no optional inputs, no final-state gradient
+            p, dout, dlast = _bwd_problem(32, z=None, D=None, delta_bias=None, initial_state=None)
+            dlast = None
+            softplus = True
+        else:               # raw step sizes (positive), no softplus
+            p, dout, dlast = _bwd_problem(33)
+            p["delta"] = np.abs(p["delta"]) * 0.3 + 0.05
+            p["delta_bias"] = None
+            softplus = False
+        g = oracle.scan_bwd(lib=lib, dout=dout, dlast_state=dlast, delta_softplus=softplus, **p)
+        eps = 1e-6
+        for name, gk in _BWD_KEYS:
+            if p.get(name) is None:
+                continue
+            arr = p[name]
+            fd = np.zeros_like(arr)
+            for i in np.ndindex(arr.shape):
+                up, dn = arr.copy(), arr.copy()
+                up[i] += eps
+                dn[i] -= eps
+                fd[i] = (_loss(lib, dict(p, **{name: up}), dout, dlast, softplus)
+                         - _loss(lib, dict(p, **{name: dn}), dout, dlast, softplus)) / (2 * eps)
+            err = np.max(np.abs(g[gk] - fd)) / (1.0 + np.max(np.abs(fd)))
+            assert err < 1e-7, (case, name, err)
+
+
+# G2 -- directional derivative of a longer problem along a random direction
+#       over every input at once: sum_i grad_i v_i = d/de L(theta + e v)
+def pin_bwd_directional(lib):
+    p, dout, dlast = _bwd_problem(34, bsz=2, L=40, dim=5, N=8)
+    g = oracle.scan_bwd(lib=lib, dout=dout, dlast_state=dlast, **p)
+    r = np.random.default_rng(35)
+    v = {name: r.standard_normal(p[name].shape) for name, _ in _BWD_KEYS}
+    eps = 1e-6
+    up = {k: (p[k] + eps * v[k] if k in v else p[k]) for k in p}
+    dn = {k: (p[k] - eps * v[k] if k in v else p[k]) for k in p}
+    fd = (_loss(lib, up, dout, dlast) - _loss(lib, dn, dout, dlast)) / (2 * eps)
+    an = sum(float(np.sum(g[gk] * v[name])) for name, gk in _BWD_KEYS)
+    assert abs(an - fd) < 1e-7 * (1.0 + abs(fd)), (an, fd)
+
+
+# G3 -- torch autograd through an fp64 loop written here (a second
+#       implementation of the forward, differentiated by the library)
+def pin_bwd_autograd(lib):
+    import torch
+    p, dout, dlast = _bwd_problem(36, bsz=2, L=9, dim=4, N=3)
+    t = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True) for k, v in p.items()}
+    bsz, L, dim = p["x"].shape
+    h = t["initial_state"]                                   # (b, d, n)
+    outs = []
+    for s in range(L):
+        dt = torch.nn.functional.softplus(t["delta"][:, s] + t["delta_bias"])   # (b, d)
+        decay = torch.exp(dt[..., None] * t["A"][None])
+        h = decay * h + (dt * t["x"][:, s])[..., None] * t["B"][:, s][:, None, :]
+        y = (h * t["C"][:, s][:, None, :]).sum(-1) + t["D"] * t["x"][:, s]
+        outs.append(y * torch.nn.functional.silu(t["z"][:, s]))
+    out = torch.stack(outs, 1)
+    loss = (out * torch.tensor(dout)).sum() + (h * torch.tensor(dlast)).sum()
+    loss.backward()
+    g = oracle.scan_bwd(lib=lib, dout=dout, dlast_state=dlast, **p)
+    for name, gk in _BWD_KEYS:
+        ref = t[name].grad.numpy()
+        assert np.max(np.abs(g[gk] - ref)) < 1e-11 * (1.0 + np.max(np.abs(ref))), name
+
+
+# G4 -- the per-thread partial sums: any thread count gives the same
+#       gradients up to fp64 rounding
+def pin_bwd_thread_count(lib):
+    p, dout, dlast = _bwd_problem(37, bsz=3, L=16, dim=7, N=4)
+    g1 = oracle.scan_bwd(lib=lib, dout=dout, dlast_state=dlast, nthreads=1, **p)
+    g3 = oracle.scan_bwd(lib=lib, dout=dout, dlast_state=dlast, nthreads=3, **p)
+    for _, gk in _BWD_KEYS:
+        assert np.max(np.abs(g1[gk] - g3[gk])) < 1e-12 * (1.0 + np.max(np.abs(g1[gk]))), gk
+
+
 ALL_PINS = [pin_closed_form, pin_prefix_sum, pin_lti_convolution, pin_small_delta,
             pin_large_delta, pin_split_carry, pin_decode_equals_scan, pin_first_order_iir,
-            pin_worked_example, pin_nonlinearities, pin_conv_numpy, pin_conv_taps, pin_conv_split]
+            pin_worked_example, pin_nonlinearities, pin_conv_numpy, pin_conv_taps, pin_conv_split,
+            pin_bwd_finite_differences, pin_bwd_directional, pin_bwd_autograd, pin_bwd_thread_count]

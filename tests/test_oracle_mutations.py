@@ -40,6 +40,20 @@ MUTATIONS = {
     "conv_state_ignored": ("v = conv_state_in ? conv_state_in[(b * dim + d) * H + (H + tt)] : 0.0;\n                    acc +=",
                            "v = 0.0;\n                    acc +="),
     "conv_taps_reversed": ("acc += w[d * width + k] * v;", "acc += w[d * width + (width - 1 - k)] * v;"),
+    # backward
+    "bwd_no_decay_propagation": ("                    g[n] *= dAn;\n", "\n"),
+    "bwd_decay_term_uses_h_t": ("ddt += g[n] * (B[row + n] * xv + a * dAn * hp[n]);",
+                                "ddt += g[n] * (B[row + n] * xv + a * dAn * h[n]);"),
+    "bwd_softplus_derivative_sign": ("ddt / (1.0 + exp(-u))", "ddt / (1.0 + exp(u))"),
+    "bwd_skip_gradient_dropped": ("double dxv = dyc * (D ? D[d] : 0.0);", "double dxv = 0.0;"),
+    "bwd_final_state_gradient_ignored": ("g[n] = dlast ? dlast[(b * dim + d) * dstate + n] : 0.0;",
+                                         "g[n] = 0.0;"),
+    "bwd_gate_derivative": ("s * (1.0 + z[tok] * (1.0 - s))", "s * (1.0 + z[tok] * s)"),
+    "bwd_dC_lagged": ("pC[row + n] += dyc * h[n];", "pC[row + n] += dyc * hp[n];"),
+    "bwd_dA_missing_delta": ("pA[d * dstate + n] += g[n] * dt * dAn * hp[n];",
+                             "pA[d * dstate + n] += g[n] * dAn * hp[n];"),
+    "bwd_readout_gradient_dropped": ("                    g[n] += dyc * C[row + n];\n                    pC",
+                                 "                    pC"),
 }
 
 
