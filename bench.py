@@ -17,6 +17,8 @@ needed).  Prints ONE JSON line (rank 0):
                buffers, host->device and device->host copies inside the timing
   cpu_baseline the fp64 oracle on the host cores, on a bounded sample
   decode       the one-token state update (256 x 5120 x 16, 128 chained steps)
+  bwd          the gradients of the same scan (ssm_scan_bwd: states
+               recomputed, dx/ddelta/dz/dA/dB/dC/dD/dbias), time per call
   conv_scan    the Mamba block's causal conv (width 4, SiLU) in front of the
                same scan: fused (ssm_conv_scan_fwd, one pass) against the two
                separate calls (ssm_conv1d_fwd writing x_conv, then ssm_scan_fwd)
@@ -66,10 +68,11 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--conv-width", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target wall time of the oracle sample")
-    ap.add_argument("--only", choices=["all", "scan", "decode", "conv"], default="all",
+    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd"], default="all",
                     help="run only the prefill scan part or only the decode part (profiling)")
     return ap.parse_args()
 
@@ -298,11 +301,13 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps(line), flush=True)
         return
-    if args.only == "conv":
+    if args.only in ("conv", "bwd"):
         peak, peak_kind = peaks()
         w = workload_by_name(args.workload)
         inp = synth.make_scan_inputs(w, device=str(dev))
-        line = {"conv_scan": run_conv(args, w, inp, dev, peak, peak_kind),
+        part = run_conv if args.only == "conv" else run_bwd
+        line = {("conv_scan" if args.only == "conv" else "bwd"): part(args, w, inp, dev, peak,
+                                                                         peak_kind),
                 "source_hash": kernel_source_hash()}
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -379,6 +384,8 @@ def run_ours(args, world, rank, local):
         line["decode"] = run_decode(args, dev, peak, peak_kind)
     if not args.no_conv and args.only == "all":
         line["conv_scan"] = run_conv(args, w, inp, dev, peak, peak_kind)
+    if not args.no_bwd and args.only == "all":
+        line["bwd"] = run_bwd(args, w, inp, dev, peak, peak_kind)
     if rank == 0 and world == 1 and not args.no_cpu:
         val, dt, nchan, cores = time_oracle(inp, w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -507,6 +514,51 @@ def run_conv(args, w, inp, dev, peak, peak_kind):
                                 "frac": conv_gbs / peak, "peak_kind": peak_kind,
                                 "algorithmic_bytes_per_launch": conv_bytes,
                                 "traffic": profiled_traffic("conv1d_fwd_" + w.name)}}
+
+
+def run_bwd(args, w, inp, dev, peak, peak_kind):
+    """ssm_scan_bwd over workload w with a random dout (no final-state
+    gradient): CUDA events per call on the launching stream."""
+    from selective_state_space_137_b300 import binding
+    g = torch.Generator(device=dev).manual_seed(w.seed + 77)
+    dout = torch.randn(inp["x"].shape, generator=g, device=dev).to(inp["x"].dtype)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dx, ddelta, dz = (torch.empty_like(inp["x"]) for _ in range(3))
+    dA = torch.empty((w.dim, w.dstate), **f32)
+    dB = torch.empty((w.batch, w.seqlen, w.dstate), **f32)
+    dC = torch.empty_like(dB)
+    dD, dbias = torch.empty(w.dim, **f32), torch.empty(w.dim, **f32)
+    desc = binding.make_desc(w.batch, w.seqlen, w.dim, w.dstate, inp["x"].dtype)
+    need = binding.ssm_scan_bwd_workspace_size(desc)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        st = binding.ssm_scan_bwd(desc, inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                  inp["D"], inp["z"], inp["delta_bias"], None, dout, None, dx,
+                                  ddelta, dA, dB, dC, dD, dz, dbias, None, ws, ws.numel(), stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_scan_bwd")
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    steps = max(3, min(args.steps, 10))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        call()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]))
+    e = inp["x"].element_size()
+    # read x, delta, z, dout, B, C; write dx, ddelta, dz (io) and dB, dC (fp32)
+    algo = (4 + 3) * w.tokens * e + 2 * w.batch * w.seqlen * w.dstate * (e + 4)
+    return {"workload": w.name, "ms": ms, "elements_per_s": w.tokens / (ms * 1e-3),
+            "items_per_s": w.items / (ms * 1e-3), "workspace_bytes": need,
+            "algorithmic_bytes_per_call": algo, "gb_per_s": algo / (ms * 1e-3) / 1e9,
+            "hbm_frac": algo / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+            "ms_vs_forward_note": "forward of the same workload: roofline.kernel_ms"}
 
 
 def run_decode(args, dev, peak, peak_kind):

@@ -123,6 +123,38 @@ SSM_API ssm_status ssm_state_update(const ssm_scan_desc *desc, float *state,
                             const void *z, const float *delta_bias,
                             void *out, void *stream);
 
+/* Gradients of ssm_scan_fwd (the backward half of training; "Mamba的三大创新",
+ * stage 2, parallel training of the recurrence).  The states are recomputed
+ * from the inputs (stored every 16 steps in the workspace), never kept from
+ * the forward call.  With L the loss:
+ *   dout          : (batch, seqlen, dim) io, dL/dout
+ *   dlast_state   : (batch, dim, dstate) fp32, dL/dlast_state, or NULL (zero)
+ * the forward's inputs x, delta, A, B, C, D, z, delta_bias, initial_state as
+ * given to ssm_scan_fwd, and outputs (written, never accumulated):
+ *   dx, ddelta    : (batch, seqlen, dim) io      -- ddelta is dL/d(delta before
+ *                                                   bias and softplus)
+ *   dz            : (batch, seqlen, dim) io, or NULL (not computed); NULL when z is NULL
+ *   dA            : (dim, dstate) fp32
+ *   dB, dC        : (batch, seqlen, dstate) fp32 (sums over the channels)
+ *   dD, ddelta_bias : (dim) fp32, or NULL (not computed); computed also when
+ *                   D / delta_bias is NULL (the gradient at zero)
+ *   dinitial_state: (batch, dim, dstate) fp32, or NULL
+ * workspace: ssm_scan_bwd_workspace_size(desc) bytes, 16-byte aligned (about
+ * 0.19 x the bytes of (batch, seqlen, dim, dstate) fp32 states, plus the
+ * per-CTA dB/dC partials).  Every sum is formed in a fixed order, so results
+ * are bit-identical from run to run.  Outputs must not alias inputs.
+ * Elements must be aligned to their size; B and C at 4-element alignment take
+ * vector loads. */
+SSM_API size_t ssm_scan_bwd_workspace_size(const ssm_scan_desc *desc);
+SSM_API ssm_status ssm_scan_bwd(const ssm_scan_desc *desc, const void *x, const void *delta,
+                                const float *A, const void *B, const void *C, const float *D,
+                                const void *z, const float *delta_bias,
+                                const float *initial_state, const void *dout,
+                                const float *dlast_state, void *dx, void *ddelta, float *dA,
+                                float *dB, float *dC, float *dD, void *dz, float *ddelta_bias,
+                                float *dinitial_state, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
 /* Causal depthwise convolution applied to x before the SSM in the Mamba block
  * ("Mamba的三大创新", simplified-architecture section: a convolution gives each
  * token its neighbours before the SSM; the unite.ai overview: a causal Conv1d

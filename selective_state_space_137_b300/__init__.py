@@ -1,6 +1,7 @@
 """B300-native selective state-space scan (Mamba S6).
 
-Prefill (``scan_fwd``) and decode (``state_update``), and the same two with
+Prefill (``scan_fwd``), its gradients (``scan_bwd``), decode
+(``state_update``), and prefill and decode with
 the Mamba block's causal conv fused in front (``conv_scan_fwd``,
 ``conv_state_update``; ``conv1d_fwd`` is the conv alone), run in hand-written
 CUDA kernels for sm_103a behind the C ABI of ``include/ssm.h``
@@ -15,7 +16,8 @@ from __future__ import annotations
 
 import importlib
 
-_OPS = ("scan_fwd", "state_update", "conv1d_fwd", "conv_scan_fwd", "conv_state_update")
+_OPS = ("scan_fwd", "scan_bwd", "state_update", "conv1d_fwd", "conv_scan_fwd",
+        "conv_state_update")
 __all__ = list(_OPS) + ["binding", "synth", "ops"]
 
 

@@ -21,7 +21,8 @@ SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
             "ssm_scan_plan", "ssm_status_string", "ssm_version", "ssm_scan_fwd_noalloc",
             "ssm_get_device_status", "ssm_selftest_wait_timeout", "ssm_conv1d_fwd",
-            "ssm_conv_scan_fwd", "ssm_conv_state_update")
+            "ssm_conv_scan_fwd", "ssm_conv_state_update", "ssm_scan_bwd_workspace_size",
+            "ssm_scan_bwd")
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -61,6 +62,11 @@ def _load():
     lib.ssm_state_update.argtypes = [dp, fp, vp, vp, fp, vp, vp, fp, vp, fp, vp, vp]
     lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
     lib.ssm_scan_fwd_noalloc.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, vp]
+    lib.ssm_scan_bwd_workspace_size.restype = sz
+    lib.ssm_scan_bwd_workspace_size.argtypes = [dp]
+    lib.ssm_scan_bwd.restype = ctypes.c_int
+    lib.ssm_scan_bwd.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, fp, vp, fp, vp, vp, fp, fp, fp,
+                                 fp, vp, fp, fp, vp, sz, vp]
     cp = ctypes.POINTER(ssm_conv_desc)
     lib.ssm_conv1d_fwd.restype = ctypes.c_int
     lib.ssm_conv1d_fwd.argtypes = [dp, cp, vp, fp, fp, fp, vp, fp, vp]
@@ -198,3 +204,19 @@ def ssm_conv_state_update(desc, conv, conv_state, conv_w, conv_bias, state, x, d
                                      _ptr(conv_w), _ptr(conv_bias), _ptr(state), _ptr(x),
                                      _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                                      _ptr(delta_bias), _ptr(out), _stream(stream))
+
+
+def ssm_scan_bwd_workspace_size(desc: ssm_scan_desc) -> int:
+    return int(lib.ssm_scan_bwd_workspace_size(ctypes.byref(desc)))
+
+
+def ssm_scan_bwd(desc, x, delta, A, B, C, D, z, delta_bias, initial_state, dout, dlast_state, dx,
+                 ddelta, dA, dB, dC, dD, dz, ddelta_bias, dinitial_state, workspace,
+                 workspace_bytes, stream=None) -> int:
+    """Gradients of the scan (the states are recomputed); status code out."""
+    return lib.ssm_scan_bwd(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                            _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(initial_state), _ptr(dout),
+                            _ptr(dlast_state), _ptr(dx), _ptr(ddelta), _ptr(dA), _ptr(dB),
+                            _ptr(dC), _ptr(dD), _ptr(dz), _ptr(ddelta_bias),
+                            _ptr(dinitial_state), _ptr(workspace), int(workspace_bytes),
+                            _stream(stream))

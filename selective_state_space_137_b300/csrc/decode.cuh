@@ -26,6 +26,7 @@ struct DecodeParams {
     void* out;
     int64_t batch, dim;
     int softplus;
+    bool vec = false;   // A 16-byte and B, C (4 x element)-byte aligned: vector loads
     // causal conv in front (read only by kernels instantiated with CONV)
     float* conv_state = nullptr;            // (batch, dim, conv_width - 1), shifted in place
     const float* conv_w = nullptr;          // (dim, conv_width)
@@ -40,10 +41,12 @@ struct DecodeShape {
     static constexpr int SPL = N / LPC;                               // states per lane
 };
 
-// SPL consecutive io elements as fp32 (16-, 8- or 4-byte loads when SPL allows).
+// SPL consecutive io elements as fp32: 16- or 8-byte loads when SPL allows
+// and the caller's pointers are aligned for them (`vec`, uniform per launch),
+// element loads otherwise.
 template <int SPL>
-__device__ __forceinline__ void load_vec(const float* p, float* f) {
-    if (SPL % 4 == 0) {
+__device__ __forceinline__ void load_vec(const float* p, float* f, bool vec) {
+    if (SPL % 4 == 0 && vec) {
 #pragma unroll
         for (int j = 0; j < SPL; j += 4) {
             const float4 v = __ldg(reinterpret_cast<const float4*>(p + j));
@@ -55,8 +58,8 @@ __device__ __forceinline__ void load_vec(const float* p, float* f) {
     }
 }
 template <int SPL>
-__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f) {
-    if (SPL % 4 == 0) {
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f, bool vec) {
+    if (SPL % 4 == 0 && vec) {
 #pragma unroll
         for (int j = 0; j < SPL; j += 4) {
             const uint2 v = __ldg(reinterpret_cast<const uint2*>(p + j));
@@ -103,9 +106,9 @@ __global__ void __launch_bounds__(256, CONV ? 4 : 8) state_update_kernel(DecodeP
 #pragma unroll
         for (int j = 0; j < SPL; ++j) h[j] = st[j];
     }
-    load_vec<SPL>(p.A + (int64_t)d * N + sub * SPL, a);
-    load_vec<SPL>(Bm + b * N + sub * SPL, bv);
-    load_vec<SPL>(Cm + b * N + sub * SPL, cv);
+    load_vec<SPL>(p.A + (int64_t)d * N + sub * SPL, a, p.vec);
+    load_vec<SPL>(Bm + b * N + sub * SPL, bv, p.vec);
+    load_vec<SPL>(Cm + b * N + sub * SPL, cv, p.vec);
     float xv = load_f32(x + ch);
     if (CONV) {
         // x_conv from the K-1 stored inputs and the new one; the state shift is

@@ -1,0 +1,780 @@
+// scan_bwd.cuh -- gradients of the selective scan (the backward half of
+// training), recomputing the states instead of storing them.
+//
+// Forward, per (b, d) and time t (the recurrent mode of "Mamba的三大创新",
+// stage 2):  Delta_t = softplus(delta_t + bias),  dA_t = exp(Delta_t A),
+//   h_t = dA_t h_{t-1} + Delta_t B_t x_t,  yc_t = C_t . h_t + D x_t,
+//   out_t = yc_t silu(z_t).
+// Backward, time reversed, with g_t = dL/dh_t and G = dA_{t+1} g_{t+1}:
+//   dyc = dout silu(z),  g_t = dyc C_t + G,   dz = dout yc silu'(z)
+//   dC_t += dyc h_t,  dB_t += g_t Delta_t x_t                  (sums over d)
+//   dx_t = dyc D + Delta_t sum_n g B,  dDelta_t = x_t sum_n g B + sum_n A g dA_t h_{t-1}
+//   dA += Delta_t g dA_t h_{t-1},  dD += dyc x,  dbias += ddelta  (sums over b, t)
+//   ddelta_t = dDelta_t sigmoid(delta_t + bias)  (softplus' = sigmoid)
+//
+// Launches (K time chunks; K = 1 needs only the last two):
+//   1. forward aggregate + carry (scan_generic.cuh): the state at every chunk start;
+//   2. scan_bwd_agg_kernel: per chunk k >= 1, E_k = dA_{t0} g_{t0} computed with
+//      nothing coming from the right, and the chunk's sum of Delta;
+//   3. scan_bwd_carry_kernel: right to left, the term e_k that chunk k receives
+//      from chunk k+1:  e_{K-1} = dlast,  e_{k-1} = E_k + exp(A sum_k Delta) e_k;
+//   4. scan_bwd_kernel: per chunk, a forward sweep that stores the state at every
+//      16-step tile start, then tiles in reverse: the tile's 16 states are
+//      recomputed into registers and the reverse step runs over them;
+//   5. scan_bwd_reduce_kernel: dB, dC (sums of the per-CTA partials over the
+//      channel blocks) and dA, dD, dbias (sums over sequences and chunks).
+// Every sum is formed in a fixed order: the result does not depend on timing.
+//
+// Thread layout of scan_bwd_kernel: LPC lanes per channel, SPL states per lane
+// (N = 16: 4 x 4), CPW channels per warp, 8 warps (CH channels) per CTA.  The
+// per-step dB/dC contributions are summed over the warp's channels by
+// recursive halving (each round a lane keeps half of its values and adds the
+// partner's half), then over the CTA's warps through shared memory at the end
+// of each tile.
+#pragma once
+#include "common.cuh"
+#include "scan_tiled.cuh"   // softplus_tiled, silu_tiled, round_up, load1
+#include "tma.cuh"
+
+namespace ssm {
+
+struct BwdParams {
+    const void* x;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    const float* initial_state;
+    const void* dout;
+    const float* dlast;
+    void* dx;
+    void* ddelta;
+    void* dz;
+    float* dinit;
+    // workspace
+    const float* fstart;   // (batch, K, dim, N): state at each chunk start (K > 1)
+    float* ebuf;           // (batch, K, dim, N): E_k, then the incoming term e_k
+    float* bdsum;          // (batch, K, dim): sum of Delta over chunk k
+    float* ckpt;           // (batch, ntiles, dim, N): state at each tile start
+    float* pBC;            // (nblk, batch, seqlen, 2N): per-CTA dB | dC
+    float* pA;             // (batch * K, dim, N)
+    float* pD;             // (batch * K, dim)
+    float* pbias;          // (batch * K, dim)
+    int64_t batch, seqlen, dim, chunk_len, ntiles;
+    int nchunk;
+    int softplus;
+    bool vec;              // B and C bases aligned for SPL-element vector loads
+};
+
+constexpr int kBwdT = 16;       // steps per tile (checkpoint spacing)
+constexpr int kBwdWarps = 8;
+
+template <int N>
+struct BwdShape {
+    static constexpr int LPC = N >= 4 ? (N / 4 > 32 ? 32 : N / 4) : 1;   // lanes per channel
+    static constexpr int SPL = N / LPC;                                  // states per lane
+    static constexpr int CPW = 32 / LPC;                                 // channels per warp
+    static constexpr int CH = CPW * kBwdWarps;                           // channels per CTA
+    static constexpr int V = 2 * SPL;                                    // dB | dC values per lane
+    static constexpr int SMEM = kBwdWarps * kBwdT * 2 * N * 4;
+};
+
+template <int SPL, typename IO>
+__device__ __forceinline__ void bwd_load(const IO* p, float* f, bool vec) {
+    if (SPL % 4 == 0 && vec) {
+#pragma unroll
+        for (int j = 0; j < SPL; j += 4) {
+            if (sizeof(IO) == 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(p + j));
+                f[j] = v.x; f[j + 1] = v.y; f[j + 2] = v.z; f[j + 3] = v.w;
+            } else {
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(p + j));
+                f[j] = __uint_as_float(v.x << 16); f[j + 1] = __uint_as_float(v.x & 0xffff0000u);
+                f[j + 2] = __uint_as_float(v.y << 16); f[j + 3] = __uint_as_float(v.y & 0xffff0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) f[j] = load_f32(p + j);
+    }
+}
+
+// The same from shared memory (plain loads; __ldg is for global memory only).
+template <int SPL, typename IO>
+__device__ __forceinline__ void bwd_load_smem(const IO* p, float* f) {
+    if (SPL % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < SPL; j += 4) {
+            if (sizeof(IO) == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(p + j);
+                f[j] = v.x; f[j + 1] = v.y; f[j + 2] = v.z; f[j + 3] = v.w;
+            } else {
+                const uint2 v = *reinterpret_cast<const uint2*>(p + j);
+                f[j] = __uint_as_float(v.x << 16); f[j + 1] = __uint_as_float(v.x & 0xffff0000u);
+                f[j + 2] = __uint_as_float(v.y << 16); f[j + 3] = __uint_as_float(v.y & 0xffff0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < SPL; ++j) f[j] = load1(p + j);
+    }
+}
+
+// Sum over the lanes of a warp that hold the same state slice (the channel
+// bits of the lane index, xor offsets LPC .. 16).  On return lane holds
+// `held` = V >> r values at v[0 .. held), the sums of the original values
+// base + i, where base is returned; when the channel bits outnumber the
+// halving rounds, the extra rounds add whole arrays (results replicated).
+template <int V, int LPC>
+__device__ __forceinline__ int reduce_channels(float (&v)[V], int lane) {
+    int base = 0;
+    int cnt = V;
+#pragma unroll
+    for (int o = 16; o >= LPC; o >>= 1) {
+        if (cnt > 1) {
+            const bool up = (lane & o) != 0;
+            const int half = cnt / 2;
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                if (i < half) {
+                    const float send = up ? v[i] : v[half + i];
+                    const float keep = up ? v[half + i] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            if (up) base += half;
+            cnt = half;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+    }
+    return base;
+}
+
+// Sum of a per-lane value over the LPC lanes of one channel.
+template <int LPC>
+__device__ __forceinline__ float reduce_slices(float v) {
+#pragma unroll
+    for (int o = LPC / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float sigmoid_fast(float u) {
+    return __frcp_rn(1.f + ex2_sfu(-u * kLog2e));
+}
+
+// ---------------------------------------------------------------------------
+// 2. Backward aggregate of chunk k >= 1: E_k with nothing from the right.
+template <typename IO, int N>
+__global__ void __launch_bounds__(128) scan_bwd_agg_kernel(BwdParams p) {
+    const int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (d >= p.dim) return;
+    const int64_t b = blockIdx.y;
+    const int k = blockIdx.z + 1;
+    const int64_t t0 = (int64_t)k * p.chunk_len;
+    int64_t t1 = t0 + p.chunk_len;
+    if (t1 > p.seqlen) t1 = p.seqlen;
+    const IO* delta = static_cast<const IO*>(p.delta);
+    const IO* Cm = static_cast<const IO*>(p.C);
+    const IO* z = static_cast<const IO*>(p.z);
+    const IO* dout = static_cast<const IO*>(p.dout);
+    float a2[N], G[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        a2[n] = __ldg(p.A + d * N + n) * kLog2e;
+        G[n] = 0.f;
+    }
+    const float bias = p.delta_bias ? __ldg(p.delta_bias + d) : 0.f;
+    float dsum = 0.f;
+    for (int64_t t = t1 - 1; t >= t0; --t) {
+        const int64_t tok = (b * p.seqlen + t) * p.dim + d;
+        const float u = load_f32(delta + tok) + bias;
+        const float dt = p.softplus ? softplus_accurate(u) : u;
+        float dyc = load_f32(dout + tok);
+        if (z) dyc *= silu_accurate(load_f32(z + tok));
+        const IO* crow = Cm + (b * p.seqlen + t) * N;
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            const float g = fmaf(dyc, load_f32(crow + n), G[n]);
+            G[n] = ex2_sfu(dt * a2[n]) * g;
+        }
+        dsum += dt;
+    }
+    float* e = p.ebuf + ((b * p.nchunk + k) * p.dim + d) * N;
+#pragma unroll
+    for (int n = 0; n < N; ++n) e[n] = G[n];
+    p.bdsum[(b * p.nchunk + k) * p.dim + d] = dsum;
+}
+
+// 3. Right-to-left combine of the chunk terms, per (b, d, n).
+__global__ void scan_bwd_carry_kernel(const float* __restrict__ A, const float* __restrict__ dlast,
+                                      float* ebuf, const float* __restrict__ bdsum, int64_t batch,
+                                      int64_t dim, int N, int nchunk) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= batch * dim * N) return;
+    const int n = (int)(i % N);
+    const int64_t d = (i / N) % dim;
+    const int64_t b = i / (N * dim);
+    const float a2 = A[d * N + n] * kLog2e;
+    float e = dlast ? dlast[i] : 0.f;
+    for (int k = nchunk - 1; k >= 0; --k) {
+        float* slot = ebuf + ((b * nchunk + k) * dim + d) * N + n;
+        const float Ek = k > 0 ? *slot : 0.f;
+        *slot = e;                                  // what chunk k receives from the right
+        if (k > 0) e = fmaf(exp2f(a2 * bdsum[(b * nchunk + k) * dim + d]), e, Ek);
+    }
+}
+
+// 4. The reverse sweep of one chunk for CH channels of one sequence.
+template <typename IO, int N>
+__global__ void __launch_bounds__(256, 2) scan_bwd_kernel(BwdParams p) {
+    using S = BwdShape<N>;
+    constexpr int LPC = S::LPC, SPL = S::SPL, CPW = S::CPW, CH = S::CH, V = S::V, T = kBwdT;
+    extern __shared__ float red[];   // [kBwdWarps][T][2N]
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPC;
+    const int64_t d_raw = (int64_t)blockIdx.x * CH + warp * CPW + lane / LPC;
+    const bool valid = d_raw < p.dim;
+    const int64_t d = valid ? d_raw : 0;   // idle lanes stay for the shuffles
+    const int64_t b = blockIdx.y;
+    const int k = blockIdx.z;
+    const int64_t t0 = (int64_t)k * p.chunk_len;
+    int64_t t1 = t0 + p.chunk_len;
+    if (t1 > p.seqlen) t1 = p.seqlen;
+    const int n0 = sub * SPL;
+
+    const IO* x = static_cast<const IO*>(p.x);
+    const IO* delta = static_cast<const IO*>(p.delta);
+    const IO* Bm = static_cast<const IO*>(p.B);
+    const IO* Cm = static_cast<const IO*>(p.C);
+    const IO* z = static_cast<const IO*>(p.z);
+    const IO* dout = static_cast<const IO*>(p.dout);
+
+    float an[SPL], a2[SPL], h[SPL], G[SPL], dAacc[SPL];
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) {
+        an[j] = __ldg(p.A + d * N + n0 + j);
+        a2[j] = an[j] * kLog2e;
+        dAacc[j] = 0.f;
+        const int64_t si = (b * p.dim + d) * N + n0 + j;
+        const int64_t ci = ((b * p.nchunk + k) * p.dim + d) * N + n0 + j;
+        h[j] = p.nchunk > 1 ? p.fstart[ci] : (p.initial_state ? __ldg(p.initial_state + si) : 0.f);
+        G[j] = p.nchunk > 1 ? p.ebuf[ci] : (p.dlast ? __ldg(p.dlast + si) : 0.f);
+    }
+    const float bias = p.delta_bias ? __ldg(p.delta_bias + d) : 0.f;
+    const float Dd = p.D ? __ldg(p.D + d) : 0.f;
+    const int ntile = (int)((t1 - t0 + T - 1) / T);
+    const int64_t tile0 = t0 / T;
+    auto ckpt_at = [&](int j) { return p.ckpt + ((b * p.ntiles + tile0 + j) * p.dim + d) * N + n0; };
+    auto dt_of = [&](int64_t tok) {
+        const float u = load_f32(delta + tok) + bias;
+        return p.softplus ? softplus_tiled<IO>(u) : u;
+    };
+
+    // ---- forward sweep: the state at every tile start
+    for (int j = 0; j < ntile; ++j) {
+        const int64_t ts = t0 + (int64_t)j * T;
+        if (valid) {
+            float* ck = ckpt_at(j);
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) ck[q] = h[q];
+        }
+        const int steps = (int)((t1 - ts) < T ? (t1 - ts) : T);
+        for (int s = 0; s < steps; ++s) {
+            const int64_t t = ts + s;
+            const int64_t tok = (b * p.seqlen + t) * p.dim + d;
+            const float dt = dt_of(tok);
+            const float dx = dt * load_f32(x + tok);
+            float bv[SPL];
+            bwd_load<SPL>(Bm + (b * p.seqlen + t) * N + n0, bv, p.vec);
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) h[q] = fmaf(ex2_sfu(dt * a2[q]), h[q], dx * bv[q]);
+        }
+    }
+
+    // ---- reverse sweep over the tiles
+    float dD = 0.f, dbias = 0.f;
+    float* myred = red + warp * (T * 2 * N);
+    for (int j = ntile - 1; j >= 0; --j) {
+        const int64_t ts = t0 + (int64_t)j * T;
+        const int steps = (int)((t1 - ts) < T ? (t1 - ts) : T);
+        float hs[SPL];
+        {
+            const float* ck = ckpt_at(j);
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) hs[q] = valid ? ck[q] : 0.f;
+        }
+        // recompute the tile's states (registers, static indices)
+        float hist[T][SPL], dth[T];
+        {
+            float hc[SPL];
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) hc[q] = hs[q];
+#pragma unroll
+            for (int s = 0; s < T; ++s) {
+                if (s < steps) {
+                    const int64_t t = ts + s;
+                    const int64_t tok = (b * p.seqlen + t) * p.dim + d;
+                    const float dt = dt_of(tok);
+                    dth[s] = dt;
+                    const float dx = dt * load_f32(x + tok);
+                    float bv[SPL];
+                    bwd_load<SPL>(Bm + (b * p.seqlen + t) * N + n0, bv, p.vec);
+#pragma unroll
+                    for (int q = 0; q < SPL; ++q) {
+                        hc[q] = fmaf(ex2_sfu(dt * a2[q]), hc[q], dx * bv[q]);
+                        hist[s][q] = hc[q];
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int s = T - 1; s >= 0; --s) {
+            if (s < steps) {
+                const int64_t t = ts + s;
+                const int64_t tok = (b * p.seqlen + t) * p.dim + d;
+                const float dt = dth[s];
+                const float xv = load_f32(x + tok);
+                float bv[SPL], cv[SPL];
+                bwd_load<SPL>(Bm + (b * p.seqlen + t) * N + n0, bv, p.vec);
+                bwd_load<SPL>(Cm + (b * p.seqlen + t) * N + n0, cv, p.vec);
+                // yc = C . h_t + D x (needed for dz only)
+                float yp = 0.f;
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) yp = fmaf(cv[q], hist[s][q], yp);
+                const float dov = load_f32(dout + tok);
+                float dyc = dov, dzv = 0.f;
+                if (z) {
+                    const float zv = load_f32(z + tok);
+                    const float sg = sigmoid_fast(zv);
+                    dyc = dov * zv * sg;
+                    const float yc = reduce_slices<LPC>(yp) + Dd * xv;
+                    dzv = dov * yc * sg * (1.f + zv * (1.f - sg));
+                }
+                float vals[V];
+                float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) {
+                    const float hprev = s > 0 ? hist[s > 0 ? s - 1 : 0][q] : hs[q];
+                    const float g = fmaf(dyc, cv[q], G[q]);
+                    const float dA = ex2_sfu(dt * a2[q]);
+                    const float qv = g * dA * hprev;
+                    s1 = fmaf(g, bv[q], s1);
+                    s2 = fmaf(an[q], qv, s2);
+                    dAacc[q] = fmaf(dt, qv, dAacc[q]);
+                    vals[q] = g * dt * xv;                // dB
+                    vals[SPL + q] = dyc * hist[s][q];     // dC
+                    G[q] = dA * g;
+                }
+                s1 = reduce_slices<LPC>(s1);
+                s2 = reduce_slices<LPC>(s2);
+                const float ddt = fmaf(xv, s1, s2);
+                const float du = p.softplus ? ddt * sigmoid_fast(load_f32(delta + tok) + bias) : ddt;
+                dD = fmaf(dyc, xv, dD);
+                dbias += du;
+                if (valid && sub == 0) {
+                    store_io(static_cast<IO*>(p.dx) + tok, fmaf(dt, s1, dyc * Dd));
+                    store_io(static_cast<IO*>(p.ddelta) + tok, du);
+                    if (p.dz) store_io(static_cast<IO*>(p.dz) + tok, dzv);
+                }
+                // dB | dC summed over the warp's channels (idle lanes add zeros)
+                if (!valid) {
+#pragma unroll
+                    for (int i = 0; i < V; ++i) vals[i] = 0.f;
+                }
+                const int base = reduce_channels<V, LPC>(vals, lane);
+                constexpr int HOLD = V / CPW > 0 ? V / CPW : 1;   // values a lane holds
+                // lanes whose leftover channel bits are zero write (replicas skip)
+                const bool writer = CPW <= V || ((lane / LPC) % (CPW / (V < CPW ? V : CPW))) == 0;
+                if (writer) {
+#pragma unroll
+                    for (int i = 0; i < HOLD; ++i) {
+                        const int vi = base + i;               // original value index
+                        const int kind = vi / SPL, jj = vi % SPL;
+                        myred[s * 2 * N + kind * N + n0 + jj] = vals[i];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        // sum over the CTA's warps and store this tile's partials
+        for (int e = threadIdx.x; e < steps * 2 * N; e += blockDim.x) {
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kBwdWarps; ++w) acc += red[w * T * 2 * N + e];
+            const int s = e / (2 * N), v = e % (2 * N);
+            p.pBC[(((int64_t)blockIdx.x * p.batch + b) * p.seqlen + ts + s) * 2 * N + v] = acc;
+        }
+        __syncthreads();
+    }
+
+    // ---- per-(sequence, chunk) partial sums over time; the initial state's gradient
+    if (!valid) return;
+    const int64_t bk = b * p.nchunk + k;
+#pragma unroll
+    for (int q = 0; q < SPL; ++q) p.pA[(bk * p.dim + d) * N + n0 + q] = dAacc[q];
+    if (sub == 0) {   // every lane of the channel holds the whole dD and dbias
+        p.pD[bk * p.dim + d] = dD;
+        p.pbias[bk * p.dim + d] = dbias;
+    }
+    if (k == 0 && p.dinit) {
+#pragma unroll
+        for (int q = 0; q < SPL; ++q) p.dinit[(b * p.dim + d) * N + n0 + q] = G[q];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 4'. The same reverse sweep with every tile's inputs staged in shared memory
+// by TMA (two-stage ring, the next tile in flight while this one computes) and
+// the per-token gradients written back a tile at a time by TMA stores.  Used
+// when the rows are 16-byte multiples and the tensors 16-byte aligned; the
+// arithmetic is that of scan_bwd_kernel.
+//
+// Load sequence u = 0 .. 2 ntile - 1: u < ntile is forward-sweep tile u
+// (x, delta, B); u >= ntile is reverse tile 2 ntile - 1 - u (x, delta, dout,
+// z, B, C).  Stage u % 2, parity (u / 2) & 1.
+struct BwdMaps {
+    CUtensorMap x, delta, dout, z, B, C, dx, ddelta, dz;
+};
+
+template <typename IO, int N>
+struct BwdTmaCfg {
+    using S = BwdShape<N>;
+    static constexpr int CH = S::CH, T = kBwdT, ESZ = (int)sizeof(IO), NST = 2;
+    static constexpr int TOK = T * CH * ESZ;                 // one [T][CH] tile
+    static constexpr int ROW = T * N * ESZ;                  // one [T][N] tile
+    static constexpr int OFF_X = 0, OFF_DL = TOK, OFF_DO = 2 * TOK, OFF_Z = 3 * TOK;
+    static constexpr int OFF_B = 4 * TOK, OFF_C = 4 * TOK + ROW;
+    static constexpr int STAGE = round_up(4 * TOK + 2 * ROW, 128);
+    static constexpr int OFF_OUT = NST * STAGE;              // [2][3][T][CH] io
+    static constexpr int OFF_RED = round_up(OFF_OUT + 2 * 3 * TOK, 128);
+    static constexpr int OFF_BAR = OFF_RED + kBwdWarps * T * 2 * N * 4;
+    static constexpr int OFF_FLAG = OFF_BAR + NST * 8;
+    static constexpr int SMEM = OFF_FLAG + 16;
+    static_assert((CH * ESZ) % 16 == 0 && (N * ESZ) % 16 == 0, "TMA rows are 16-byte multiples");
+};
+
+template <typename IO, int N>
+__global__ void __launch_bounds__(256, 2)
+    scan_bwd_tma_kernel(const __grid_constant__ BwdMaps maps, BwdParams p) {
+    using Cfg = BwdTmaCfg<IO, N>;
+    using S = BwdShape<N>;
+    constexpr int LPC = S::LPC, SPL = S::SPL, CPW = S::CPW, CH = S::CH, V = S::V, T = kBwdT;
+    constexpr int NST = Cfg::NST;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_FLAG);
+    float* red = reinterpret_cast<float*>(smem + Cfg::OFF_RED);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPC;
+    const int cl = warp * CPW + lane / LPC;                 // channel within the CTA
+    const int d0 = blockIdx.x * CH;
+    const int64_t d_raw = (int64_t)d0 + cl;
+    const bool valid = d_raw < p.dim;
+    const int64_t d = valid ? d_raw : 0;
+    const int b = blockIdx.y;
+    const int k = blockIdx.z;
+    const int64_t t0 = (int64_t)k * p.chunk_len;
+    int64_t t1 = t0 + p.chunk_len;
+    if (t1 > p.seqlen) t1 = p.seqlen;
+    const int n0 = sub * SPL;
+    const int ntile = (int)((t1 - t0 + T - 1) / T);
+    const int nload = 2 * ntile;
+    const bool z_on = p.z != nullptr;
+    const bool dz_on = p.dz != nullptr;
+
+    int issued = 0;             // loads issued so far (thread 0's count)
+    auto issue = [&](int u) {   // one thread
+        issued = u + 1;
+        unsigned char* st = smem + (u % NST) * Cfg::STAGE;
+        const bool fwd = u < ntile;
+        const int j = fwd ? u : 2 * ntile - 1 - u;
+        const int r = (int)(t0 + (int64_t)j * T);
+        uint64_t* bar = &full[u % NST];
+        const uint32_t tx = fwd ? (uint32_t)(2 * Cfg::TOK + Cfg::ROW)
+                                : (uint32_t)((z_on ? 4 : 3) * Cfg::TOK + 2 * Cfg::ROW);
+        mbar_arrive_expect_tx(bar, tx);
+        tma_load_3d(st + Cfg::OFF_X, &maps.x, bar, d0, r, b);
+        tma_load_3d(st + Cfg::OFF_DL, &maps.delta, bar, d0, r, b);
+        tma_load_3d(st + Cfg::OFF_B, &maps.B, bar, 0, r, b);
+        if (!fwd) {
+            tma_load_3d(st + Cfg::OFF_DO, &maps.dout, bar, d0, r, b);
+            if (z_on) tma_load_3d(st + Cfg::OFF_Z, &maps.z, bar, d0, r, b);
+            tma_load_3d(st + Cfg::OFF_C, &maps.C, bar, 0, r, b);
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&maps.x);
+        prefetch_tmap(&maps.delta);
+        prefetch_tmap(&maps.B);
+        for (int u = 0; u < NST && u < nload; ++u) issue(u);
+    }
+
+    float an[SPL], a2[SPL], h[SPL], G[SPL], dAacc[SPL];
+#pragma unroll
+    for (int j = 0; j < SPL; ++j) {
+        an[j] = __ldg(p.A + d * N + n0 + j);
+        a2[j] = an[j] * kLog2e;
+        dAacc[j] = 0.f;
+        const int64_t si = ((int64_t)b * p.dim + d) * N + n0 + j;
+        const int64_t ci = (((int64_t)b * p.nchunk + k) * p.dim + d) * N + n0 + j;
+        h[j] = p.nchunk > 1 ? p.fstart[ci] : (p.initial_state ? __ldg(p.initial_state + si) : 0.f);
+        G[j] = p.nchunk > 1 ? p.ebuf[ci] : (p.dlast ? __ldg(p.dlast + si) : 0.f);
+    }
+    const float bias = p.delta_bias ? __ldg(p.delta_bias + d) : 0.f;
+    const float Dd = p.D ? __ldg(p.D + d) : 0.f;
+    const int64_t tile0 = t0 / T;
+    auto ckpt_at = [&](int j) {
+        return p.ckpt + (((int64_t)b * p.ntiles + tile0 + j) * p.dim + d) * N + n0;
+    };
+    auto wait_stage = [&](int u) {
+        if (!mbar_wait_bounded(&full[u % NST], (uint32_t)((u / NST) & 1))) *abort_flag = 1;
+    };
+    // after a block barrier: every thread sees the same flag
+    auto aborted = [&]() { return *abort_flag != 0; };
+    auto refill = [&](int u) {   // after the barrier that follows the last read of stage u
+        if (threadIdx.x == 0 && u + NST < nload) issue(u + NST);
+    };
+
+    // ---- forward sweep: the state at every tile start
+    for (int j = 0; j < ntile; ++j) {
+        const int u = j;
+        wait_stage(u);
+        if (valid) {
+            float* ck = ckpt_at(j);
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) ck[q] = h[q];
+        }
+        const unsigned char* st = smem + (u % NST) * Cfg::STAGE;
+        const IO* xs = reinterpret_cast<const IO*>(st + Cfg::OFF_X);
+        const IO* ds = reinterpret_cast<const IO*>(st + Cfg::OFF_DL);
+        const IO* Bs = reinterpret_cast<const IO*>(st + Cfg::OFF_B);
+        const int steps = (int)((t1 - (t0 + (int64_t)j * T)) < T ? (t1 - (t0 + (int64_t)j * T)) : T);
+        if (!aborted()) {
+#pragma unroll 4
+            for (int s = 0; s < steps; ++s) {
+                const float u_ = load1(ds + s * CH + cl) + bias;
+                const float dt = p.softplus ? softplus_tiled<IO>(u_) : u_;
+                const float dx = dt * load1(xs + s * CH + cl);
+                float bv[SPL];
+                bwd_load_smem<SPL>(Bs + s * N + n0, bv);
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) h[q] = fmaf(ex2_sfu(dt * a2[q]), h[q], dx * bv[q]);
+            }
+        }
+        __syncthreads();
+        if (aborted()) break;
+        refill(u);
+    }
+
+    // ---- reverse sweep
+    float dD = 0.f, dbias = 0.f;
+    float* myred = red + warp * (T * 2 * N);
+    float hs_next[SPL];
+    if (ntile > 0 && !aborted()) {
+        const float* ck = ckpt_at(ntile - 1);
+#pragma unroll
+        for (int q = 0; q < SPL; ++q) hs_next[q] = valid ? ck[q] : 0.f;
+    }
+    for (int jj = 0; jj < ntile && !aborted(); ++jj) {
+        const int j = ntile - 1 - jj;
+        const int u = ntile + jj;
+        const int64_t ts = t0 + (int64_t)j * T;
+        const int steps = (int)((t1 - ts) < T ? (t1 - ts) : T);
+        float hs[SPL];
+#pragma unroll
+        for (int q = 0; q < SPL; ++q) hs[q] = hs_next[q];
+        if (j > 0) {   // the next tile's checkpoint, in flight during this tile
+            const float* ck = ckpt_at(j - 1);
+#pragma unroll
+            for (int q = 0; q < SPL; ++q) hs_next[q] = valid ? ck[q] : 0.f;
+        }
+        wait_stage(u);
+        const unsigned char* st = smem + (u % NST) * Cfg::STAGE;
+        const IO* xs = reinterpret_cast<const IO*>(st + Cfg::OFF_X);
+        const IO* ds = reinterpret_cast<const IO*>(st + Cfg::OFF_DL);
+        const IO* dos = reinterpret_cast<const IO*>(st + Cfg::OFF_DO);
+        const IO* zs = reinterpret_cast<const IO*>(st + Cfg::OFF_Z);
+        const IO* Bs = reinterpret_cast<const IO*>(st + Cfg::OFF_B);
+        const IO* Cs = reinterpret_cast<const IO*>(st + Cfg::OFF_C);
+        IO* ob = reinterpret_cast<IO*>(smem + Cfg::OFF_OUT + (jj & 1) * 3 * Cfg::TOK);
+        if (!aborted()) {
+            float hist[T][SPL], dth[T];
+            {
+                float hc[SPL];
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) hc[q] = hs[q];
+#pragma unroll
+                for (int s = 0; s < T; ++s) {
+                    if (s < steps) {
+                        const float u_ = load1(ds + s * CH + cl) + bias;
+                        const float dt = p.softplus ? softplus_tiled<IO>(u_) : u_;
+                        dth[s] = dt;
+                        const float dx = dt * load1(xs + s * CH + cl);
+                        float bv[SPL];
+                        bwd_load_smem<SPL>(Bs + s * N + n0, bv);
+#pragma unroll
+                        for (int q = 0; q < SPL; ++q) {
+                            hc[q] = fmaf(ex2_sfu(dt * a2[q]), hc[q], dx * bv[q]);
+                            hist[s][q] = hc[q];
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = T - 1; s >= 0; --s) {
+                if (s < steps) {
+                    const float dt = dth[s];
+                    const float xv = load1(xs + s * CH + cl);
+                    float bv[SPL], cv[SPL];
+                    bwd_load_smem<SPL>(Bs + s * N + n0, bv);
+                    bwd_load_smem<SPL>(Cs + s * N + n0, cv);
+                    float yp = 0.f;
+#pragma unroll
+                    for (int q = 0; q < SPL; ++q) yp = fmaf(cv[q], hist[s][q], yp);
+                    const float dov = load1(dos + s * CH + cl);
+                    float dyc = dov, dzv = 0.f;
+                    if (z_on) {
+                        const float zv = load1(zs + s * CH + cl);
+                        const float sg = sigmoid_fast(zv);
+                        dyc = dov * zv * sg;
+                        const float yc = reduce_slices<LPC>(yp) + Dd * xv;
+                        dzv = dov * yc * sg * (1.f + zv * (1.f - sg));
+                    }
+                    float vals[V];
+                    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+                    for (int q = 0; q < SPL; ++q) {
+                        const float hprev = s > 0 ? hist[s > 0 ? s - 1 : 0][q] : hs[q];
+                        const float g = fmaf(dyc, cv[q], G[q]);
+                        const float dA = ex2_sfu(dt * a2[q]);
+                        const float qv = g * dA * hprev;
+                        s1 = fmaf(g, bv[q], s1);
+                        s2 = fmaf(an[q], qv, s2);
+                        dAacc[q] = fmaf(dt, qv, dAacc[q]);
+                        vals[q] = g * dt * xv;
+                        vals[SPL + q] = dyc * hist[s][q];
+                        G[q] = dA * g;
+                    }
+                    s1 = reduce_slices<LPC>(s1);
+                    s2 = reduce_slices<LPC>(s2);
+                    const float ddt = fmaf(xv, s1, s2);
+                    const float du = p.softplus
+                        ? ddt * sigmoid_fast(load1(ds + s * CH + cl) + bias) : ddt;
+                    dD = fmaf(dyc, xv, dD);
+                    dbias += du;
+                    if (sub == 0) {
+                        store_io(ob + s * CH + cl, fmaf(dt, s1, dyc * Dd));
+                        store_io(ob + Cfg::TOK / Cfg::ESZ + s * CH + cl, du);
+                        store_io(ob + 2 * (Cfg::TOK / Cfg::ESZ) + s * CH + cl, dzv);
+                    }
+                    if (!valid) {
+#pragma unroll
+                        for (int i = 0; i < V; ++i) vals[i] = 0.f;
+                    }
+                    const int base = reduce_channels<V, LPC>(vals, lane);
+                    constexpr int HOLD = V / CPW > 0 ? V / CPW : 1;
+                    const bool writer = CPW <= V || ((lane / LPC) % (CPW / (V < CPW ? V : CPW))) == 0;
+                    if (writer) {
+#pragma unroll
+                        for (int i = 0; i < HOLD; ++i) {
+                            const int vi = base + i;
+                            myred[s * 2 * N + (vi / SPL) * N + n0 + vi % SPL] = vals[i];
+                        }
+                    }
+                }
+            }
+        }
+        fence_proxy_async_smem();   // the output tile is read by the TMA store below
+        __syncthreads();
+        if (aborted()) break;
+        for (int e = threadIdx.x; e < steps * 2 * N; e += blockDim.x) {
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kBwdWarps; ++w) acc += red[w * T * 2 * N + e];
+            const int s = e / (2 * N), v = e % (2 * N);
+            p.pBC[(((int64_t)blockIdx.x * p.batch + b) * p.seqlen + ts + s) * 2 * N + v] = acc;
+        }
+        if (threadIdx.x == 0) {
+            tma_store_3d(&maps.dx, ob, d0, (int)ts, b);
+            tma_store_3d(&maps.ddelta, ob + Cfg::TOK / Cfg::ESZ, d0, (int)ts, b);
+            if (dz_on) tma_store_3d(&maps.dz, ob + 2 * (Cfg::TOK / Cfg::ESZ), d0, (int)ts, b);
+            bulk_commit();
+            bulk_wait_read<1>();     // the output buffer written next is free again
+        }
+        __syncthreads();             // red and the stage are free; ob[(jj + 1) & 1] too
+        refill(u);
+    }
+    if (threadIdx.x == 0) {
+        bulk_wait<0>();
+        if (aborted()) {
+            // let the loads still in flight land before the CTA exits
+            for (int u = issued - NST > 0 ? issued - NST : 0; u < issued; ++u)
+                mbar_wait_bounded(&full[u % NST], (uint32_t)((u / NST) & 1), 100000000ull);
+        }
+    }
+    if (aborted() || !valid) return;
+    const int64_t bk = (int64_t)b * p.nchunk + k;
+#pragma unroll
+    for (int q = 0; q < SPL; ++q) p.pA[(bk * p.dim + d) * N + n0 + q] = dAacc[q];
+    if (sub == 0) {
+        p.pD[bk * p.dim + d] = dD;
+        p.pbias[bk * p.dim + d] = dbias;
+    }
+    if (k == 0 && p.dinit) {
+#pragma unroll
+        for (int q = 0; q < SPL; ++q) p.dinit[((int64_t)b * p.dim + d) * N + n0 + q] = G[q];
+    }
+}
+
+// 5. Final sums: dB, dC over the channel blocks; dA, dD, dbias over (b, k).
+template <int N>
+__global__ void scan_bwd_reduce_kernel(BwdParams p, int nblk, float* __restrict__ dB,
+                                       float* __restrict__ dC, float* __restrict__ dA,
+                                       float* __restrict__ dD, float* __restrict__ dbias) {
+    const int64_t nbc = p.batch * p.seqlen * 2 * N;
+    const int64_t npar = p.dim * N + 2 * p.dim;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < nbc) {
+        float acc = 0.f;
+        for (int c = 0; c < nblk; ++c) acc += p.pBC[(int64_t)c * nbc + i];
+        const int v = (int)(i % (2 * N));
+        const int64_t row = i / (2 * N);                 // (b, t)
+        if (v < N) dB[row * N + v] = acc;
+        else dC[row * N + v - N] = acc;
+        return;
+    }
+    const int64_t j = i - nbc;
+    if (j >= npar) return;
+    const int64_t nbk = p.batch * p.nchunk;
+    if (j < p.dim * N) {
+        float acc = 0.f;
+        for (int64_t c = 0; c < nbk; ++c) acc += p.pA[c * p.dim * N + j];
+        dA[j] = acc;
+    } else if (j < p.dim * N + p.dim) {
+        const int64_t dd = j - p.dim * N;
+        float acc = 0.f;
+        for (int64_t c = 0; c < nbk; ++c) acc += p.pD[c * p.dim + dd];
+        if (dD) dD[dd] = acc;
+    } else {
+        const int64_t dd = j - p.dim * N - p.dim;
+        float acc = 0.f;
+        for (int64_t c = 0; c < nbk; ++c) acc += p.pbias[c * p.dim + dd];
+        if (dbias) dbias[dd] = acc;
+    }
+}
+
+}  // namespace ssm

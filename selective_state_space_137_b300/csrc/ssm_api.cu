@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -14,6 +15,7 @@
 #include "common.cuh"
 #include "conv.cuh"
 #include "decode.cuh"
+#include "scan_bwd.cuh"
 #include "scan_generic.cuh"
 #include "scan_tiled.cuh"
 #include "scan_ws.cuh"
@@ -109,6 +111,14 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
     const dim3 grid((unsigned)((lanes + 255) / 256), (unsigned)p.batch);
     ssm::state_update_kernel<IO, N, CONV><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
+}
+
+// Vector loads of the A, B and C slices need 16-byte (A) and 4-element (B, C)
+// alignment of the bases; element-aligned callers get element loads.
+bool decode_vec_ok(const ssm_scan_desc* d, const void* A, const void* B, const void* C) {
+    const size_t v = 4 * io_size(d);
+    return (reinterpret_cast<uintptr_t>(A) % 16) == 0 && (reinterpret_cast<uintptr_t>(B) % v) == 0 &&
+           (reinterpret_cast<uintptr_t>(C) % v) == 0;
 }
 
 template <typename IO, bool CONV = false>
@@ -521,6 +531,7 @@ ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void*
     p.delta_bias = delta_bias; p.out = out;
     p.batch = desc->batch; p.dim = desc->dim;
     p.softplus = desc->delta_softplus ? 1 : 0;
+    p.vec = decode_vec_ok(desc, A, B, C);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_decode<float>(desc->dstate, p, s)
                                                     : dispatch_decode<__nv_bfloat16>(desc->dstate, p, s);
@@ -755,10 +766,261 @@ ssm_status ssm_conv_state_update(const ssm_scan_desc* desc, const ssm_conv_desc*
     p.softplus = desc->delta_softplus ? 1 : 0;
     p.conv_state = conv_state; p.conv_w = conv_w; p.conv_bias = conv_bias;
     p.conv_width = conv->width; p.conv_act = conv->activation;
+    p.vec = decode_vec_ok(desc, A, B, C);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = desc->io_dtype == SSM_DTYPE_F32
                         ? dispatch_decode<float, true>(desc->dstate, p, s)
                         : dispatch_decode<__nv_bfloat16, true>(desc->dstate, p, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward (gradients of the scan).
+namespace {
+
+struct BwdPlan {
+    int nchunk = 1;
+    int64_t chunk_len = 0, ntiles = 0, nblk = 0;
+    size_t off_fstart = 0, off_fdsum = 0, off_ebuf = 0, off_bdsum = 0, off_ckpt = 0, off_pbc = 0,
+           off_pa = 0, off_pd = 0, off_pbias = 0, bytes = 0;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+int bwd_channels_per_cta(int64_t n) {
+    switch (n) {
+        case 1: return ssm::BwdShape<1>::CH;
+        case 2: return ssm::BwdShape<2>::CH;
+        case 4: return ssm::BwdShape<4>::CH;
+        case 8: return ssm::BwdShape<8>::CH;
+        case 16: return ssm::BwdShape<16>::CH;
+        case 32: return ssm::BwdShape<32>::CH;
+        case 64: return ssm::BwdShape<64>::CH;
+    }
+    return 0;
+}
+
+// Chunks of the time axis: one chunk unless the (sequence, channel-block)
+// CTAs fill less than half of the GPU's 2 x 148 slots (each chunk beyond the
+// first costs an aggregate pass forward and one backward).
+BwdPlan bwd_plan(const ssm_scan_desc* d) {
+    BwdPlan pl;
+    const int64_t N = d->dstate, L = d->seqlen;
+    const int64_t ch = bwd_channels_per_cta(N);
+    pl.nblk = ch > 0 ? (d->dim + ch - 1) / ch : 0;
+    const int64_t groups = d->batch * pl.nblk;
+    const int64_t slots = (int64_t)kPlanSMs * 2;
+    int64_t k = 1;
+    if (groups > 0 && groups * 2 < slots) {
+        k = (slots + groups - 1) / groups;
+        const int64_t kmax = L / 512;
+        if (k > kmax) k = kmax;
+        if (k > 4096) k = 4096;
+        if (k < 1) k = 1;
+    }
+    const int64_t T = ssm::kBwdT;
+    int64_t len = (L + k - 1) / k;
+    len = (len + T - 1) / T * T;
+    if (len < T) len = T;
+    pl.chunk_len = len;
+    pl.nchunk = L > 0 ? (int)((L + len - 1) / len) : 1;
+    pl.ntiles = (L + T - 1) / T;
+    const size_t B = (size_t)d->batch, D = (size_t)d->dim, K = (size_t)pl.nchunk;
+    size_t o = 0;
+    if (pl.nchunk > 1) {
+        pl.off_fstart = o; o = align256(o + B * K * D * N * 4);
+        pl.off_fdsum = o;  o = align256(o + B * K * D * 4);
+        pl.off_ebuf = o;   o = align256(o + B * K * D * N * 4);
+        pl.off_bdsum = o;  o = align256(o + B * K * D * 4);
+    }
+    pl.off_ckpt = o;  o = align256(o + B * (size_t)pl.ntiles * D * N * 4);
+    pl.off_pbc = o;   o = align256(o + (size_t)pl.nblk * B * (size_t)L * 2 * N * 4);
+    pl.off_pa = o;    o = align256(o + B * K * D * N * 4);
+    pl.off_pd = o;    o = align256(o + B * K * D * 4);
+    pl.off_pbias = o; o = align256(o + B * K * D * 4);
+    pl.bytes = o;
+    return pl;
+}
+
+// The TMA-staged reverse sweep (scan_bwd_tma_kernel) applies to dstate 8..64
+// with 16-byte rows and 16-byte aligned token tensors (checked by the caller).
+template <typename IO, int N>
+cudaError_t launch_bwd(const BwdPlan& pl, ssm::BwdParams p, const ScanParams& fp, float* dB,
+                       float* dC, float* dA, float* dD, float* dbias, bool tma, cudaStream_t s) {
+    using S = ssm::BwdShape<N>;
+    if (p.nchunk > 1) {
+        // chunk start states, as the forward's chunked path computes them
+        dim3 grid((unsigned)((p.dim + 127) / 128), (unsigned)p.batch, (unsigned)(p.nchunk - 1));
+        ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG><<<grid, 128, 0, s>>>(fp);
+        const int64_t total = p.batch * p.dim * N;
+        ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+            p.A, p.initial_state, fp.carry, fp.dsum, p.batch, p.dim, N, p.nchunk);
+        ssm::scan_bwd_agg_kernel<IO, N><<<grid, 128, 0, s>>>(p);
+        ssm::scan_bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+            p.A, p.dlast, p.ebuf, p.bdsum, p.batch, p.dim, N, p.nchunk);
+    }
+    const dim3 grid((unsigned)pl.nblk, (unsigned)p.batch, (unsigned)p.nchunk);
+    if constexpr (N >= 8) {
+        if (tma) {
+            using Cfg = ssm::BwdTmaCfg<IO, N>;
+            const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+            const int e = (int)sizeof(IO);
+            ssm::BwdMaps maps;
+            memset(&maps, 0, sizeof(maps));
+            const int64_t Dm = p.dim, L = p.seqlen, Bz = p.batch;
+            bool ok = encode_3d(&maps.x, p.x, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
+                      encode_3d(&maps.delta, p.delta, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
+                      encode_3d(&maps.dout, p.dout, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
+                      encode_3d(&maps.B, p.B, dt, e, N, L, Bz, N, Cfg::T) &&
+                      encode_3d(&maps.C, p.C, dt, e, N, L, Bz, N, Cfg::T) &&
+                      encode_3d(&maps.dx, p.dx, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
+                      encode_3d(&maps.ddelta, p.ddelta, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T);
+            if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T);
+            if (ok && p.dz) ok = encode_3d(&maps.dz, p.dz, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T);
+            if (!ok) return cudaErrorInvalidValue;
+            auto kt = ssm::scan_bwd_tma_kernel<IO, N>;
+            cudaError_t err = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+            if (err != cudaSuccess) return err;
+            kt<<<grid, 256, Cfg::SMEM, s>>>(maps, p);
+        }
+    }
+    if (!tma || N < 8) {
+        auto kb = ssm::scan_bwd_kernel<IO, N>;
+        cudaError_t err = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+        if (err != cudaSuccess) return err;
+        kb<<<grid, 256, S::SMEM, s>>>(p);
+    }
+    const int64_t nout = p.batch * p.seqlen * 2 * N + p.dim * N + 2 * p.dim;
+    ssm::scan_bwd_reduce_kernel<N><<<(unsigned)((nout + 255) / 256), 256, 0, s>>>(
+        p, (int)pl.nblk, dB, dC, dA, dD, dbias);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t dispatch_bwd(int64_t n, const BwdPlan& pl, const ssm::BwdParams& p, const ScanParams& fp,
+                         float* dB, float* dC, float* dA, float* dD, float* dbias, bool tma,
+                         cudaStream_t s) {
+    switch (n) {
+        case 1: return launch_bwd<IO, 1>(pl, p, fp, dB, dC, dA, dD, dbias, false, s);
+        case 2: return launch_bwd<IO, 2>(pl, p, fp, dB, dC, dA, dD, dbias, false, s);
+        case 4: return launch_bwd<IO, 4>(pl, p, fp, dB, dC, dA, dD, dbias, false, s);
+        case 8: return launch_bwd<IO, 8>(pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
+        case 16: return launch_bwd<IO, 16>(pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
+        case 32: return launch_bwd<IO, 32>(pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
+        case 64: return launch_bwd<IO, 64>(pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// Shape and alignment rules of the TMA-staged backward.
+bool bwd_tma_ok(const ssm_scan_desc* d, std::initializer_list<const void*> tok) {
+    if (d->dstate < 8) return false;
+    const int64_t e = (int64_t)io_size(d);
+    if ((d->dim * e) % 16 != 0 || (d->dstate * e) % 16 != 0) return false;
+    if (d->seqlen >= ((int64_t)1 << 31) || d->dim >= ((int64_t)1 << 31)) return false;
+    for (const void* q : tok)
+        if (!opt_aligned(q, 16)) return false;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_bwd_workspace_size(const ssm_scan_desc* desc) {
+    if (check_desc(desc) != SSM_OK) return 0;
+    if (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) return 0;
+    return bwd_plan(desc).bytes;
+}
+
+ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* delta,
+                        const float* A, const void* B, const void* C, const float* D,
+                        const void* z, const float* delta_bias, const float* initial_state,
+                        const void* dout, const float* dlast_state, void* dx, void* ddelta,
+                        float* dA, float* dB, float* dC, float* dD, void* dz,
+                        float* ddelta_bias, float* dinitial_state, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    const ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    const size_t esz = io_size(desc);
+    if (!opt_aligned(x, esz) || !opt_aligned(delta, esz) || !opt_aligned(B, esz) ||
+        !opt_aligned(C, esz) || !opt_aligned(z, esz) || !opt_aligned(dout, esz) ||
+        !opt_aligned(dx, esz) || !opt_aligned(ddelta, esz) || !opt_aligned(dz, esz) ||
+        !opt_aligned(A, 4) || !opt_aligned(D, 4) || !opt_aligned(delta_bias, 4) ||
+        !opt_aligned(initial_state, 4) || !opt_aligned(dlast_state, 4) || !opt_aligned(dA, 4) ||
+        !opt_aligned(dB, 4) || !opt_aligned(dC, 4) || !opt_aligned(dD, 4) ||
+        !opt_aligned(ddelta_bias, 4) || !opt_aligned(dinitial_state, 4))
+        return SSM_ERR_INVALID_ARG;
+    if (dz && !z) return SSM_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t N = desc->dstate;
+    const size_t Bz = (size_t)desc->batch, L = (size_t)desc->seqlen, Dm = (size_t)desc->dim;
+    if (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) {
+        // No token reaches the loss through the scan: every sum is empty, and
+        // the initial state's gradient is the final state's.
+        cudaError_t e = cudaSuccess;
+        auto zero = [&](void* ptr, size_t bytes) {
+            if (ptr && bytes && e == cudaSuccess) e = cudaMemsetAsync(ptr, 0, bytes, s);
+        };
+        zero(dA, Dm * N * 4);
+        zero(dD, Dm * 4);
+        zero(ddelta_bias, Dm * 4);
+        zero(dB, Bz * L * N * 4);
+        zero(dC, Bz * L * N * 4);
+        if (dinitial_state && e == cudaSuccess) {
+            const size_t sb = Bz * Dm * N * 4;
+            if (dlast_state)
+                e = sb ? cudaMemcpyAsync(dinitial_state, dlast_state, sb, cudaMemcpyDeviceToDevice, s)
+                       : cudaSuccess;
+            else
+                zero(dinitial_state, sb);
+        }
+        return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    }
+    if (!x || !delta || !A || !B || !C || !dout || !dx || !ddelta || !dA || !dB || !dC)
+        return SSM_ERR_INVALID_ARG;
+    if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
+    const BwdPlan pl = bwd_plan(desc);
+    if (pl.nblk > 0x7fffffff || pl.nchunk > 65535) return SSM_ERR_UNSUPPORTED;
+    if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace))
+        return SSM_ERR_INVALID_ARG;
+    char* w = static_cast<char*>(workspace);
+
+    ScanParams fp;   // forward aggregate pass (chunk start states)
+    fp.x = x; fp.delta = delta; fp.A = A; fp.B = B; fp.C = C; fp.D = nullptr; fp.z = nullptr;
+    fp.delta_bias = delta_bias; fp.out = nullptr; fp.last_state = nullptr;
+    fp.initial_state = initial_state;
+    fp.batch = desc->batch; fp.seqlen = desc->seqlen; fp.dim = desc->dim;
+    fp.nchunk = pl.nchunk; fp.chunk_len = pl.chunk_len;
+    fp.softplus = desc->delta_softplus ? 1 : 0;
+    fp.carry = pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.off_fstart) : nullptr;
+    fp.dsum = pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.off_fdsum) : nullptr;
+
+    ssm::BwdParams p;
+    p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+    p.delta_bias = delta_bias; p.initial_state = initial_state; p.dout = dout;
+    p.dlast = dlast_state; p.dx = dx; p.ddelta = ddelta; p.dz = dz; p.dinit = dinitial_state;
+    p.fstart = fp.carry;
+    p.ebuf = pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.off_ebuf) : nullptr;
+    p.bdsum = pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.off_bdsum) : nullptr;
+    p.ckpt = reinterpret_cast<float*>(w + pl.off_ckpt);
+    p.pBC = reinterpret_cast<float*>(w + pl.off_pbc);
+    p.pA = reinterpret_cast<float*>(w + pl.off_pa);
+    p.pD = reinterpret_cast<float*>(w + pl.off_pd);
+    p.pbias = reinterpret_cast<float*>(w + pl.off_pbias);
+    p.batch = desc->batch; p.seqlen = desc->seqlen; p.dim = desc->dim;
+    p.chunk_len = pl.chunk_len; p.ntiles = pl.ntiles; p.nchunk = pl.nchunk;
+    p.softplus = desc->delta_softplus ? 1 : 0;
+    const size_t v = (size_t)(ssm::BwdShape<16>::SPL) * esz;   // 4 elements for every dstate >= 4
+    p.vec = (reinterpret_cast<uintptr_t>(B) % v) == 0 && (reinterpret_cast<uintptr_t>(C) % v) == 0;
+
+    const bool tma = bwd_tma_ok(desc, {x, delta, B, C, z, dout, dx, ddelta, dz});
+    const cudaError_t e = desc->io_dtype == SSM_DTYPE_F32
+        ? dispatch_bwd<float>(N, pl, p, fp, dB, dC, dA, dD, ddelta_bias, tma, s)
+        : dispatch_bwd<__nv_bfloat16>(N, pl, p, fp, dB, dC, dA, dD, ddelta_bias, tma, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

@@ -1,7 +1,7 @@
 """Tensor-level entry points over the C ABI.
 
-``scan_fwd``, ``state_update`` and the conv variants (``conv1d_fwd``,
-``conv_scan_fwd``, ``conv_state_update``) check shapes, allocate outputs (and
+``scan_fwd``, ``scan_bwd`` (its gradients), ``state_update`` and the conv
+variants (``conv1d_fwd``, ``conv_scan_fwd``, ``conv_state_update``) check shapes, allocate outputs (and
 the scan workspace) with torch on the inputs' device, and call the library.
 They add no arithmetic of their own.
 """
@@ -192,3 +192,45 @@ def conv_state_update(conv_state, conv_w, state, x, delta, A, B, C, D=None, z=No
     if st != _b.SSM_OK:
         raise _b.SSMError(st, "ssm_conv_state_update")
     return out
+
+
+def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, delta_bias=None, initial_state=None,
+             dlast_state=None, delta_softplus=True, workspace=None, stream=None):
+    """Gradients of ``scan_fwd`` for dout = dL/dout (batch, seqlen, dim) and
+    optionally dlast_state = dL/dlast_state (batch, dim, dstate) fp32.
+    Returns a dict: dx, ddelta, dz (or None without z) in the I/O dtype; dA,
+    dB, dC, dD, ddelta_bias, dinitial_state in fp32."""
+    if not x.is_cuda:
+        raise ValueError("scan_bwd runs on a CUDA device only")
+    bsz, seqlen, dim = x.shape
+    dstate = A.shape[1]
+    dev, io = x.device, x.dtype
+    _check(delta, "delta", x.shape, io, dev)
+    _check(z, "z", x.shape, io, dev)
+    _check(dout, "dout", x.shape, io, dev)
+    _check(B, "B", (bsz, seqlen, dstate), io, dev)
+    _check(C, "C", (bsz, seqlen, dstate), io, dev)
+    _check(A, "A", (dim, dstate), torch.float32, dev)
+    _check(D, "D", (dim,), torch.float32, dev)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    _check(initial_state, "initial_state", (bsz, dim, dstate), torch.float32, dev)
+    _check(dlast_state, "dlast_state", (bsz, dim, dstate), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x),
+         "dz": torch.empty_like(x) if z is not None else None,
+         "dA": torch.empty((dim, dstate), **f32), "dB": torch.empty((bsz, seqlen, dstate), **f32),
+         "dC": torch.empty((bsz, seqlen, dstate), **f32), "dD": torch.empty((dim,), **f32),
+         "ddelta_bias": torch.empty((dim,), **f32),
+         "dinitial_state": torch.empty((bsz, dim, dstate), **f32)}
+    desc = _b.make_desc(bsz, seqlen, dim, dstate, io, delta_softplus)
+    need = _b.ssm_scan_bwd_workspace_size(desc)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _b.ssm_scan_bwd(desc, x, delta, A, B, C, D, z, delta_bias, initial_state, dout,
+                         dlast_state, g["dx"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"],
+                         g["dz"], g["ddelta_bias"], g["dinitial_state"],
+                         workspace if need else None, wbytes if need else 0, stream)
+    if st != _b.SSM_OK:
+        raise _b.SSMError(st, "ssm_scan_bwd")
+    return g

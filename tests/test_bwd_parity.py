@@ -1,0 +1,207 @@
+"""GPU parity of ssm_scan_bwd (the gradients of the scan) against the fp64
+oracle's reverse-mode loop, through the C ABI.
+
+Bounds (the pages fix none for gradients; derived from the arithmetic):
+  per-token gradients dx, ddelta, dz (one value per (b, t, d), written in the
+  I/O dtype): elementwise |g - g_ref| <= tol (1 + |g_ref|), tol = 1e-4 for
+  fp32 I/O and 1e-2 for bf16 I/O -- the forward's bound, since each is a
+  short fp32 chain like an output, rounded once to the I/O type;
+  summed gradients dA, dB, dC, dD, ddelta_bias, dinitial_state (fp32 sums over
+  channels, sequences or time): max |g - g_ref| <= SUM_TOL (1 + max |g_ref|)
+  over the tensor -- sums of up to ~1e5 terms of mixed sign, whose error
+  scales with the tensor's magnitude, not each element's.  SUM_TOL = 1e-4 for
+  fp32 I/O; 1e-3 for bf16 I/O, whose path evaluates softplus and sigmoid with
+  the SFU forms (relative error of Delta up to ~1e-3 where Delta ~ 1e-4, well
+  inside the per-token bf16 bound), which long cancelling sums carry through.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import TOL, f64, rel_err, to_device
+from selective_state_space_137_b300 import binding, ops, synth
+
+pytestmark = pytest.mark.gpu
+
+SUM_TOL = {torch.float32: 1e-4, torch.bfloat16: 1e-3}
+PER_TOKEN = ("dx", "ddelta", "dz")
+SUMMED = ("dA", "dB", "dC", "dD", "ddelta_bias", "dinitial_state")
+
+
+def norm_err(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    return float(np.max(np.abs(got - ref)) / (1.0 + np.max(np.abs(ref))))
+
+
+def make_case(w, dlast=True, seed_off=500):
+    inp = synth.make_scan_inputs(w)
+    g = torch.Generator().manual_seed(w.seed + seed_off)
+    dout = torch.randn(inp["x"].shape, generator=g).to(inp["x"].dtype)
+    dl = torch.randn((w.batch, w.dim, w.dstate), generator=g) if dlast else None
+    return inp, dout, dl
+
+
+def check_bwd(w, cuda, dlast=True, delta_softplus=True, modify=None):
+    inp, dout, dl = make_case(w, dlast)
+    if modify:
+        modify(inp)
+    dev = to_device(inp, cuda)
+    got = ops.scan_bwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"], dout.to(cuda),
+                       D=dev["D"], z=dev["z"], delta_bias=dev["delta_bias"],
+                       initial_state=dev["initial_state"],
+                       dlast_state=None if dl is None else dl.to(cuda),
+                       delta_softplus=delta_softplus)
+    torch.cuda.synchronize()
+    ref = oracle.scan_bwd(f64(inp["x"]), f64(inp["delta"]), f64(inp["A"]), f64(inp["B"]),
+                          f64(inp["C"]), f64(dout), D=f64(inp["D"]), z=f64(inp["z"]),
+                          delta_bias=f64(inp["delta_bias"]), delta_softplus=delta_softplus,
+                          initial_state=f64(inp["initial_state"]), dlast_state=f64(dl))
+    tol = TOL[inp["x"].dtype]
+    errs = {}
+    for k in PER_TOKEN:
+        if ref[k] is None:
+            assert got[k] is None
+            continue
+        errs[k] = rel_err(f64(got[k]), ref[k])
+        assert np.isfinite(f64(got[k])).all(), k
+        assert errs[k] <= tol, f"{w.name}: {k} error {errs[k]:.3e} > {tol}"
+    for k in SUMMED:
+        errs[k] = norm_err(f64(got[k]), ref[k])
+        assert np.isfinite(f64(got[k])).all(), k
+        stol = SUM_TOL[inp["x"].dtype]
+        assert errs[k] <= stol, f"{w.name}: {k} error {errs[k]:.3e} > {stol}"
+    return errs
+
+
+SMALL = synth.ScanWorkload("bwd-small", 2, 300, 72, 16, "bf16", 11, init_state=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_small(cuda, io):
+    check_bwd(dataclasses.replace(SMALL, io=io, name=f"bwd-small-{io}"), cuda)
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 8, 32, 64])
+def test_bwd_dstates(cuda, n):
+    check_bwd(dataclasses.replace(SMALL, io="f32", dstate=n, seed=200 + n, name=f"bwd-n{n}"), cuda)
+
+
+@pytest.mark.parametrize("variant", ["no_z", "no_D", "no_bias", "no_init", "no_dlast",
+                                     "nothing_optional", "random_A", "ragged_dim"])
+def test_bwd_variants(cuda, variant):
+    kw = {"no_z": dict(with_z=False), "no_D": dict(with_D=False), "no_bias": dict(with_bias=False),
+          "no_init": dict(init_state=False), "no_dlast": {},
+          "nothing_optional": dict(with_z=False, with_D=False, with_bias=False, init_state=False),
+          "random_A": dict(random_A=True), "ragged_dim": dict(dim=40, seqlen=257)}[variant]
+    check_bwd(dataclasses.replace(SMALL, name=variant, seed=7, **kw), cuda,
+              dlast=variant not in ("no_dlast", "nothing_optional"))
+
+
+def test_bwd_without_softplus(cuda):
+    def positive_delta(inp):
+        inp["delta"] = (inp["delta"].float().abs() * 0.05 + 0.01).to(inp["delta"].dtype)
+    check_bwd(dataclasses.replace(SMALL, name="bwd-nosoftplus", with_bias=False, seqlen=64), cuda,
+              delta_softplus=False, modify=positive_delta)
+
+
+@pytest.mark.parametrize("L", [1, 15, 16, 17, 33])
+def test_bwd_edge_lengths(cuda, L):
+    check_bwd(dataclasses.replace(SMALL, seqlen=L, seed=40 + L, name=f"bwd-L{L}"), cuda)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_chunked_long_sequence(cuda, io):
+    """Few channels and a long sequence: the time axis is cut into chunks,
+    joined forward (state carries) and backward (gradient carries)."""
+    w = synth.ScanWorkload(f"bwd-chunked-{io}", 1, 6000, 48, 16, io, 21, dt_lo=1e-4, dt_hi=1e-2,
+                           init_state=True)
+    check_bwd(w, cuda)
+
+
+def test_bwd_empty_sequence(cuda):
+    w = dataclasses.replace(SMALL, seqlen=0)
+    inp, dout, dl = make_case(w)
+    dev = to_device(inp, cuda)
+    got = ops.scan_bwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"], dout.to(cuda),
+                       D=dev["D"], z=dev["z"], delta_bias=dev["delta_bias"],
+                       initial_state=dev["initial_state"], dlast_state=dl.to(cuda))
+    torch.cuda.synchronize()
+    assert torch.equal(got["dinitial_state"].cpu(), dl)
+    for k in ("dA", "dD", "ddelta_bias"):
+        assert torch.count_nonzero(got[k]) == 0
+
+
+def test_bwd_is_deterministic(cuda):
+    w = dataclasses.replace(SMALL, seqlen=1000, dim=256, name="bwd-det")
+    inp, dout, dl = make_case(w)
+    dev = to_device(inp, cuda)
+    args = (dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"], dout.to(cuda))
+    kw = dict(D=dev["D"], z=dev["z"], delta_bias=dev["delta_bias"],
+              initial_state=dev["initial_state"], dlast_state=dl.to(cuda))
+    a = ops.scan_bwd(*args, **kw)
+    b = ops.scan_bwd(*args, **kw)
+    torch.cuda.synchronize()
+    for k in a:
+        if a[k] is not None:
+            assert torch.equal(a[k], b[k]), k
+
+
+def test_bwd_full_channel_sums_medium(cuda):
+    """All gradients, dB and dC included (sums over 512 channels), at a size
+    the oracle finishes in seconds."""
+    check_bwd(synth.ScanWorkload("bwd-medium", 2, 1024, 512, 16, "bf16", 13, init_state=True), cuda)
+
+
+def test_bwd_full_size_sampled_channels(cuda):
+    """The Mamba-1.4B layer (4 x 8192 x 4096 x 16, bf16): the per-channel
+    gradients (dx, ddelta, dz over all tokens; dA, dD, ddelta_bias) of sampled
+    channels against the oracle run on those channels alone (a channel's own
+    gradients depend only on its own inputs and the shared B, C rows)."""
+    w = synth.MAMBA_1P4B
+    inp = synth.make_scan_inputs(w, device=str(cuda))
+    g = torch.Generator(device=cuda).manual_seed(99)
+    dout = torch.randn(inp["x"].shape, generator=g, device=cuda).to(inp["x"].dtype)
+    got = ops.scan_bwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], dout, D=inp["D"],
+                       z=inp["z"], delta_bias=inp["delta_bias"])
+    torch.cuda.synchronize()
+    ds = [0, 1, 2047, 4095]
+    idx = torch.tensor(ds, device=cuda)
+    sub = lambda t: f64(t.index_select(-1, idx))
+    ref = oracle.scan_bwd(sub(inp["x"]), sub(inp["delta"]), f64(inp["A"].index_select(0, idx)),
+                          f64(inp["B"]), f64(inp["C"]), sub(dout),
+                          D=f64(inp["D"].index_select(0, idx)), z=sub(inp["z"]),
+                          delta_bias=f64(inp["delta_bias"].index_select(0, idx)))
+    tol = TOL[torch.bfloat16]
+    for k in PER_TOKEN:
+        e = rel_err(sub(got[k]), ref[k])
+        assert e <= tol, (k, e)
+    stol = SUM_TOL[torch.bfloat16]
+    assert norm_err(f64(got["dA"].index_select(0, idx)), ref["dA"]) <= stol
+    assert norm_err(f64(got["dD"].index_select(0, idx)), ref["dD"]) <= stol
+    assert norm_err(f64(got["ddelta_bias"].index_select(0, idx)), ref["ddelta_bias"]) <= stol
+    for k in ("dB", "dC"):
+        assert torch.isfinite(got[k]).all()
+
+
+def test_bwd_workspace_checks(cuda):
+    w = SMALL
+    inp, dout, dl = make_case(w)
+    dev = to_device(inp, cuda)
+    desc = binding.make_desc(w.batch, w.seqlen, w.dim, w.dstate, dev["x"].dtype)
+    need = binding.ssm_scan_bwd_workspace_size(desc)
+    assert need > 0
+    small = torch.empty(need - 256, dtype=torch.uint8, device=cuda)
+    outs = [torch.empty_like(dev["x"]) for _ in range(2)]
+    f = lambda *s: torch.empty(s, device=cuda)
+    st = binding.ssm_scan_bwd(desc, dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"], None,
+                              None, None, None, dout.to(cuda), None, outs[0], outs[1],
+                              f(w.dim, w.dstate), f(w.batch, w.seqlen, w.dstate),
+                              f(w.batch, w.seqlen, w.dstate), None, None, None, None, small,
+                              small.numel())
+    assert st == binding.SSM_ERR_INVALID_ARG

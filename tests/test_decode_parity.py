@@ -99,3 +99,29 @@ def test_decode_equals_scan(cuda):
     torch.cuda.synchronize()
     assert rel_err(f64(torch.stack(outs, 1)), f64(out)) <= 1e-4
     assert rel_err(f64(state), f64(last)) <= 1e-4
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_decode_element_aligned_pointers(cuda, io):
+    """A, B and C one element past a 16-byte boundary (element-aligned, which
+    the contract accepts): the step takes element loads and matches the oracle."""
+    w = dataclasses.replace(SMALL, io=io, steps=3, seed=77)
+    inp = to_device(synth.make_decode_inputs(w), cuda)
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+        v = buf[1:].view(t.shape)
+        v.copy_(t)
+        return v
+
+    A, Bs, Cs = shifted(inp["A"]), shifted(inp["B"]), shifted(inp["C"])
+    assert A.data_ptr() % 16 != 0 and Bs.data_ptr() % 8 != 0
+    ref_out, ref_st = oracle_chain(inp, list(range(w.batch)), list(range(w.dim)), w.steps)
+    state = inp["state"].clone()
+    tol = TOL[synth.io_dtype(io)]
+    for s in range(w.steps):
+        out = ops.state_update(state, inp["x"][s], inp["delta"][s], A, Bs[s], Cs[s], inp["D"],
+                               inp["z"][s], inp["delta_bias"])
+        torch.cuda.synchronize()
+        assert rel_err(f64(out), ref_out[s]) <= tol
+        assert rel_err(f64(state), ref_st[s]) <= tol
