@@ -162,8 +162,12 @@ __device__ __forceinline__ float reduce_slices(float v) {
     return v;
 }
 
+// sigmoid(u) = 1 / (1 + 2^(-u log2 e)) with the SFU exponential and the
+// approximate reciprocal (saturates to 0 and 1 at the ends).
 __device__ __forceinline__ float sigmoid_fast(float u) {
-    return __frcp_rn(1.f + ex2_sfu(-u * kLog2e));
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + ex2_sfu(-u * kLog2e)));
+    return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -452,7 +456,13 @@ struct BwdTmaCfg {
     static constexpr int STAGE = round_up(4 * TOK + 2 * ROW, 128);
     static constexpr int OFF_OUT = NST * STAGE;              // [2][3][T][CH] io
     static constexpr int OFF_RED = round_up(OFF_OUT + 2 * 3 * TOK, 128);
-    static constexpr int OFF_BAR = OFF_RED + kBwdWarps * T * 2 * N * 4;
+    // per-token values of the tile, computed once per (step, channel) by the
+    // channel's lanes together: [NSCR][T][SROW] fp32 (padded rows: the lanes
+    // of a channel write different steps without bank conflicts)
+    static constexpr int SROW = CH + 8, NSCR = 6;
+    enum { S_DT = 0, S_DX, S_X, S_DYC, S_ZF, S_SGU };
+    static constexpr int OFF_SCR = OFF_RED + kBwdWarps * T * 2 * N * 4;
+    static constexpr int OFF_BAR = OFF_SCR + NSCR * T * SROW * 4;
     static constexpr int OFF_FLAG = OFF_BAR + NST * 8;
     static constexpr int SMEM = OFF_FLAG + 16;
     static_assert((CH * ESZ) % 16 == 0 && (N * ESZ) % 16 == 0, "TMA rows are 16-byte multiples");
@@ -469,6 +479,7 @@ __global__ void __launch_bounds__(256, 2)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_FLAG);
     float* red = reinterpret_cast<float*>(smem + Cfg::OFF_RED);
+    float* scr = reinterpret_cast<float*>(smem + Cfg::OFF_SCR) + 0;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -564,11 +575,20 @@ __global__ void __launch_bounds__(256, 2)
         const IO* Bs = reinterpret_cast<const IO*>(st + Cfg::OFF_B);
         const int steps = (int)((t1 - (t0 + (int64_t)j * T)) < T ? (t1 - (t0 + (int64_t)j * T)) : T);
         if (!aborted()) {
+            // Delta and Delta*x once per (step, channel): lane sub takes steps sub, sub + LPC, ...
+#pragma unroll
+            for (int m = 0; m < T / LPC; ++m) {
+                const int sl = sub + LPC * m;
+                const float u_ = load1(ds + sl * CH + cl) + bias;
+                const float dt = p.softplus ? softplus_tiled<IO>(u_) : u_;
+                scr[Cfg::S_DT * T * Cfg::SROW + sl * Cfg::SROW + cl] = dt;
+                scr[Cfg::S_DX * T * Cfg::SROW + sl * Cfg::SROW + cl] = dt * load1(xs + sl * CH + cl);
+            }
+            __syncwarp();
 #pragma unroll 4
             for (int s = 0; s < steps; ++s) {
-                const float u_ = load1(ds + s * CH + cl) + bias;
-                const float dt = p.softplus ? softplus_tiled<IO>(u_) : u_;
-                const float dx = dt * load1(xs + s * CH + cl);
+                const float dt = scr[Cfg::S_DT * T * Cfg::SROW + s * Cfg::SROW + cl];
+                const float dx = scr[Cfg::S_DX * T * Cfg::SROW + s * Cfg::SROW + cl];
                 float bv[SPL];
                 bwd_load_smem<SPL>(Bs + s * N + n0, bv);
 #pragma unroll
@@ -612,7 +632,33 @@ __global__ void __launch_bounds__(256, 2)
         const IO* Cs = reinterpret_cast<const IO*>(st + Cfg::OFF_C);
         IO* ob = reinterpret_cast<IO*>(smem + Cfg::OFF_OUT + (jj & 1) * 3 * Cfg::TOK);
         if (!aborted()) {
-            float hist[T][SPL], dth[T];
+            // per-token values once per (step, channel), split over the channel's lanes
+#pragma unroll
+            for (int m = 0; m < T / LPC; ++m) {
+                const int sl = sub + LPC * m;
+                const float u_ = load1(ds + sl * CH + cl) + bias;
+                const float dt = p.softplus ? softplus_tiled<IO>(u_) : u_;
+                const float xv = load1(xs + sl * CH + cl);
+                const float dov = load1(dos + sl * CH + cl);
+                float dyc = dov, zf = 0.f;
+                if (z_on) {
+                    const float zv = load1(zs + sl * CH + cl);
+                    const float sg = sigmoid_fast(zv);
+                    dyc = dov * zv * sg;
+                    zf = dov * sg * (1.f + zv * (1.f - sg));
+                }
+                float* sc = scr + sl * Cfg::SROW + cl;
+                sc[Cfg::S_DT * T * Cfg::SROW] = dt;
+                sc[Cfg::S_DX * T * Cfg::SROW] = dt * xv;
+                sc[Cfg::S_X * T * Cfg::SROW] = xv;
+                sc[Cfg::S_DYC * T * Cfg::SROW] = dyc;
+                sc[Cfg::S_ZF * T * Cfg::SROW] = zf;
+                sc[Cfg::S_SGU * T * Cfg::SROW] = p.softplus ? sigmoid_fast(u_) : 1.f;
+                if (sl < steps) dD = fmaf(dyc, xv, dD);
+            }
+            __syncwarp();
+            auto sv = [&](int which, int s_) { return scr[which * T * Cfg::SROW + s_ * Cfg::SROW + cl]; };
+            float hist[T][SPL];
             {
                 float hc[SPL];
 #pragma unroll
@@ -620,10 +666,8 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
                 for (int s = 0; s < T; ++s) {
                     if (s < steps) {
-                        const float u_ = load1(ds + s * CH + cl) + bias;
-                        const float dt = p.softplus ? softplus_tiled<IO>(u_) : u_;
-                        dth[s] = dt;
-                        const float dx = dt * load1(xs + s * CH + cl);
+                        const float dt = sv(Cfg::S_DT, s);
+                        const float dx = sv(Cfg::S_DX, s);
                         float bv[SPL];
                         bwd_load_smem<SPL>(Bs + s * N + n0, bv);
 #pragma unroll
@@ -637,22 +681,19 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
             for (int s = T - 1; s >= 0; --s) {
                 if (s < steps) {
-                    const float dt = dth[s];
-                    const float xv = load1(xs + s * CH + cl);
+                    const float dt = sv(Cfg::S_DT, s);
+                    const float dx = sv(Cfg::S_DX, s);
+                    const float xv = sv(Cfg::S_X, s);
+                    const float dyc = sv(Cfg::S_DYC, s);
                     float bv[SPL], cv[SPL];
                     bwd_load_smem<SPL>(Bs + s * N + n0, bv);
                     bwd_load_smem<SPL>(Cs + s * N + n0, cv);
-                    float yp = 0.f;
-#pragma unroll
-                    for (int q = 0; q < SPL; ++q) yp = fmaf(cv[q], hist[s][q], yp);
-                    const float dov = load1(dos + s * CH + cl);
-                    float dyc = dov, dzv = 0.f;
+                    float dzv = 0.f;
                     if (z_on) {
-                        const float zv = load1(zs + s * CH + cl);
-                        const float sg = sigmoid_fast(zv);
-                        dyc = dov * zv * sg;
-                        const float yc = reduce_slices<LPC>(yp) + Dd * xv;
-                        dzv = dov * yc * sg * (1.f + zv * (1.f - sg));
+                        float yp = 0.f;
+#pragma unroll
+                        for (int q = 0; q < SPL; ++q) yp = fmaf(cv[q], hist[s][q], yp);
+                        dzv = sv(Cfg::S_ZF, s) * (reduce_slices<LPC>(yp) + Dd * xv);
                     }
                     float vals[V];
                     float s1 = 0.f, s2 = 0.f;
@@ -665,16 +706,13 @@ __global__ void __launch_bounds__(256, 2)
                         s1 = fmaf(g, bv[q], s1);
                         s2 = fmaf(an[q], qv, s2);
                         dAacc[q] = fmaf(dt, qv, dAacc[q]);
-                        vals[q] = g * dt * xv;
-                        vals[SPL + q] = dyc * hist[s][q];
+                        vals[q] = g * dx;                     // dB
+                        vals[SPL + q] = dyc * hist[s][q];     // dC
                         G[q] = dA * g;
                     }
                     s1 = reduce_slices<LPC>(s1);
                     s2 = reduce_slices<LPC>(s2);
-                    const float ddt = fmaf(xv, s1, s2);
-                    const float du = p.softplus
-                        ? ddt * sigmoid_fast(load1(ds + s * CH + cl) + bias) : ddt;
-                    dD = fmaf(dyc, xv, dD);
+                    const float du = fmaf(xv, s1, s2) * sv(Cfg::S_SGU, s);
                     dbias += du;
                     if (sub == 0) {
                         store_io(ob + s * CH + cl, fmaf(dt, s1, dyc * Dd));
@@ -697,6 +735,7 @@ __global__ void __launch_bounds__(256, 2)
                     }
                 }
             }
+            __syncwarp();   // the scratch rows are rewritten by the next tile's prologue
         }
         fence_proxy_async_smem();   // the output tile is read by the TMA store below
         __syncthreads();
@@ -726,7 +765,9 @@ __global__ void __launch_bounds__(256, 2)
                 mbar_wait_bounded(&full[u % NST], (uint32_t)((u / NST) & 1), 100000000ull);
         }
     }
-    if (aborted() || !valid) return;
+    if (aborted()) return;
+    dD = reduce_slices<LPC>(dD);   // each lane summed the steps of its prologue share
+    if (!valid) return;
     const int64_t bk = (int64_t)b * p.nchunk + k;
 #pragma unroll
     for (int q = 0; q < SPL; ++q) p.pA[(bk * p.dim + d) * N + n0 + q] = dAacc[q];
