@@ -94,10 +94,28 @@ def peaks():
         return PEAK_FALLBACK_GBS, "fallback"
 
 
-def kernel_source_hash():
+# The sources that define each profiled kernel: its own header, the headers it
+# includes, and the launch code.  A committed ncu summary records the hash of
+# these files when it was captured; its traffic figure is used only while they
+# are unchanged.
+_KERNEL_SOURCES = {
+    "scan_fwd": ("common.cuh", "tma.cuh", "scan_generic.cuh", "scan_tiled.cuh", "scan_ws.cuh",
+                 "ssm_api.cu"),
+    "conv_scan_fwd": ("common.cuh", "tma.cuh", "scan_generic.cuh", "scan_tiled.cuh",
+                      "scan_ws.cuh", "ssm_api.cu"),
+    "state_update": ("common.cuh", "scan_tiled.cuh", "decode.cuh", "ssm_api.cu"),
+    "conv1d_fwd": ("common.cuh", "scan_generic.cuh", "scan_tiled.cuh", "conv.cuh", "ssm_api.cu"),
+    "scan_bwd": ("common.cuh", "tma.cuh", "scan_tiled.cuh", "scan_bwd.cuh", "ssm_api.cu"),
+}
+
+
+def kernel_source_hash(kernel=None):
+    """sha256 prefix of the kernel's defining sources (all of csrc/ when
+    ``kernel`` is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_137_b300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    files = sorted(os.listdir(csrc)) if kernel is None else sorted(_KERNEL_SOURCES[kernel])
+    for fn in files:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -105,7 +123,7 @@ def kernel_source_hash():
 
 def profiled_traffic(kernel_tag):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (the summary records their hash)."""
+    the current sources of that kernel (the summary records their hash)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     try:
         text = open(path).read()
@@ -113,7 +131,9 @@ def profiled_traffic(kernel_tag):
         return None
     m_hash = re.search(r"source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    kernel = next((k for k in sorted(_KERNEL_SOURCES, key=len, reverse=True)
+                   if kernel_tag.startswith(k + "_")), None)
+    if not m_hash or not m_bytes or kernel is None or m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_bytes.group(1))
 
@@ -506,7 +526,8 @@ def run_conv(args, w, inp, dev, peak, peak_kind):
     return {"width": K, "activation": "silu",
             "fused": {"ms": fused_ms, "elements_per_s": w.tokens / (fused_ms * 1e-3),
                       "gb_per_s": fused_bytes / (fused_ms * 1e-3) / 1e9,
-                      "algorithmic_bytes_per_launch": fused_bytes},
+                      "algorithmic_bytes_per_launch": fused_bytes,
+                      "traffic": profiled_traffic("conv_scan_fwd_" + w.name)},
             "separate": {"conv1d_ms": conv_ms, "scan_ms": scan_ms, "ms": conv_ms + scan_ms,
                          "elements_per_s": w.tokens / ((conv_ms + scan_ms) * 1e-3)},
             "fused_speedup": (conv_ms + scan_ms) / fused_ms,
