@@ -13,8 +13,10 @@ This module only marshals numpy arrays into fp64 buffers for it.
 Definitions followed (see the header of ``ssm_oracle.c`` for the passages):
 the recurrence h_t = exp(Delta_t A) * h_{t-1} + Delta_t B_t x_t, the readout
 y_t = C_t . h_t + D x_t, the gate silu(z_t), and Delta = softplus(raw + bias);
-the causal depthwise conv in front of it; and the gradients of the scan
-(``scan_bwd``: the same loop differentiated in reverse mode).
+the causal depthwise conv in front of it; the gradients of the scan
+(``scan_bwd``: the same loop differentiated in reverse mode); the exact
+zero-order-hold input term (``scan_fwd(zoh=True)``); and the time-invariant
+convolution mode (``lti_kernel``, ``lti_conv``).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 identities and closed forms that are independent of this code.
@@ -70,6 +72,12 @@ def _bind(lib):
                                                                        ctypes.c_int]
     lib.oracle_state_update.restype = ctypes.c_int
     lib.oracle_state_update.argtypes = [ctypes.c_int64] * 3 + [_dp] * 9 + [ctypes.c_int, _dp]
+    lib.oracle_scan_fwd_zoh.restype = ctypes.c_int
+    lib.oracle_scan_fwd_zoh.argtypes = lib.oracle_scan_fwd.argtypes
+    lib.oracle_lti_kernel.restype = ctypes.c_int
+    lib.oracle_lti_kernel.argtypes = [ctypes.c_int64] * 3 + [_dp] * 4 + [ctypes.c_int, _dp]
+    lib.oracle_lti_conv.restype = ctypes.c_int
+    lib.oracle_lti_conv.argtypes = [ctypes.c_int64] * 3 + [_dp] * 5
     lib.oracle_scan_bwd.restype = ctypes.c_int
     lib.oracle_scan_bwd.argtypes = ([ctypes.c_int64] * 4 + [_dp] * 8 + [ctypes.c_int] + [_dp] * 12
                                     + [ctypes.c_int])
@@ -107,13 +115,14 @@ def _ptr(a):
 
 
 def scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-             initial_state=None, nthreads=0, lib=None):
+             initial_state=None, nthreads=0, lib=None, zoh=False):
     """Selective scan forward in fp64.
 
     x, delta, z: (batch, seqlen, dim); B, C: (batch, seqlen, dstate);
     A: (dim, dstate); D, delta_bias: (dim,); initial_state: (batch, dim, dstate).
     Returns ``(out, last_state)``, fp64 arrays of shapes (batch, seqlen, dim) and
-    (batch, dim, dstate).
+    (batch, dim, dstate).  ``zoh=True`` takes the exact zero-order-hold input
+    term ((exp(Delta A) - 1) / A) B x instead of Delta B x.
     """
     x = _f64(x)
     bsz, seqlen, dim = x.shape
@@ -128,7 +137,9 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=
     initial_state = _f64(initial_state, (bsz, dim, dstate))
     out = np.empty((bsz, seqlen, dim), dtype=np.float64)
     last = np.empty((bsz, dim, dstate), dtype=np.float64)
-    rc = (lib or load()).oracle_scan_fwd(bsz, seqlen, dim, dstate, _ptr(x), _ptr(delta), _ptr(A),
+    L_ = lib or load()
+    fn = L_.oracle_scan_fwd_zoh if zoh else L_.oracle_scan_fwd
+    rc = fn(bsz, seqlen, dim, dstate, _ptr(x), _ptr(delta), _ptr(A),
                                          _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
                                          int(bool(delta_softplus)), _ptr(initial_state), _ptr(out),
                                          _ptr(last), int(nthreads))
@@ -196,6 +207,38 @@ def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, delt
     if rc != 0:
         raise ValueError("oracle_state_update rejected its arguments")
     return out, st
+
+
+def lti_kernel(delta, A, B, C, seqlen, zoh=False, lib=None):
+    """Convolution kernel K (dim, seqlen) of the time-invariant model with
+    per-channel step delta (dim,) and per-channel B, C (dim, dstate)."""
+    A = _f64(A)
+    dim, dstate = A.shape
+    delta = _f64(delta, (dim,))
+    B = _f64(B, (dim, dstate))
+    C = _f64(C, (dim, dstate))
+    K = np.empty((dim, int(seqlen)), dtype=np.float64)
+    rc = (lib or load()).oracle_lti_kernel(dim, dstate, int(seqlen), _ptr(delta), _ptr(A), _ptr(B),
+                                           _ptr(C), int(bool(zoh)), _ptr(K))
+    if rc != 0:
+        raise ValueError("oracle_lti_kernel rejected its arguments")
+    return K
+
+
+def lti_conv(K, x, D=None, z=None, lib=None):
+    """y = K * x (causal, per channel) + D x, gated by silu(z) when given.
+    K: (dim, seqlen); x, z: (batch, seqlen, dim)."""
+    x = _f64(x)
+    bsz, seqlen, dim = x.shape
+    K = _f64(K, (dim, seqlen))
+    D = _f64(D, (dim,))
+    z = _f64(z, x.shape)
+    out = np.empty(x.shape, dtype=np.float64)
+    rc = (lib or load()).oracle_lti_conv(bsz, seqlen, dim, _ptr(K), _ptr(x), _ptr(D), _ptr(z),
+                                         _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_lti_conv rejected its arguments")
+    return out
 
 
 def conv1d_fwd(x, w, bias=None, conv_state=None, activation=True, lib=None):

@@ -203,6 +203,111 @@ int oracle_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t dim, int64_t width,
     return 0;
 }
 
+/* The scan with the exact zero-order-hold input term ("Mamba的三大创新",
+ * stage 1, zero-order hold): holding x constant over a step of length Delta,
+ * the diagonal system h' = A h + B x integrates exactly to
+ *   h_t = exp(Delta A) h_{t-1} + ((exp(Delta A) - 1) / A) B x_t,
+ * i.e. Bbar = (Delta A)^{-1} (exp(Delta A) - I) Delta B, which tends to
+ * Delta B (the first-order form of oracle_scan_fwd) as Delta A -> 0; at
+ * A = 0 it is Delta B exactly.  Everything else (softplus, readout, skip,
+ * gate, layouts, arguments) is that of oracle_scan_fwd. */
+int oracle_scan_fwd_zoh(int64_t batch, int64_t seqlen, int64_t dim, int64_t dstate,
+                        const double *x, const double *delta, const double *A,
+                        const double *B, const double *C, const double *D,
+                        const double *z, const double *delta_bias, int delta_softplus,
+                        const double *initial_state, double *out, double *last_state,
+                        int nthreads)
+{
+    if (batch < 0 || seqlen < 0 || dim < 0 || dstate <= 0 || dstate > 4096)
+        return -1;
+    if (!x || !delta || !A || !B || !C || !out)
+        return -1;
+    const int64_t nchan = batch * dim;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t ch = 0; ch < nchan; ++ch) {
+        const int64_t bb = ch / dim;
+        const int64_t dd = ch % dim;
+        double st[4096];   /* the state of channel (bb, dd) */
+        for (int64_t n = 0; n < dstate; ++n)
+            st[n] = initial_state ? initial_state[ch * dstate + n] : 0.0;
+        for (int64_t t = 0; t < seqlen; ++t) {
+            const int64_t i = (bb * seqlen + t) * dim + dd;   /* (b, t, d) */
+            const int64_t r = (bb * seqlen + t) * dstate;     /* (b, t, :) */
+            const double step = delta_softplus
+                ? oracle_softplus(delta[i] + (delta_bias ? delta_bias[dd] : 0.0))
+                : delta[i] + (delta_bias ? delta_bias[dd] : 0.0);
+            double acc = 0.0;
+            for (int64_t n = 0; n < dstate; ++n) {
+                const double a = A[dd * dstate + n];
+                const double decay = exp(step * a);
+                const double gain = a != 0.0 ? expm1(step * a) / a : step;   /* (e^{dt a} - 1) / a */
+                st[n] = decay * st[n] + gain * B[r + n] * x[i];
+                acc += C[r + n] * st[n];
+            }
+            acc += D ? D[dd] * x[i] : 0.0;
+            out[i] = z ? acc * oracle_silu(z[i]) : acc;
+        }
+        for (int64_t n = 0; last_state && n < dstate; ++n)
+            last_state[ch * dstate + n] = st[n];
+    }
+    return 0;
+}
+
+/* Convolution kernel of the time-invariant (LTI, S4) model ("Mamba的三大创新",
+ * stage 3, the convolution mode): with a constant step Delta[d] and
+ * per-channel B[d][n], C[d][n], unrolling the recurrence from a zero state
+ * gives y = K * x with
+ *   K[d][k] = sum_n C[d][n] exp(k Delta[d] A[d][n]) Bbar[d][n],   k = 0 .. L-1,
+ * Bbar = Delta B (zoh = 0, the first-order form) or (exp(Delta A) - 1) / A B
+ * (zoh = 1).  Layouts: delta (dim); A, B, C (dim, dstate); K (dim, L). */
+int oracle_lti_kernel(int64_t dim, int64_t dstate, int64_t seqlen, const double *delta,
+                      const double *A, const double *B, const double *C, int zoh, double *K)
+{
+    if (dim < 0 || dstate <= 0 || seqlen < 0 || !delta || !A || !B || !C || !K)
+        return -1;
+    for (int64_t d = 0; d < dim; ++d) {
+        const double dt = delta[d];
+        for (int64_t k = 0; k < seqlen; ++k) {
+            double acc = 0.0;
+            for (int64_t n = 0; n < dstate; ++n) {
+                const double a = A[d * dstate + n];
+                const double gain = zoh ? (a != 0.0 ? expm1(dt * a) / a : dt) : dt;
+                acc += C[d * dstate + n] * exp((double)k * dt * a) * gain * B[d * dstate + n];
+            }
+            K[d * seqlen + k] = acc;
+        }
+    }
+    return 0;
+}
+
+/* The convolution mode itself: y[b][t][d] = sum_{k=0..t} K[d][k] x[b][t-k][d]
+ * + D[d] x[b][t][d], then the gate silu(z) when z is given (as in
+ * oracle_scan_fwd).  x, z, out: (batch, seqlen, dim); K: (dim, seqlen). */
+int oracle_lti_conv(int64_t batch, int64_t seqlen, int64_t dim, const double *K,
+                    const double *x, const double *D, const double *z, double *out)
+{
+    if (batch < 0 || seqlen < 0 || dim < 0 || (seqlen > 0 && (!K || !x || !out)))
+        return -1;
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t d = 0; d < dim; ++d)
+            for (int64_t t = 0; t < seqlen; ++t) {
+                double y = 0.0;
+                for (int64_t k = 0; k <= t; ++k)
+                    y += K[d * seqlen + k] * x[(b * seqlen + (t - k)) * dim + d];
+                const int64_t tok = (b * seqlen + t) * dim + d;
+                if (D)
+                    y += D[d] * x[tok];
+                if (z)
+                    y *= oracle_silu(z[tok]);
+                out[tok] = y;
+            }
+    return 0;
+}
+
 /* Gradients of oracle_scan_fwd: the loop of that function differentiated
  * by hand in reverse mode (the backward half of training the selective SSM:
  * "Mamba的三大创新", stage 2, the parallel training of the recurrence; the

@@ -285,6 +285,93 @@ def pin_conv_split(lib):
         assert np.array_equal(s2, st_out)
 
 
+# ------------------------------------------------------- exact ZOH and LTI mode
+
+# Z1 -- the exact zero-order hold through scipy's matrix exponential: for each
+#       (step, channel, state) the augmented system [[Delta a, Delta], [0, 0]]
+#       exponentiates to [[Abar, Bbar / b], [0, 1]]; the recurrence is then run
+#       in numpy with those coefficients
+def pin_zoh_expm(lib):
+    from scipy.linalg import expm
+    p = rand_problem(51, bsz=2, L=7, dim=3, N=4)
+    out, last = oracle.scan_fwd(lib=lib, zoh=True, **p)
+    bsz, L, dim = p["x"].shape
+    N = p["A"].shape[1]
+    ref = np.empty_like(out)
+    ref_last = np.empty_like(last)
+    for b in range(bsz):
+        for d in range(dim):
+            h = p["initial_state"][b, d].copy()
+            for t in range(L):
+                dt = softplus_ref(p["delta"][b, t, d] + p["delta_bias"][d])
+                y = 0.0
+                for n in range(N):
+                    E = expm(np.array([[dt * p["A"][d, n], dt], [0.0, 0.0]]))
+                    h[n] = E[0, 0] * h[n] + E[0, 1] * p["B"][b, t, n] * p["x"][b, t, d]
+                    y += p["C"][b, t, n] * h[n]
+                y += p["D"][d] * p["x"][b, t, d]
+                ref[b, t, d] = y * silu_ref(p["z"][b, t, d])
+            ref_last[b, d] = h
+    assert _rel(out, ref) < 1e-11 and _rel(last, ref_last) < 1e-11
+
+
+# Z2 -- N = 1, constant step and input: a first-order filter with gain
+#       g = (r - 1) / a, r = exp(Delta a); h_t = g (1 - r^(t+1)) / (1 - r)
+def pin_zoh_first_order(lib):
+    L, a, dt = 30, -0.7, 0.4
+    one = np.ones((1, L, 1))
+    out, last = oracle.scan_fwd(one, np.full((1, L, 1), dt), np.array([[a]]), one, one,
+                                delta_softplus=False, lib=lib, zoh=True)
+    r = math.exp(dt * a)
+    g = (r - 1.0) / a
+    t = np.arange(L)
+    ref = g * (1.0 - r ** (t + 1)) / (1.0 - r)
+    assert np.max(np.abs(out[0, :, 0] - ref)) < 1e-13
+    assert abs(last[0, 0, 0] - ref[-1]) < 1e-13
+
+
+def _lti_params(seed, dim=3, N=4):
+    r = np.random.default_rng(seed)
+    return (r.uniform(0.05, 0.6, dim), -np.exp(r.uniform(-1.0, 1.5, (dim, N))),
+            r.standard_normal((dim, N)), r.standard_normal((dim, N)))
+
+
+# L1 -- the LTI kernel is the impulse response of the recurrence: for each
+#       channel, the scan (first-order or exact ZOH) over a unit impulse with
+#       constant step, B, C returns K[d][t]
+def pin_lti_kernel_impulse(lib):
+    delta, A, B, C = _lti_params(52)
+    L = 25
+    for zoh in (False, True):
+        K = oracle.lti_kernel(delta, A, B, C, L, zoh=zoh, lib=lib)
+        for d in range(A.shape[0]):
+            x = np.zeros((1, L, 1))
+            x[0, 0, 0] = 1.0
+            y, _ = oracle.scan_fwd(x, np.full((1, L, 1), delta[d]), A[d:d + 1],
+                                   np.broadcast_to(B[d], (1, L, B.shape[1])),
+                                   np.broadcast_to(C[d], (1, L, C.shape[1])),
+                                   delta_softplus=False, lib=lib, zoh=zoh)
+            assert np.max(np.abs(K[d] - y[0, :, 0])) < 1e-13, (zoh, d)
+
+
+# L2 -- the convolution mode against numpy's convolution, plus skip and gate
+def pin_lti_conv_numpy(lib):
+    delta, A, B, C = _lti_params(53)
+    r = np.random.default_rng(54)
+    bsz, L, dim = 2, 19, A.shape[0]
+    K = oracle.lti_kernel(delta, A, B, C, L, lib=lib)
+    x = r.standard_normal((bsz, L, dim))
+    z = r.standard_normal((bsz, L, dim))
+    Dv = r.standard_normal(dim)
+    y = oracle.lti_conv(K, x, D=Dv, z=z, lib=lib)
+    for b in range(bsz):
+        for d in range(dim):
+            ref = np.convolve(K[d], x[b, :, d])[:L] + Dv[d] * x[b, :, d]
+            assert np.max(np.abs(y[b, :, d] - ref * silu_ref(z[b, :, d]))) < 1e-12
+    y0 = oracle.lti_conv(K, x, lib=lib)
+    assert np.max(np.abs(y0[0, :, 1] - np.convolve(K[1], x[0, :, 1])[:L])) < 1e-12
+
+
 # ------------------------------------------------------------------ backward
 # The gradients of the scan (oracle.scan_bwd) are pinned by differentiating
 # the forward numerically and by torch's autograd on an fp64 loop of its own.
@@ -394,4 +481,5 @@ def pin_bwd_thread_count(lib):
 ALL_PINS = [pin_closed_form, pin_prefix_sum, pin_lti_convolution, pin_small_delta,
             pin_large_delta, pin_split_carry, pin_decode_equals_scan, pin_first_order_iir,
             pin_worked_example, pin_nonlinearities, pin_conv_numpy, pin_conv_taps, pin_conv_split,
-            pin_bwd_finite_differences, pin_bwd_directional, pin_bwd_autograd, pin_bwd_thread_count]
+            pin_bwd_finite_differences, pin_bwd_directional, pin_bwd_autograd, pin_bwd_thread_count,
+            pin_zoh_expm, pin_zoh_first_order, pin_lti_kernel_impulse, pin_lti_conv_numpy]

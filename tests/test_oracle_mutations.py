@@ -40,6 +40,15 @@ MUTATIONS = {
     "conv_state_ignored": ("v = conv_state_in ? conv_state_in[(b * dim + d) * H + (H + tt)] : 0.0;\n                    acc +=",
                            "v = 0.0;\n                    acc +="),
     "conv_taps_reversed": ("acc += w[d * width + k] * v;", "acc += w[d * width + (width - 1 - k)] * v;"),
+    # exact zero-order hold and the LTI convolution mode
+    "zoh_gain_not_divided": ("expm1(step * a) / a : step;", "expm1(step * a) : step;"),
+    "zoh_gain_first_order": ("const double gain = a != 0.0 ? expm1(step * a) / a : step;",
+                             "const double gain = step;"),
+    "lti_kernel_lagged": ("exp((double)k * dt * a)", "exp((double)(k + 1) * dt * a)"),
+    "lti_kernel_ignores_zoh": ("const double gain = zoh ? (a != 0.0 ? expm1(dt * a) / a : dt) : dt;",
+                               "const double gain = dt;"),
+    "lti_conv_anticausal": ("x[(b * seqlen + (t - k)) * dim + d]", "x[(b * seqlen + k) * dim + d]"),
+    "lti_conv_skip_dropped": ("                if (D)\n                    y += D[d] * x[tok];\n", "\n"),
     # backward
     "bwd_no_decay_propagation": ("                    g[n] *= dAn;\n", "\n"),
     "bwd_decay_term_uses_h_t": ("ddt += g[n] * (B[row + n] * xv + a * dAn * hp[n]);",
