@@ -19,6 +19,10 @@ needed).  Prints ONE JSON line (rank 0):
   decode       the one-token state update (256 x 5120 x 16, 128 chained steps)
   bwd          the gradients of the same scan (ssm_scan_bwd: states
                recomputed, dx/ddelta/dz/dA/dB/dC/dD/dbias), time per call
+  zoh          the same scan with the exact zero-order-hold input term
+  lti          the time-invariant model's convolution mode (kernel + causal
+               convolution) against the recurrence on the same constant inputs,
+               on the Mamba-130M-shaped layer (the convolution is O(L^2))
   conv_scan    the Mamba block's causal conv (width 4, SiLU) in front of the
                same scan: fused (ssm_conv_scan_fwd, one pass) against the two
                separate calls (ssm_conv1d_fwd writing x_conv, then ssm_scan_fwd)
@@ -69,10 +73,12 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--no-variants", action="store_true", help="skip the zoh and lti sections")
     ap.add_argument("--conv-width", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target wall time of the oracle sample")
-    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd"], default="all",
+    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd", "variants"],
+                    default="all",
                     help="run only the prefill scan part or only the decode part (profiling)")
     return ap.parse_args()
 
@@ -321,6 +327,15 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps(line), flush=True)
         return
+    if args.only == "variants":
+        peak, peak_kind = peaks()
+        w = workload_by_name(args.workload)
+        inp = synth.make_scan_inputs(w, device=str(dev))
+        line = {"zoh": run_zoh(args, w, inp, dev), "lti": run_lti(args, dev),
+                "source_hash": kernel_source_hash()}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.only in ("conv", "bwd"):
         peak, peak_kind = peaks()
         w = workload_by_name(args.workload)
@@ -406,6 +421,9 @@ def run_ours(args, world, rank, local):
         line["conv_scan"] = run_conv(args, w, inp, dev, peak, peak_kind)
     if not args.no_bwd and args.only == "all":
         line["bwd"] = run_bwd(args, w, inp, dev, peak, peak_kind)
+    if not args.no_variants and args.only == "all":
+        line["zoh"] = run_zoh(args, w, inp, dev)
+        line["lti"] = run_lti(args, dev)
     if rank == 0 and world == 1 and not args.no_cpu:
         val, dt, nchan, cores = time_oracle(inp, w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -535,6 +553,90 @@ def run_conv(args, w, inp, dev, peak, peak_kind):
                                 "frac": conv_gbs / peak, "peak_kind": peak_kind,
                                 "algorithmic_bytes_per_launch": conv_bytes,
                                 "traffic": profiled_traffic("conv1d_fwd_" + w.name)}}
+
+
+def _time_calls(fn, dev, steps):
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    return float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]))
+
+
+def run_zoh(args, w, inp, dev):
+    """The forward scan of workload w with the exact zero-order-hold input
+    term (ssm_scan_fwd_ex), beside the first-order one."""
+    from selective_state_space_137_b300 import binding
+    out = torch.empty_like(inp["x"])
+    last = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device=dev)
+    desc = binding.make_desc(w.batch, w.seqlen, w.dim, w.dstate, inp["x"].dtype)
+    ws = torch.empty(max(binding.ssm_scan_workspace_size(desc), 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {"workload": w.name}
+    for name in ("euler", "zoh"):
+        opts = binding.make_opts(name)
+
+        def call():
+            st = binding.ssm_scan_fwd_ex(desc, opts, inp["x"], inp["delta"], inp["A"], inp["B"],
+                                         inp["C"], inp["D"], inp["z"], inp["delta_bias"], out, last,
+                                         None, ws, ws.numel(), stream)
+            if st != binding.SSM_OK:
+                raise binding.SSMError(st, "ssm_scan_fwd_ex")
+        ms = _time_calls(call, dev, max(3, min(args.steps, 10)))
+        res[name] = {"ms": ms, "elements_per_s": w.tokens / (ms * 1e-3)}
+    return res
+
+
+def run_lti(args, dev):
+    """Convolution mode (ssm_lti_kernel + ssm_lti_conv_fwd) against the
+    recurrence (ssm_scan_fwd with a constant step and B, C shared by all
+    channels) on the Mamba-130M-shaped layer, fp32 kernel, bf16 I/O."""
+    from selective_state_space_137_b300 import binding
+    w = synth.MAMBA_130M
+    g = torch.Generator(device=dev).manual_seed(5)
+    N = w.dstate
+    delta = 0.001 + 0.1 * torch.rand(w.dim, generator=g, device=dev)
+    A = -torch.arange(1, N + 1, device=dev, dtype=torch.float32).repeat(w.dim, 1).contiguous()
+    Bv = torch.randn(N, generator=g, device=dev)
+    Cv = torch.randn(N, generator=g, device=dev)
+    Bp, Cp = Bv.repeat(w.dim, 1).contiguous(), Cv.repeat(w.dim, 1).contiguous()
+    x = torch.randn((w.batch, w.seqlen, w.dim), generator=g, device=dev).to(torch.bfloat16)
+    K = torch.empty((w.dim, w.seqlen), dtype=torch.float32, device=dev)
+    y = torch.empty_like(x)
+    kdesc = binding.make_desc(1, w.seqlen, w.dim, N, torch.float32, False)
+    cdesc = binding.make_desc(w.batch, w.seqlen, w.dim, 1, torch.bfloat16, False)
+    stream = torch.cuda.current_stream(dev)
+
+    def kern():
+        assert binding.ssm_lti_kernel(kdesc, None, delta, A, Bp, Cp, K, stream) == binding.SSM_OK
+
+    def conv():
+        assert binding.ssm_lti_conv_fwd(cdesc, K, x, None, None, y, stream) == binding.SSM_OK
+
+    dl = delta[None, None, :].expand(w.batch, w.seqlen, w.dim).contiguous().to(torch.bfloat16)
+    Bs = Bv[None, None, :].expand(w.batch, w.seqlen, N).contiguous().to(torch.bfloat16)
+    Cs = Cv[None, None, :].expand(w.batch, w.seqlen, N).contiguous().to(torch.bfloat16)
+    sdesc = binding.make_desc(w.batch, w.seqlen, w.dim, N, torch.bfloat16, False)
+    ws = torch.empty(max(binding.ssm_scan_workspace_size(sdesc), 16), dtype=torch.uint8, device=dev)
+    last = torch.empty((w.batch, w.dim, N), dtype=torch.float32, device=dev)
+
+    def rec():
+        st = binding.ssm_scan_fwd(sdesc, x, dl, A, Bs, Cs, None, None, None, y, last, None, ws,
+                                  ws.numel(), stream)
+        assert st == binding.SSM_OK
+
+    steps = max(3, min(args.steps, 10))
+    k_ms, c_ms, r_ms = (_time_calls(f, dev, steps) for f in (kern, conv, rec))
+    macs = w.batch * w.dim * w.seqlen * (w.seqlen + 1) / 2
+    return {"workload": w.name, "kernel_ms": k_ms, "conv_ms": c_ms,
+            "conv_gmac_per_s": macs / (c_ms * 1e-3) / 1e9, "recurrence_ms": r_ms,
+            "note": "convolution mode is O(L^2) per channel; the recurrence O(L N)"}
 
 
 def run_bwd(args, w, inp, dev, peak, peak_kind):

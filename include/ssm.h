@@ -123,6 +123,55 @@ SSM_API ssm_status ssm_state_update(const ssm_scan_desc *desc, float *state,
                             const void *z, const float *delta_bias,
                             void *out, void *stream);
 
+/* Discretisation of the input term ("Mamba的三大创新", stage 1, zero-order hold).
+ * The decay is exp(Delta A) in both; the input term is
+ *   SSM_DISC_EULER : Delta B x                      (the first-order form; ssm_scan_fwd)
+ *   SSM_DISC_ZOH   : ((exp(Delta A) - 1) / A) B x   (exact for x held over the step;
+ *                                                     Delta B x where A = 0) */
+typedef enum { SSM_DISC_EULER = 0, SSM_DISC_ZOH = 1 } ssm_discretization;
+
+/* Options of the _ex entry points; reserved[] must be zero. */
+typedef struct {
+    int32_t discretization;   /* ssm_discretization */
+    int32_t reserved[3];
+} ssm_scan_opts;
+
+/* ssm_scan_fwd / ssm_state_update with options (today: the discretisation).
+ * Arguments, layouts, workspace and errors are those of the plain calls;
+ * opts NULL, an unknown discretisation or non-zero reserved fields return
+ * SSM_ERR_INVALID_ARG.  SSM_DISC_ZOH runs in the warp-specialised kernel for
+ * dstate 16 and in the general kernel for the other state sizes. */
+SSM_API ssm_status ssm_scan_fwd_ex(const ssm_scan_desc *desc, const ssm_scan_opts *opts,
+                                   const void *x, const void *delta, const float *A,
+                                   const void *B, const void *C, const float *D, const void *z,
+                                   const float *delta_bias, void *out, float *last_state,
+                                   const float *initial_state, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+SSM_API ssm_status ssm_state_update_ex(const ssm_scan_desc *desc, const ssm_scan_opts *opts,
+                                       float *state, const void *x, const void *delta,
+                                       const float *A, const void *B, const void *C,
+                                       const float *D, const void *z, const float *delta_bias,
+                                       void *out, void *stream);
+
+/* The time-invariant (LTI, S4) model in its convolution mode ("Mamba的三大创新",
+ * stage 3).  With a constant per-channel step delta[d] (> 0, used as given:
+ * no bias, no softplus) and input-independent per-channel B, C, the
+ * recurrence from a zero state is the causal convolution y = K * x with
+ *   K[d][k] = sum_n C[d][n] exp(k delta[d] A[d][n]) Bbar[d][n],  k < seqlen,
+ * Bbar per opts->discretization (NULL opts: first order).
+ *   ssm_lti_kernel  : delta (dim) fp32; A, B, C (dim, dstate) fp32; K out (dim, seqlen) fp32.
+ *                     desc->batch and desc->io_dtype are ignored.
+ *   ssm_lti_conv_fwd: y[b][t][d] = sum_{k<=t} K[d][k] x[b][t-k][d] + D[d] x[b][t][d],
+ *                     gated by silu(z) when z is not NULL.  x, z, out (batch,
+ *                     seqlen, dim) io; K (dim, seqlen) fp32; D (dim) fp32 or NULL.
+ *                     O(seqlen^2) work per (sequence, channel); desc->dstate and
+ *                     desc->delta_softplus are ignored.  out must not alias x. */
+SSM_API ssm_status ssm_lti_kernel(const ssm_scan_desc *desc, const ssm_scan_opts *opts,
+                                  const float *delta, const float *A, const float *B,
+                                  const float *C, float *K, void *stream);
+SSM_API ssm_status ssm_lti_conv_fwd(const ssm_scan_desc *desc, const float *K, const void *x,
+                                    const float *D, const void *z, void *out, void *stream);
+
 /* Gradients of ssm_scan_fwd (the backward half of training; "Mamba的三大创新",
  * stage 2, parallel training of the recurrence).  The states are recomputed
  * from the inputs (stored every 16 steps in the workspace), never kept from

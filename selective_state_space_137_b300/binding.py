@@ -22,7 +22,9 @@ EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
             "ssm_scan_plan", "ssm_status_string", "ssm_version", "ssm_scan_fwd_noalloc",
             "ssm_get_device_status", "ssm_selftest_wait_timeout", "ssm_conv1d_fwd",
             "ssm_conv_scan_fwd", "ssm_conv_state_update", "ssm_scan_bwd_workspace_size",
-            "ssm_scan_bwd")
+            "ssm_scan_bwd", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_lti_kernel",
+            "ssm_lti_conv_fwd")
+SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -34,6 +36,10 @@ class ssm_scan_desc(ctypes.Structure):
 
 class ssm_conv_desc(ctypes.Structure):
     _fields_ = [("width", ctypes.c_int32), ("activation", ctypes.c_int32)]
+
+
+class ssm_scan_opts(ctypes.Structure):
+    _fields_ = [("discretization", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class ssm_scan_plan_info(ctypes.Structure):
@@ -62,6 +68,15 @@ def _load():
     lib.ssm_state_update.argtypes = [dp, fp, vp, vp, fp, vp, vp, fp, vp, fp, vp, vp]
     lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
     lib.ssm_scan_fwd_noalloc.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, vp]
+    op = ctypes.POINTER(ssm_scan_opts)
+    lib.ssm_scan_fwd_ex.restype = ctypes.c_int
+    lib.ssm_scan_fwd_ex.argtypes = [dp, op, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, vp, sz, vp]
+    lib.ssm_state_update_ex.restype = ctypes.c_int
+    lib.ssm_state_update_ex.argtypes = [dp, op, fp, vp, vp, fp, vp, vp, fp, vp, fp, vp, vp]
+    lib.ssm_lti_kernel.restype = ctypes.c_int
+    lib.ssm_lti_kernel.argtypes = [dp, op, fp, fp, fp, fp, fp, vp]
+    lib.ssm_lti_conv_fwd.restype = ctypes.c_int
+    lib.ssm_lti_conv_fwd.argtypes = [dp, fp, vp, fp, vp, vp, vp]
     lib.ssm_scan_bwd_workspace_size.restype = sz
     lib.ssm_scan_bwd_workspace_size.argtypes = [dp]
     lib.ssm_scan_bwd.restype = ctypes.c_int
@@ -220,3 +235,39 @@ def ssm_scan_bwd(desc, x, delta, A, B, C, D, z, delta_bias, initial_state, dout,
                             _ptr(dC), _ptr(dD), _ptr(dz), _ptr(ddelta_bias),
                             _ptr(dinitial_state), _ptr(workspace), int(workspace_bytes),
                             _stream(stream))
+
+
+def make_opts(discretization="euler") -> ssm_scan_opts:
+    code = {"euler": SSM_DISC_EULER, "zoh": SSM_DISC_ZOH}.get(discretization, discretization)
+    o = ssm_scan_opts()
+    o.discretization = int(code)
+    return o
+
+
+def ssm_scan_fwd_ex(desc, opts, x, delta, A, B, C, D, z, delta_bias, out, last_state,
+                    initial_state, workspace, workspace_bytes, stream=None) -> int:
+    """ssm_scan_fwd with options (opts: ssm_scan_opts or None)."""
+    return lib.ssm_scan_fwd_ex(ctypes.byref(desc), None if opts is None else ctypes.byref(opts),
+                               _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                               _ptr(delta_bias), _ptr(out), _ptr(last_state),
+                               _ptr(initial_state), _ptr(workspace), int(workspace_bytes),
+                               _stream(stream))
+
+
+def ssm_state_update_ex(desc, opts, state, x, delta, A, B, C, D, z, delta_bias, out,
+                        stream=None) -> int:
+    return lib.ssm_state_update_ex(ctypes.byref(desc), None if opts is None else ctypes.byref(opts),
+                                   _ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                   _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out), _stream(stream))
+
+
+def ssm_lti_kernel(desc, opts, delta, A, B, C, K, stream=None) -> int:
+    """Convolution kernel K (dim, seqlen) of the time-invariant model."""
+    return lib.ssm_lti_kernel(ctypes.byref(desc), None if opts is None else ctypes.byref(opts),
+                              _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(K), _stream(stream))
+
+
+def ssm_lti_conv_fwd(desc, K, x, D, z, out, stream=None) -> int:
+    """y = K * x + D x (gated by silu(z)), the convolution mode."""
+    return lib.ssm_lti_conv_fwd(ctypes.byref(desc), _ptr(K), _ptr(x), _ptr(D), _ptr(z), _ptr(out),
+                                _stream(stream))

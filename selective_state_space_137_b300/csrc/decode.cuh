@@ -76,8 +76,8 @@ __device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f, bool 
 // threads per block), y is the sequence.  Each thread loads its 16-byte slice
 // of the state, the matching A row slice and B/C slices with vector loads, and
 // the channel's x, delta, z; no integer division is needed to locate them.
-template <typename IO, int N, bool CONV = false>
-__global__ void __launch_bounds__(256, CONV ? 4 : 8) state_update_kernel(DecodeParams p) {
+template <typename IO, int N, bool CONV = false, bool ZOH = false>
+__global__ void __launch_bounds__(256, (CONV || ZOH) ? 4 : 8) state_update_kernel(DecodeParams p) {
     constexpr int LPC = DecodeShape<N>::LPC;
     constexpr int SPL = DecodeShape<N>::SPL;
     const int lin = blockIdx.x * blockDim.x + threadIdx.x;    // lane index within the sequence
@@ -136,7 +136,12 @@ __global__ void __launch_bounds__(256, CONV ? 4 : 8) state_update_kernel(DecodeP
 #pragma unroll
     for (int j = 0; j < SPL; ++j) {
         const float dA = ex2_sfu(dt * (a[j] * kLog2e));
-        h[j] = fmaf(dA, h[j], dx * bv[j]);
+        if (ZOH) {   // exact zero-order hold: ((exp(Delta A) - 1) / A) B x
+            const float gain = a[j] != 0.f ? expm1f(dt * a[j]) / a[j] : dt;
+            h[j] = fmaf(dA, h[j], gain * xv * bv[j]);
+        } else {
+            h[j] = fmaf(dA, h[j], dx * bv[j]);
+        }
         y = fmaf(cv[j], h[j], y);
     }
 #pragma unroll

@@ -46,7 +46,9 @@ constexpr int kMaxConvWidth = 8;
 // MODE_AGG : chunk end-state from a zero start, plus the chunk's sum of Delta.
 enum { MODE_FULL = 0, MODE_AGG = 1 };
 
-template <typename IO, int N, int MODE, bool CONV = false>
+// ZOH: the exact zero-order-hold input term ((exp(Delta A) - 1) / A) B x in
+// place of Delta B x (expm1f keeps it accurate for small Delta A).
+template <typename IO, int N, int MODE, bool CONV = false, bool ZOH = false>
 __global__ void __launch_bounds__(128) scan_generic_kernel(ScanParams p) {
     const int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t b = blockIdx.y;
@@ -129,7 +131,13 @@ __global__ void __launch_bounds__(128) scan_generic_kernel(ScanParams p) {
 #pragma unroll
         for (int n = 0; n < N; ++n) {
             const float dA = ex2_sfu(dt * a2[n]);
-            h[n] = fmaf(dA, h[n], dx * load_f32(Bm + row + n));
+            if (ZOH) {
+                const float an = a2[n] * kLn2;
+                const float gain = an != 0.f ? expm1f(dt * an) / an : dt;
+                h[n] = fmaf(dA, h[n], gain * xv * load_f32(Bm + row + n));
+            } else {
+                h[n] = fmaf(dA, h[n], dx * load_f32(Bm + row + n));
+            }
             if (MODE == MODE_FULL) y = fmaf(load_f32(Cm + row + n), h[n], y);
         }
         if (MODE == MODE_FULL) {

@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "conv.cuh"
 #include "decode.cuh"
+#include "lti.cuh"
 #include "scan_bwd.cuh"
 #include "scan_generic.cuh"
 #include "scan_tiled.cuh"
@@ -75,41 +76,41 @@ size_t workspace_for(const ssm_scan_desc* d, int nchunk) {
     return bytes;
 }
 
-template <typename IO, int N, bool CONV = false>
+template <typename IO, int N, bool CONV = false, bool ZOH = false>
 cudaError_t launch_generic(const ScanParams& p, cudaStream_t s) {
     const dim3 block(128);
     const unsigned gx = (unsigned)((p.dim + 127) / 128);
     if (p.nchunk > 1) {
         dim3 grid(gx, (unsigned)p.batch, (unsigned)(p.nchunk - 1));
-        ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG, CONV><<<grid, block, 0, s>>>(p);
+        ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG, CONV, ZOH><<<grid, block, 0, s>>>(p);
         const int64_t total = p.batch * p.dim * N;
         ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
             p.A, p.initial_state, p.carry, p.dsum, p.batch, p.dim, N, p.nchunk);
     }
     dim3 grid(gx, (unsigned)p.batch, (unsigned)p.nchunk);
-    ssm::scan_generic_kernel<IO, N, ssm::MODE_FULL, CONV><<<grid, block, 0, s>>>(p);
+    ssm::scan_generic_kernel<IO, N, ssm::MODE_FULL, CONV, ZOH><<<grid, block, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-template <typename IO, bool CONV = false>
+template <typename IO, bool CONV = false, bool ZOH = false>
 cudaError_t dispatch_generic(int64_t n, const ScanParams& p, cudaStream_t s) {
     switch (n) {
-        case 1: return launch_generic<IO, 1, CONV>(p, s);
-        case 2: return launch_generic<IO, 2, CONV>(p, s);
-        case 4: return launch_generic<IO, 4, CONV>(p, s);
-        case 8: return launch_generic<IO, 8, CONV>(p, s);
-        case 16: return launch_generic<IO, 16, CONV>(p, s);
-        case 32: return launch_generic<IO, 32, CONV>(p, s);
-        case 64: return launch_generic<IO, 64, CONV>(p, s);
+        case 1: return launch_generic<IO, 1, CONV, ZOH>(p, s);
+        case 2: return launch_generic<IO, 2, CONV, ZOH>(p, s);
+        case 4: return launch_generic<IO, 4, CONV, ZOH>(p, s);
+        case 8: return launch_generic<IO, 8, CONV, ZOH>(p, s);
+        case 16: return launch_generic<IO, 16, CONV, ZOH>(p, s);
+        case 32: return launch_generic<IO, 32, CONV, ZOH>(p, s);
+        case 64: return launch_generic<IO, 64, CONV, ZOH>(p, s);
     }
     return cudaErrorInvalidValue;
 }
 
-template <typename IO, int N, bool CONV = false>
+template <typename IO, int N, bool CONV = false, bool ZOH = false>
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
     const int64_t lanes = p.dim * ssm::DecodeShape<N>::LPC;   // per sequence
     const dim3 grid((unsigned)((lanes + 255) / 256), (unsigned)p.batch);
-    ssm::state_update_kernel<IO, N, CONV><<<grid, 256, 0, s>>>(p);
+    ssm::state_update_kernel<IO, N, CONV, ZOH><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -121,16 +122,16 @@ bool decode_vec_ok(const ssm_scan_desc* d, const void* A, const void* B, const v
            (reinterpret_cast<uintptr_t>(C) % v) == 0;
 }
 
-template <typename IO, bool CONV = false>
+template <typename IO, bool CONV = false, bool ZOH = false>
 cudaError_t dispatch_decode(int64_t n, const DecodeParams& p, cudaStream_t s) {
     switch (n) {
-        case 1: return launch_decode<IO, 1, CONV>(p, s);
-        case 2: return launch_decode<IO, 2, CONV>(p, s);
-        case 4: return launch_decode<IO, 4, CONV>(p, s);
-        case 8: return launch_decode<IO, 8, CONV>(p, s);
-        case 16: return launch_decode<IO, 16, CONV>(p, s);
-        case 32: return launch_decode<IO, 32, CONV>(p, s);
-        case 64: return launch_decode<IO, 64, CONV>(p, s);
+        case 1: return launch_decode<IO, 1, CONV, ZOH>(p, s);
+        case 2: return launch_decode<IO, 2, CONV, ZOH>(p, s);
+        case 4: return launch_decode<IO, 4, CONV, ZOH>(p, s);
+        case 8: return launch_decode<IO, 8, CONV, ZOH>(p, s);
+        case 16: return launch_decode<IO, 16, CONV, ZOH>(p, s);
+        case 32: return launch_decode<IO, 32, CONV, ZOH>(p, s);
+        case 64: return launch_decode<IO, 64, CONV, ZOH>(p, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -305,7 +306,7 @@ cudaError_t launch_tiled(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <typename IO, int CK = 0>
+template <typename IO, int CK = 0, bool ZOH = false>
 cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
     using Cfg = WsConfig<IO, CK>;
     const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -322,8 +323,8 @@ cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
               encode_3d(&maps.out, p.out, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
     if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
     if (!ok) return cudaErrorInvalidValue;
-    auto kfull = ssm::scan_ws_kernel<IO, Cfg, ssm::MODE_FULL>;
-    auto kagg = ssm::scan_ws_kernel<IO, Cfg, ssm::MODE_AGG>;
+    auto kfull = ssm::scan_ws_kernel<IO, Cfg, ssm::MODE_FULL, ZOH>;
+    auto kagg = ssm::scan_ws_kernel<IO, Cfg, ssm::MODE_AGG, ZOH>;
     cudaError_t err = cudaFuncSetAttribute(kfull, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
     if (err == cudaSuccess)
         err = cudaFuncSetAttribute(kagg, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
@@ -414,11 +415,16 @@ size_t ssm_scan_workspace_size(const ssm_scan_desc* desc) {
     return need;
 }
 
-ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta,
-                        const float* A, const void* B, const void* C, const float* D,
-                        const void* z, const float* delta_bias, void* out, float* last_state,
-                        const float* initial_state, void* workspace, size_t workspace_bytes,
-                        void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The scan behind ssm_scan_fwd (zoh = false) and ssm_scan_fwd_ex.
+ssm_status scan_fwd_impl(const ssm_scan_desc* desc, bool zoh, const void* x, const void* delta,
+                         const float* A, const void* B, const void* C, const float* D,
+                         const void* z, const float* delta_bias, void* out, float* last_state,
+                         const float* initial_state, void* workspace, size_t workspace_bytes,
+                         void* stream) {
     const ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -479,16 +485,57 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
     if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
 
     cudaError_t e;
-    if (tiled && ws_path(desc))
-        e = desc->io_dtype == SSM_DTYPE_F32 ? launch_ws<float>(desc, p, s)
-                                            : launch_ws<__nv_bfloat16>(desc, p, s);
-    else if (tiled)
-        e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_tiled<float>(desc, p, s)
-                                            : dispatch_tiled<__nv_bfloat16>(desc, p, s);
-    else
-        e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_generic<float>(N, p, s)
-                                            : dispatch_generic<__nv_bfloat16>(N, p, s);
+    const bool f32 = desc->io_dtype == SSM_DTYPE_F32;
+    if (zoh) {
+        // exact zero-order hold: the warp-specialised kernel for dstate 16,
+        // the generic kernel (with the same chunk plan's workspace) otherwise
+        if (tiled && ws_path(desc))
+            e = f32 ? launch_ws<float, 0, true>(desc, p, s) : launch_ws<__nv_bfloat16, 0, true>(desc, p, s);
+        else
+            e = f32 ? dispatch_generic<float, false, true>(N, p, s)
+                    : dispatch_generic<__nv_bfloat16, false, true>(N, p, s);
+    } else if (tiled && ws_path(desc)) {
+        e = f32 ? launch_ws<float>(desc, p, s) : launch_ws<__nv_bfloat16>(desc, p, s);
+    } else if (tiled) {
+        e = f32 ? dispatch_tiled<float>(desc, p, s) : dispatch_tiled<__nv_bfloat16>(desc, p, s);
+    } else {
+        e = f32 ? dispatch_generic<float>(N, p, s) : dispatch_generic<__nv_bfloat16>(N, p, s);
+    }
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status check_opts(const ssm_scan_opts* o) {
+    if (!o) return SSM_ERR_INVALID_ARG;
+    if (o->discretization != SSM_DISC_EULER && o->discretization != SSM_DISC_ZOH)
+        return SSM_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+        if (o->reserved[i] != 0) return SSM_ERR_INVALID_ARG;
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* delta,
+                        const float* A, const void* B, const void* C, const float* D,
+                        const void* z, const float* delta_bias, void* out, float* last_state,
+                        const float* initial_state, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    return scan_fwd_impl(desc, false, x, delta, A, B, C, D, z, delta_bias, out, last_state,
+                         initial_state, workspace, workspace_bytes, stream);
+}
+
+ssm_status ssm_scan_fwd_ex(const ssm_scan_desc* desc, const ssm_scan_opts* opts, const void* x,
+                           const void* delta, const float* A, const void* B, const void* C,
+                           const float* D, const void* z, const float* delta_bias, void* out,
+                           float* last_state, const float* initial_state, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    const ssm_status so = check_opts(opts);
+    if (so != SSM_OK) return so;
+    return scan_fwd_impl(desc, opts->discretization == SSM_DISC_ZOH, x, delta, A, B, C, D, z,
+                         delta_bias, out, last_state, initial_state, workspace, workspace_bytes,
+                         stream);
 }
 
 ssm_status ssm_selftest_wait_timeout(int64_t limit_ns, void* stream) {
@@ -508,10 +555,14 @@ ssm_status ssm_get_device_status(void) {
     return SSM_ERR_TIMEOUT;
 }
 
-ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void* x,
-                            const void* delta, const float* A, const void* B, const void* C,
-                            const float* D, const void* z, const float* delta_bias, void* out,
-                            void* stream) {
+}  // extern "C"
+
+namespace {
+
+ssm_status state_update_impl(const ssm_scan_desc* desc, bool zoh, float* state, const void* x,
+                             const void* delta, const float* A, const void* B, const void* C,
+                             const float* D, const void* z, const float* delta_bias, void* out,
+                             void* stream) {
     const ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     const size_t esz = io_size(desc);
@@ -533,9 +584,36 @@ ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void*
     p.softplus = desc->delta_softplus ? 1 : 0;
     p.vec = decode_vec_ok(desc, A, B, C);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = desc->io_dtype == SSM_DTYPE_F32 ? dispatch_decode<float>(desc->dstate, p, s)
-                                                    : dispatch_decode<__nv_bfloat16>(desc->dstate, p, s);
+    const bool f32 = desc->io_dtype == SSM_DTYPE_F32;
+    cudaError_t e;
+    if (zoh)
+        e = f32 ? dispatch_decode<float, false, true>(desc->dstate, p, s)
+                : dispatch_decode<__nv_bfloat16, false, true>(desc->dstate, p, s);
+    else
+        e = f32 ? dispatch_decode<float>(desc->dstate, p, s)
+                : dispatch_decode<__nv_bfloat16>(desc->dstate, p, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void* x,
+                            const void* delta, const float* A, const void* B, const void* C,
+                            const float* D, const void* z, const float* delta_bias, void* out,
+                            void* stream) {
+    return state_update_impl(desc, false, state, x, delta, A, B, C, D, z, delta_bias, out, stream);
+}
+
+ssm_status ssm_state_update_ex(const ssm_scan_desc* desc, const ssm_scan_opts* opts, float* state,
+                               const void* x, const void* delta, const float* A, const void* B,
+                               const void* C, const float* D, const void* z,
+                               const float* delta_bias, void* out, void* stream) {
+    const ssm_status so = check_opts(opts);
+    if (so != SSM_OK) return so;
+    return state_update_impl(desc, opts->discretization == SSM_DISC_ZOH, state, x, delta, A, B, C,
+                             D, z, delta_bias, out, stream);
 }
 
 }  // extern "C"
@@ -772,6 +850,59 @@ ssm_status ssm_conv_state_update(const ssm_scan_desc* desc, const ssm_conv_desc*
                         ? dispatch_decode<float, true>(desc->dstate, p, s)
                         : dispatch_decode<__nv_bfloat16, true>(desc->dstate, p, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The time-invariant model's convolution mode.
+extern "C" {
+
+ssm_status ssm_lti_kernel(const ssm_scan_desc* desc, const ssm_scan_opts* opts,
+                          const float* delta, const float* A, const float* B, const float* C,
+                          float* K, void* stream) {
+    if (!desc || desc->dim < 0 || desc->seqlen < 0 || desc->dstate <= 0) return SSM_ERR_INVALID_ARG;
+    if (!dstate_supported(desc->dstate)) return SSM_ERR_UNSUPPORTED;
+    if (opts && check_opts(opts) != SSM_OK) return SSM_ERR_INVALID_ARG;
+    if (!opt_aligned(delta, 4) || !opt_aligned(A, 4) || !opt_aligned(B, 4) || !opt_aligned(C, 4) ||
+        !opt_aligned(K, 4))
+        return SSM_ERR_INVALID_ARG;
+    if (desc->dim == 0 || desc->seqlen == 0) return SSM_OK;
+    if (!delta || !A || !B || !C || !K) return SSM_ERR_INVALID_ARG;
+    const int64_t blocks = desc->dim * ((desc->seqlen + 255) / 256);
+    if (blocks > 0x7fffffff) return SSM_ERR_UNSUPPORTED;
+    ssm::LtiKernelParams p;
+    p.delta = delta; p.A = A; p.B = B; p.C = C; p.K = K;
+    p.dim = desc->dim; p.seqlen = desc->seqlen; p.N = (int)desc->dstate;
+    p.zoh = (opts && opts->discretization == SSM_DISC_ZOH) ? 1 : 0;
+    ssm::lti_kernel_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+ssm_status ssm_lti_conv_fwd(const ssm_scan_desc* desc, const float* K, const void* x,
+                            const float* D, const void* z, void* out, void* stream) {
+    if (!desc || desc->batch < 0 || desc->dim < 0 || desc->seqlen < 0) return SSM_ERR_INVALID_ARG;
+    if (desc->io_dtype != SSM_DTYPE_F32 && desc->io_dtype != SSM_DTYPE_BF16)
+        return SSM_ERR_UNSUPPORTED;
+    const size_t esz = io_size(desc);
+    if (!opt_aligned(K, 4) || !opt_aligned(x, esz) || !opt_aligned(D, 4) || !opt_aligned(z, esz) ||
+        !opt_aligned(out, esz))
+        return SSM_ERR_INVALID_ARG;
+    if (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) return SSM_OK;
+    if (!K || !x || !out) return SSM_ERR_INVALID_ARG;
+    const int64_t ty = (desc->seqlen + ssm::kLtiTo - 1) / ssm::kLtiTo;
+    const int64_t tx = (desc->dim + ssm::kLtiCh - 1) / ssm::kLtiCh;
+    if (ty > 65535 || desc->batch > 65535 || tx > 0x7fffffff) return SSM_ERR_UNSUPPORTED;
+    ssm::LtiConvParams p;
+    p.K = K; p.x = x; p.D = D; p.z = z; p.out = out;
+    p.batch = desc->batch; p.seqlen = desc->seqlen; p.dim = desc->dim;
+    const dim3 grid((unsigned)tx, (unsigned)ty, (unsigned)desc->batch);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (desc->io_dtype == SSM_DTYPE_F32)
+        ssm::lti_conv_kernel<float><<<grid, 256, 0, s>>>(p);
+    else
+        ssm::lti_conv_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -26,10 +26,12 @@ def _check(t, name, shape, dtype, device):
 
 
 def scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, initial_state=None,
-             delta_softplus=True, out=None, last_state=None, workspace=None, stream=None):
+             delta_softplus=True, out=None, last_state=None, workspace=None, stream=None,
+             discretization="euler"):
     """Selective scan forward.  x, delta, z: (batch, seqlen, dim); B, C:
     (batch, seqlen, dstate); A: (dim, dstate) fp32; D, delta_bias: (dim,) fp32;
-    initial_state: (batch, dim, dstate) fp32 or None.
+    initial_state: (batch, dim, dstate) fp32 or None.  ``discretization``:
+    "euler" (input term Delta B x) or "zoh" (exact zero-order hold).
     Returns ``(out, last_state)``."""
     if not x.is_cuda:
         raise ValueError("scan_fwd runs on a CUDA device only")
@@ -53,15 +55,21 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, initial_state=N
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _b.ssm_scan_fwd(desc, x, delta, A, B, C, D, z, delta_bias, out, last_state,
-                         initial_state, workspace if need else None, wbytes if need else 0, stream)
+    if discretization == "euler":
+        st = _b.ssm_scan_fwd(desc, x, delta, A, B, C, D, z, delta_bias, out, last_state,
+                             initial_state, workspace if need else None, wbytes if need else 0,
+                             stream)
+    else:
+        st = _b.ssm_scan_fwd_ex(desc, _b.make_opts(discretization), x, delta, A, B, C, D, z,
+                                delta_bias, out, last_state, initial_state,
+                                workspace if need else None, wbytes if need else 0, stream)
     if st != _b.SSM_OK:
         raise _b.SSMError(st, "ssm_scan_fwd")
     return out, last_state
 
 
 def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, delta_softplus=True,
-                 out=None, stream=None):
+                 out=None, stream=None, discretization="euler"):
     """One decode step in place on ``state`` (batch, dim, dstate) fp32.
     x, delta, z: (batch, dim); B, C: (batch, dstate).  Returns ``out``."""
     if not state.is_cuda:
@@ -80,7 +88,11 @@ def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, delt
     if out is None:
         out = torch.empty_like(x)
     desc = _b.make_desc(bsz, 1, dim, dstate, io, delta_softplus)
-    st = _b.ssm_state_update(desc, state, x, delta, A, B, C, D, z, delta_bias, out, stream)
+    if discretization == "euler":
+        st = _b.ssm_state_update(desc, state, x, delta, A, B, C, D, z, delta_bias, out, stream)
+    else:
+        st = _b.ssm_state_update_ex(desc, _b.make_opts(discretization), state, x, delta, A, B, C,
+                                    D, z, delta_bias, out, stream)
     if st != _b.SSM_OK:
         raise _b.SSMError(st, "ssm_state_update")
     return out
@@ -234,3 +246,39 @@ def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, delta_bias=None, initial_s
     if st != _b.SSM_OK:
         raise _b.SSMError(st, "ssm_scan_bwd")
     return g
+
+
+def lti_kernel(delta, A, B, C, seqlen, discretization="euler", stream=None):
+    """Convolution kernel (dim, seqlen) fp32 of the time-invariant model:
+    delta (dim,), A, B, C (dim, dstate), all fp32 on one device."""
+    if not A.is_cuda:
+        raise ValueError("lti_kernel runs on a CUDA device only")
+    dim, dstate = A.shape
+    dev = A.device
+    for t, name, shape in ((delta, "delta", (dim,)), (B, "B", (dim, dstate)), (C, "C", (dim, dstate))):
+        _check(t, name, shape, torch.float32, dev)
+    K = torch.empty((dim, int(seqlen)), dtype=torch.float32, device=dev)
+    desc = _b.make_desc(1, seqlen, dim, dstate, torch.float32, False)
+    st = _b.ssm_lti_kernel(desc, _b.make_opts(discretization), delta, A, B, C, K, stream)
+    if st != _b.SSM_OK:
+        raise _b.SSMError(st, "ssm_lti_kernel")
+    return K
+
+
+def lti_conv_fwd(K, x, D=None, z=None, out=None, stream=None):
+    """y = K * x + D x, gated by silu(z): the convolution mode.  K (dim,
+    seqlen) fp32; x, z (batch, seqlen, dim)."""
+    if not x.is_cuda:
+        raise ValueError("lti_conv_fwd runs on a CUDA device only")
+    bsz, seqlen, dim = x.shape
+    dev, io = x.device, x.dtype
+    _check(K, "K", (dim, seqlen), torch.float32, dev)
+    _check(D, "D", (dim,), torch.float32, dev)
+    _check(z, "z", x.shape, io, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    desc = _b.make_desc(bsz, seqlen, dim, 1, io, False)
+    st = _b.ssm_lti_conv_fwd(desc, K, x, D, z, out, stream)
+    if st != _b.SSM_OK:
+        raise _b.SSMError(st, "ssm_lti_conv_fwd")
+    return out

@@ -155,3 +155,31 @@ def test_conv_rejections_before_launch(ssm_lib):
     assert step(L.make_conv_desc(4), w=None) == L.SSM_ERR_INVALID_ARG
     assert step(L.ssm_conv_desc(4, -1)) == L.SSM_ERR_INVALID_ARG
     assert step(L.make_conv_desc(4), cs=A16 + 2) == L.SSM_ERR_INVALID_ARG   # misaligned state
+
+
+def test_options_rejections_before_launch(ssm_lib):
+    L = ssm_lib
+    d = L.make_desc(1, 8, 16, 16, L.SSM_DTYPE_F32)
+    args = (A16, A16, A16, A16, A16, None, None, None, A16 + 4096, None, None, None, 0, None)
+    assert L.ssm_scan_fwd_ex(d, None, *args) == L.SSM_ERR_INVALID_ARG           # no options
+    assert L.ssm_scan_fwd_ex(d, L.make_opts(2), *args) == L.SSM_ERR_INVALID_ARG  # unknown
+    o = L.make_opts("zoh")
+    o.reserved[1] = 7
+    assert L.ssm_scan_fwd_ex(d, o, *args) == L.SSM_ERR_INVALID_ARG             # reserved set
+    assert L.ssm_scan_fwd_ex(L.make_desc(1, 8, 16, 3, 0), L.make_opts("zoh"), *args) \
+        == L.SSM_ERR_UNSUPPORTED
+    assert L.ssm_state_update_ex(d, L.make_opts(5), A16, A16, A16, A16, A16, A16, None, None,
+                                 None, A16) == L.SSM_ERR_INVALID_ARG
+
+
+def test_lti_rejections_before_launch(ssm_lib):
+    L = ssm_lib
+    d = L.make_desc(2, 64, 16, 16, L.SSM_DTYPE_F32)
+    assert L.ssm_lti_kernel(L.make_desc(1, 64, 16, 3, 0), None, A16, A16, A16, A16, A16) \
+        == L.SSM_ERR_UNSUPPORTED
+    assert L.ssm_lti_kernel(d, L.make_opts(9), A16, A16, A16, A16, A16) == L.SSM_ERR_INVALID_ARG
+    assert L.ssm_lti_kernel(d, None, A16 + 2, A16, A16, A16, A16) == L.SSM_ERR_INVALID_ARG
+    assert L.ssm_lti_kernel(d, None, None, A16, A16, A16, A16) == L.SSM_ERR_INVALID_ARG
+    assert L.ssm_lti_conv_fwd(d, A16, A16 + 2, None, None, A16) == L.SSM_ERR_INVALID_ARG
+    assert L.ssm_lti_conv_fwd(d, None, A16, None, None, A16) == L.SSM_ERR_INVALID_ARG
+    assert L.ssm_lti_conv_fwd(L.make_desc(0, 64, 16, 1, 0), A16, A16, None, None, A16) == L.SSM_OK

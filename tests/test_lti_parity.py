@@ -1,0 +1,76 @@
+"""GPU parity of the time-invariant model's convolution mode: ssm_lti_kernel
+(the kernel K) and ssm_lti_conv_fwd (y = K * x + D x, gated) against the fp64
+oracle, through the C ABI.  Bounds: K (fp32 output) and y with fp32 I/O
+elementwise 1e-4 (1 + |ref|); y with bf16 I/O 1e-2 (1 + |ref|)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import TOL, f64, rel_err
+from selective_state_space_137_b300 import ops
+
+pytestmark = pytest.mark.gpu
+
+
+def lti_params(dim, N, seed):
+    r = np.random.default_rng(seed)
+    delta = r.uniform(1e-3, 0.3, dim).astype(np.float32)
+    A = (-np.exp(np.log(np.arange(1, N + 1))[None, :].repeat(dim, 0)
+                 + r.uniform(-0.3, 0.3, (dim, N)))).astype(np.float32)
+    B = r.standard_normal((dim, N)).astype(np.float32)
+    C = r.standard_normal((dim, N)).astype(np.float32)
+    return delta, A, B, C
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("N", [1, 4, 16, 64])
+def test_lti_kernel(cuda, disc, N):
+    dim, L = 40, 300
+    delta, A, B, C = lti_params(dim, N, 10 + N)
+    K = ops.lti_kernel(*(torch.from_numpy(a).to(cuda) for a in (delta, A, B, C)), L,
+                       discretization=disc)
+    torch.cuda.synchronize()
+    ref = oracle.lti_kernel(delta, A, B, C, L, zoh=disc == "zoh")
+    assert rel_err(f64(K), ref) <= 1e-4
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 300, 72), (1, 1, 8), (3, 63, 40), (1, 129, 33)])
+def test_lti_conv(cuda, io, shape):
+    bsz, L, dim = shape
+    dt = {"f32": torch.float32, "bf16": torch.bfloat16}[io]
+    delta, A, B, C = lti_params(dim, 16, 5 + L)
+    Kref = oracle.lti_kernel(delta, A, B, C, L)
+    g = torch.Generator().manual_seed(L + dim)
+    x = torch.randn((bsz, L, dim), generator=g).to(dt)
+    z = torch.randn((bsz, L, dim), generator=g).to(dt)
+    D = torch.randn(dim, generator=g)
+    K32 = torch.from_numpy(Kref.astype(np.float32))
+    y = ops.lti_conv_fwd(K32.to(cuda), x.to(cuda), D=D.to(cuda), z=z.to(cuda))
+    y0 = ops.lti_conv_fwd(K32.to(cuda), x.to(cuda))
+    torch.cuda.synchronize()
+    ref = oracle.lti_conv(f64(K32), f64(x), D=f64(D), z=f64(z))
+    ref0 = oracle.lti_conv(f64(K32), f64(x))
+    assert rel_err(f64(y), ref) <= TOL[dt]
+    assert rel_err(f64(y0), ref0) <= TOL[dt]
+
+
+def test_lti_conv_mode_equals_recurrence(cuda):
+    """Convolution mode (kernel + conv) and the recurrence (ssm_scan_fwd with
+    the constant step, B and C shared by all channels) give the same output."""
+    bsz, L, dim, N = 2, 500, 64, 16
+    delta, A, B, C = lti_params(dim, N, 77)
+    B[:] = B[0]
+    C[:] = C[0]
+    t = lambda a: torch.from_numpy(a).to(cuda)
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn((bsz, L, dim), generator=g).to(cuda)
+    K = ops.lti_kernel(t(delta), t(A), t(B), t(C), L)
+    y_conv = ops.lti_conv_fwd(K, x)
+    dl = t(delta)[None, None, :].expand(bsz, L, dim).contiguous()
+    Bs = t(B[0])[None, None, :].expand(bsz, L, N).contiguous()
+    Cs = t(C[0])[None, None, :].expand(bsz, L, N).contiguous()
+    y_rec, _ = ops.scan_fwd(x, dl, t(A), Bs, Cs, delta_softplus=False)
+    torch.cuda.synchronize()
+    assert rel_err(f64(y_conv), f64(y_rec)) <= 1e-4
