@@ -26,7 +26,7 @@ struct DecodeParams {
     void* out;
     int64_t batch, dim;
     int softplus;
-    bool vec = false;   // A 16-byte and B, C (4 x element)-byte aligned: vector loads
+    bool vec = false;   // A 16-byte and B, C (4 x element)-byte aligned: the VEC kernel
     // causal conv in front (read only by kernels instantiated with CONV)
     float* conv_state = nullptr;            // (batch, dim, conv_width - 1), shifted in place
     const float* conv_w = nullptr;          // (dim, conv_width)
@@ -42,11 +42,11 @@ struct DecodeShape {
 };
 
 // SPL consecutive io elements as fp32: 16- or 8-byte loads when SPL allows
-// and the caller's pointers are aligned for them (`vec`, uniform per launch),
+// and the caller's pointers are aligned for them (VEC, chosen at launch),
 // element loads otherwise.
-template <int SPL>
-__device__ __forceinline__ void load_vec(const float* p, float* f, bool vec) {
-    if (SPL % 4 == 0 && vec) {
+template <int SPL, bool VEC>
+__device__ __forceinline__ void load_vec(const float* p, float* f) {
+    if (SPL % 4 == 0 && VEC) {
 #pragma unroll
         for (int j = 0; j < SPL; j += 4) {
             const float4 v = __ldg(reinterpret_cast<const float4*>(p + j));
@@ -57,9 +57,9 @@ __device__ __forceinline__ void load_vec(const float* p, float* f, bool vec) {
         for (int j = 0; j < SPL; ++j) f[j] = __ldg(p + j);
     }
 }
-template <int SPL>
-__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f, bool vec) {
-    if (SPL % 4 == 0 && vec) {
+template <int SPL, bool VEC>
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f) {
+    if (SPL % 4 == 0 && VEC) {
 #pragma unroll
         for (int j = 0; j < SPL; j += 4) {
             const uint2 v = __ldg(reinterpret_cast<const uint2*>(p + j));
@@ -76,7 +76,7 @@ __device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f, bool 
 // threads per block), y is the sequence.  Each thread loads its 16-byte slice
 // of the state, the matching A row slice and B/C slices with vector loads, and
 // the channel's x, delta, z; no integer division is needed to locate them.
-template <typename IO, int N, bool CONV = false, bool ZOH = false>
+template <typename IO, int N, bool CONV = false, bool ZOH = false, bool VEC = true>
 __global__ void __launch_bounds__(256, (CONV || ZOH) ? 4 : 8) state_update_kernel(DecodeParams p) {
     constexpr int LPC = DecodeShape<N>::LPC;
     constexpr int SPL = DecodeShape<N>::SPL;
@@ -106,9 +106,9 @@ __global__ void __launch_bounds__(256, (CONV || ZOH) ? 4 : 8) state_update_kerne
 #pragma unroll
         for (int j = 0; j < SPL; ++j) h[j] = st[j];
     }
-    load_vec<SPL>(p.A + (int64_t)d * N + sub * SPL, a, p.vec);
-    load_vec<SPL>(Bm + b * N + sub * SPL, bv, p.vec);
-    load_vec<SPL>(Cm + b * N + sub * SPL, cv, p.vec);
+    load_vec<SPL, VEC>(p.A + (int64_t)d * N + sub * SPL, a);
+    load_vec<SPL, VEC>(Bm + b * N + sub * SPL, bv);
+    load_vec<SPL, VEC>(Cm + b * N + sub * SPL, cv);
     float xv = load_f32(x + ch);
     if (CONV) {
         // x_conv from the K-1 stored inputs and the new one; the state shift is
