@@ -241,6 +241,34 @@ def lti_conv(K, x, D=None, z=None, lib=None):
     return out
 
 
+def selection_proj(x, W_x, W_dt, dt_rank):
+    """The input-dependent selection of S6 ("Mamba的三大创新", the selection
+    mechanism: Delta, B and C computed from the input by linear projections):
+        xdbl = x W_x^T                  (tokens, dt_rank + 2 N)
+        dt_low, B, C = xdbl[:, :R], xdbl[:, R:R+N], xdbl[:, R+N:]
+        delta_raw = dt_low W_dt^T       (tokens, dim)
+    x: (batch, seqlen, dim); W_x: (R + 2N, dim); W_dt: (dim, R).  fp64 numpy
+    matmuls (a library primitive as the step).  Returns (dt_low, B, C,
+    delta_raw) with the leading (batch, seqlen) shape."""
+    x = _f64(x)
+    W_x = _f64(W_x)
+    W_dt = _f64(W_dt)
+    bsz, seqlen, dim = x.shape
+    R = int(dt_rank)
+    N2 = W_x.shape[0] - R
+    if W_x.shape[1] != dim or W_dt.shape != (dim, R) or N2 <= 0 or N2 % 2:
+        raise ValueError("W_x must be (R + 2N, dim) and W_dt (dim, R)")
+    xdbl = x.reshape(-1, dim) @ W_x.T
+    dt_low = xdbl[:, :R]
+    N = N2 // 2
+    Bm = xdbl[:, R:R + N]
+    Cm = xdbl[:, R + N:]
+    delta = dt_low @ W_dt.T
+    shp = (bsz, seqlen)
+    return (dt_low.reshape(*shp, R), Bm.reshape(*shp, N), Cm.reshape(*shp, N),
+            delta.reshape(*shp, dim))
+
+
 def conv1d_fwd(x, w, bias=None, conv_state=None, activation=True, lib=None):
     """Causal depthwise conv1d (+ SiLU) in fp64.  x: (batch, seqlen, dim);
     w: (dim, width); bias: (dim,); conv_state: (batch, dim, width-1) inputs

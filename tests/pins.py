@@ -372,6 +372,45 @@ def pin_lti_conv_numpy(lib):
     assert np.max(np.abs(y0[0, :, 1] - np.convolve(K[1], x[0, :, 1])[:L])) < 1e-12
 
 
+# ------------------------------------------------------- selection projections
+# oracle.selection_proj is numpy (no C library): ``lib`` is unused here, and
+# the C-source mutations cannot reach it; its own pins are these two.
+
+# P1 -- brute-force triple loops in plain Python on a tiny problem
+def pin_proj_bruteforce(lib):
+    r = np.random.default_rng(61)
+    bsz, L, dim, R, N = 2, 3, 5, 2, 3
+    x = r.standard_normal((bsz, L, dim))
+    Wx = r.standard_normal((R + 2 * N, dim))
+    Wdt = r.standard_normal((dim, R))
+    dt_low, Bm, Cm, delta = oracle.selection_proj(x, Wx, Wdt, R)
+    for b in range(bsz):
+        for t in range(L):
+            xd = [sum(x[b, t, k] * Wx[j, k] for k in range(dim)) for j in range(R + 2 * N)]
+            assert np.allclose(dt_low[b, t], xd[:R], atol=1e-13)
+            assert np.allclose(Bm[b, t], xd[R:R + N], atol=1e-13)
+            assert np.allclose(Cm[b, t], xd[R + N:], atol=1e-13)
+            for d in range(dim):
+                ref = sum(xd[j] * Wdt[d, j] for j in range(R))
+                assert abs(delta[b, t, d] - ref) < 1e-12
+
+
+# P2 -- selector weights: rows of the identity pick input channels out
+def pin_proj_selectors(lib):
+    r = np.random.default_rng(62)
+    bsz, L, dim, R, N = 1, 4, 8, 2, 3
+    x = r.standard_normal((bsz, L, dim))
+    Wx = np.zeros((R + 2 * N, dim))
+    for j in range(R + 2 * N):
+        Wx[j, j] = 1.0                      # xdbl[:, j] = x[:, j]
+    Wdt = np.zeros((dim, R))
+    Wdt[:, 0] = 1.0                         # delta[:, d] = dt_low[:, 0] = x[:, 0]
+    dt_low, Bm, Cm, delta = oracle.selection_proj(x, Wx, Wdt, R)
+    assert np.array_equal(dt_low, x[..., :R]) and np.array_equal(Bm, x[..., R:R + N])
+    assert np.array_equal(Cm, x[..., R + N:R + 2 * N])
+    assert np.array_equal(delta, np.repeat(x[..., :1], dim, axis=-1))
+
+
 # ------------------------------------------------------------------ backward
 # The gradients of the scan (oracle.scan_bwd) are pinned by differentiating
 # the forward numerically and by torch's autograd on an fp64 loop of its own.
@@ -482,4 +521,5 @@ ALL_PINS = [pin_closed_form, pin_prefix_sum, pin_lti_convolution, pin_small_delt
             pin_large_delta, pin_split_carry, pin_decode_equals_scan, pin_first_order_iir,
             pin_worked_example, pin_nonlinearities, pin_conv_numpy, pin_conv_taps, pin_conv_split,
             pin_bwd_finite_differences, pin_bwd_directional, pin_bwd_autograd, pin_bwd_thread_count,
-            pin_zoh_expm, pin_zoh_first_order, pin_lti_kernel_impulse, pin_lti_conv_numpy]
+            pin_zoh_expm, pin_zoh_first_order, pin_lti_kernel_impulse, pin_lti_conv_numpy,
+            pin_proj_bruteforce, pin_proj_selectors]
