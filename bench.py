@@ -23,6 +23,9 @@ needed).  Prints ONE JSON line (rank 0):
   lti          the time-invariant model's convolution mode (kernel + causal
                convolution) against the recurrence on the same constant inputs,
                on the Mamba-130M-shaped layer (the convolution is O(L^2))
+  proj         the selection projections on the tensor cores (x_proj ->
+               dt_low, B, C; dt_proj -> delta) for the same layer (d_model
+               2048: dt_rank 128), against the HBM and bf16 tensor rooflines
   conv_scan    the Mamba block's causal conv (width 4, SiLU) in front of the
                same scan: fused (ssm_conv_scan_fwd, one pass) against the two
                separate calls (ssm_conv1d_fwd writing x_conv, then ssm_scan_fwd)
@@ -74,10 +77,11 @@ def parse():
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip the zoh and lti sections")
+    ap.add_argument("--no-proj", action="store_true")
     ap.add_argument("--conv-width", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target wall time of the oracle sample")
-    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd", "variants"],
+    ap.add_argument("--only", choices=["all", "scan", "decode", "conv", "bwd", "variants", "proj"],
                     default="all",
                     help="run only the prefill scan part or only the decode part (profiling)")
     return ap.parse_args()
@@ -327,6 +331,12 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps(line), flush=True)
         return
+    if args.only == "proj":
+        w = workload_by_name(args.workload)
+        line = {"proj": run_proj(args, w, dev), "source_hash": kernel_source_hash()}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.only == "variants":
         peak, peak_kind = peaks()
         w = workload_by_name(args.workload)
@@ -421,6 +431,8 @@ def run_ours(args, world, rank, local):
         line["conv_scan"] = run_conv(args, w, inp, dev, peak, peak_kind)
     if not args.no_bwd and args.only == "all":
         line["bwd"] = run_bwd(args, w, inp, dev, peak, peak_kind)
+    if not args.no_proj and args.only == "all":
+        line["proj"] = run_proj(args, w, dev)
     if not args.no_variants and args.only == "all":
         line["zoh"] = run_zoh(args, w, inp, dev)
         line["lti"] = run_lti(args, dev)
@@ -567,6 +579,62 @@ def _time_calls(fn, dev, steps):
         ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     return float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]))
+
+
+def tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1800.0, "fallback"
+
+
+def run_proj(args, w, dev):
+    """x_proj and dt_proj of a Mamba layer with w's shape (dim = d_inner;
+    dt_rank = d_model / 16 = dim / 32), bf16, on the tensor cores: time of the
+    x_proj launch alone and of both, each against its HBM bytes and its
+    tensor FLOPs."""
+    from selective_state_space_137_b300 import binding
+    R, N = max(8, w.dim // 32), w.dstate
+    inp = synth.make_proj_inputs(w.batch, w.seqlen, w.dim, R, N, w.seed + 9, device=str(dev))
+    M = w.batch * w.seqlen
+    kw = dict(dtype=torch.bfloat16, device=dev)
+    dt_low = torch.empty((M, R), **kw)
+    Bm, Cm = torch.empty((M, N), **kw), torch.empty((M, N), **kw)
+    delta = torch.empty((M, w.dim), **kw)
+    desc = binding.make_desc(w.batch, w.seqlen, w.dim, N, torch.bfloat16)
+    pd = binding.ssm_proj_desc(R, 0)
+    stream = torch.cuda.current_stream(dev)
+
+    def both():
+        assert binding.ssm_selection_proj_fwd(desc, pd, inp["x"], inp["W_x"], inp["W_dt"], dt_low, Bm,
+                                              Cm, delta, stream) == binding.SSM_OK
+
+    def xonly():
+        assert binding.ssm_selection_proj_fwd(desc, pd, inp["x"], inp["W_x"], None, dt_low, Bm, Cm,
+                                              None, stream) == binding.SSM_OK
+
+    steps = max(3, min(args.steps, 20))
+    x_ms = _time_calls(xonly, dev, steps)
+    all_ms = _time_calls(both, dev, steps)
+    dt_ms = all_ms - x_ms
+    hbm, hbm_kind = peaks()
+    tc, tc_kind = tensor_peak()
+    NO = R + 2 * N
+    x_bytes = (M * w.dim + NO * w.dim + M * NO) * 2
+    x_flops = 2.0 * M * NO * w.dim
+    d_bytes = (M * R + w.dim * R + M * w.dim) * 2
+    d_flops = 2.0 * M * w.dim * R
+
+    def roof(ms, by, fl):
+        gbs = by / (ms * 1e-3) / 1e9
+        tfs = fl / (ms * 1e-3) / 1e12
+        return {"ms": ms, "gb_per_s": gbs, "hbm_frac": gbs / hbm, "tflops": tfs,
+                "tensor_frac": tfs / tc, "algorithmic_bytes": by, "flops": fl}
+    return {"workload": f"{w.name} x_proj ({M}x{w.dim} . {w.dim}x{NO}), dt_proj ({M}x{R} . {R}x{w.dim})",
+            "dt_rank": R, "x_proj": roof(x_ms, x_bytes, x_flops),
+            "dt_proj": roof(dt_ms, d_bytes, d_flops), "both_ms": all_ms,
+            "peaks": {"hbm_gbs": hbm, "hbm_kind": hbm_kind, "bf16_tflops": tc, "tensor_kind": tc_kind}}
 
 
 def run_zoh(args, w, inp, dev):

@@ -172,6 +172,27 @@ SSM_API ssm_status ssm_lti_kernel(const ssm_scan_desc *desc, const ssm_scan_opts
 SSM_API ssm_status ssm_lti_conv_fwd(const ssm_scan_desc *desc, const float *K, const void *x,
                                     const float *D, const void *z, void *out, void *stream);
 
+/* The selection projections of S6 ("Mamba的三大创新", the selection mechanism:
+ * Delta, B and C are linear functions of the input), on the tensor cores:
+ *   xdbl      = x W_x^T            x (batch*seqlen, dim), W_x (R + 2 dstate, dim)
+ *   dt_low    = xdbl[:, 0:R]       (batch, seqlen, R)
+ *   B, C      = xdbl[:, R:R+N], xdbl[:, R+N:R+2N]   (batch, seqlen, dstate) each
+ *   delta_raw = dt_low W_dt^T      W_dt (dim, R) -> (batch, seqlen, dim)
+ * All tensors bf16 (desc->io_dtype must be SSM_DTYPE_BF16), row-major,
+ * 16-byte aligned, with dim and R multiples of 8 and R + 2 dstate <= 256;
+ * fp32 accumulation.  delta_raw is the step before bias and softplus, i.e.
+ * the `delta` input of ssm_scan_fwd; B and C are its B and C.  delta_raw may
+ * be NULL (x_proj only).  Two tcgen05 GEMM launches. */
+typedef struct {
+    int32_t dt_rank;      /* R */
+    int32_t reserved;     /* must be 0 */
+} ssm_proj_desc;
+
+SSM_API ssm_status ssm_selection_proj_fwd(const ssm_scan_desc *desc, const ssm_proj_desc *proj,
+                                          const void *x, const void *W_x, const void *W_dt,
+                                          void *dt_low, void *B, void *C, void *delta_raw,
+                                          void *stream);
+
 /* Gradients of ssm_scan_fwd (the backward half of training; "Mamba的三大创新",
  * stage 2, parallel training of the recurrence).  The states are recomputed
  * from the inputs (stored every 16 steps in the workspace), never kept from

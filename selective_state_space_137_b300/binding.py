@@ -23,7 +23,7 @@ EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
             "ssm_get_device_status", "ssm_selftest_wait_timeout", "ssm_conv1d_fwd",
             "ssm_conv_scan_fwd", "ssm_conv_state_update", "ssm_scan_bwd_workspace_size",
             "ssm_scan_bwd", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_lti_kernel",
-            "ssm_lti_conv_fwd")
+            "ssm_lti_conv_fwd", "ssm_selection_proj_fwd")
 SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -40,6 +40,10 @@ class ssm_conv_desc(ctypes.Structure):
 
 class ssm_scan_opts(ctypes.Structure):
     _fields_ = [("discretization", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+
+
+class ssm_proj_desc(ctypes.Structure):
+    _fields_ = [("dt_rank", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class ssm_scan_plan_info(ctypes.Structure):
@@ -77,6 +81,9 @@ def _load():
     lib.ssm_lti_kernel.argtypes = [dp, op, fp, fp, fp, fp, fp, vp]
     lib.ssm_lti_conv_fwd.restype = ctypes.c_int
     lib.ssm_lti_conv_fwd.argtypes = [dp, fp, vp, fp, vp, vp, vp]
+    lib.ssm_selection_proj_fwd.restype = ctypes.c_int
+    lib.ssm_selection_proj_fwd.argtypes = [dp, ctypes.POINTER(ssm_proj_desc), vp, vp, vp, vp, vp, vp,
+                                           vp, vp]
     lib.ssm_scan_bwd_workspace_size.restype = sz
     lib.ssm_scan_bwd_workspace_size.argtypes = [dp]
     lib.ssm_scan_bwd.restype = ctypes.c_int
@@ -271,3 +278,10 @@ def ssm_lti_conv_fwd(desc, K, x, D, z, out, stream=None) -> int:
     """y = K * x + D x (gated by silu(z)), the convolution mode."""
     return lib.ssm_lti_conv_fwd(ctypes.byref(desc), _ptr(K), _ptr(x), _ptr(D), _ptr(z), _ptr(out),
                                 _stream(stream))
+
+
+def ssm_selection_proj_fwd(desc, proj, x, W_x, W_dt, dt_low, B, C, delta_raw, stream=None) -> int:
+    """x_proj (-> dt_low, B, C) and dt_proj (-> delta_raw) on the tensor cores."""
+    return lib.ssm_selection_proj_fwd(ctypes.byref(desc), ctypes.byref(proj), _ptr(x), _ptr(W_x),
+                                      _ptr(W_dt), _ptr(dt_low), _ptr(B), _ptr(C), _ptr(delta_raw),
+                                      _stream(stream))

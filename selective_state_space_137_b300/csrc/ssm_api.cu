@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "conv.cuh"
 #include "decode.cuh"
+#include "gemm.cuh"
 #include "lti.cuh"
 #include "scan_bwd.cuh"
 #include "scan_generic.cuh"
@@ -856,6 +857,139 @@ ssm_status ssm_conv_state_update(const ssm_scan_desc* desc, const ssm_conv_desc*
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The selection projections (tcgen05 GEMMs).
+namespace {
+
+// 2-D bf16 tensor map of a row-major (rows, cols) matrix, box [box_rows][64],
+// 128-byte swizzle (the tcgen05 K-major operand layout).
+bool encode_2d_sw128(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t ld,
+                     int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    const cuuint32_t box[2] = {(cuuint32_t)ssm::kGemmBK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+#ifndef SSM_XPROJ_STAGES
+#define SSM_XPROJ_STAGES 3   // TMA ring depth of x_proj (K = dim: a long loop)
+#endif
+#ifndef SSM_DTPROJ_BN
+#define SSM_DTPROJ_BN 128    // dt_proj tile width
+#endif
+#ifndef SSM_DTPROJ_STAGES
+#define SSM_DTPROJ_STAGES 2  // dt_proj ring depth (K = dt_rank: a few slabs)
+#endif
+
+template <int BN, int STAGES>
+cudaError_t launch_gemm(const void* A, const void* Bw, int64_t M, int N, int K, const ssm::GemmParams& p,
+                        cudaStream_t s) {
+    using Cfg = ssm::GemmCfg<BN, STAGES>;
+    ssm::GemmMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (!encode_2d_sw128(&maps.a, A, K, M, K, ssm::kGemmBM) ||
+        !encode_2d_sw128(&maps.b, Bw, K, N, K, BN))
+        return cudaErrorInvalidValue;
+    auto k = ssm::gemm_bf16_tn_kernel<BN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((M + ssm::kGemmBM - 1) / ssm::kGemmBM), (unsigned)((N + BN - 1) / BN));
+    k<<<grid, ssm::kGemmThreads, Cfg::SMEM, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+// The persistent form (dt_proj): as many CTAs as fit on the GPU at once
+// (shared memory and the 512 TMEM columns of an SM), each walking tiles.
+template <int BN, int STAGES>
+cudaError_t launch_gemm_persistent(const void* A, const void* Bw, int64_t M, int N, int K,
+                                   const ssm::GemmParams& p, cudaStream_t s) {
+    using Cfg = ssm::GemmPCfg<BN, STAGES>;
+    ssm::GemmMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (!encode_2d_sw128(&maps.a, A, K, M, K, ssm::kGemmBM) ||
+        !encode_2d_sw128(&maps.b, Bw, K, N, K, BN))
+        return cudaErrorInvalidValue;
+    auto k = ssm::gemm_bf16_tn_persistent_kernel<BN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    int per_sm = (228 * 1024) / (Cfg::SMEM + 1024);
+    if (per_sm > 512 / Cfg::TMEM_COLS) per_sm = 512 / Cfg::TMEM_COLS;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t tiles = ((M + ssm::kGemmBM - 1) / ssm::kGemmBM) * ((N + BN - 1) / BN);
+    if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+    int64_t grid = (int64_t)kPlanSMs * per_sm;
+    if (grid > tiles) grid = tiles;
+    k<<<(unsigned)grid, ssm::kGemmPThreads, Cfg::SMEM, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+// x_proj: the whole (R + 2N)-wide output in one tile column (BN = its size
+// rounded up to 32).
+cudaError_t launch_xproj(int bn, const void* A, const void* Bw, int64_t M, int N, int K,
+                         const ssm::GemmParams& p, cudaStream_t s) {
+    switch (bn) {
+        case 32: return launch_gemm<32, SSM_XPROJ_STAGES>(A, Bw, M, N, K, p, s);
+        case 64: return launch_gemm<64, SSM_XPROJ_STAGES>(A, Bw, M, N, K, p, s);
+        case 96: return launch_gemm<96, SSM_XPROJ_STAGES>(A, Bw, M, N, K, p, s);
+        case 128: return launch_gemm<128, SSM_XPROJ_STAGES>(A, Bw, M, N, K, p, s);
+        case 160: return launch_gemm<160, SSM_XPROJ_STAGES>(A, Bw, M, N, K, p, s);
+        case 192: return launch_gemm<192, SSM_XPROJ_STAGES>(A, Bw, M, N, K, p, s);
+        case 224: return launch_gemm<224, SSM_XPROJ_STAGES>(A, Bw, M, N, K, p, s);
+        case 256: return launch_gemm<256, SSM_XPROJ_STAGES>(A, Bw, M, N, K, p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+extern "C" ssm_status ssm_selection_proj_fwd(const ssm_scan_desc* desc, const ssm_proj_desc* proj,
+                                             const void* x, const void* W_x, const void* W_dt,
+                                             void* dt_low, void* B, void* C, void* delta_raw,
+                                             void* stream) {
+    if (!desc || !proj) return SSM_ERR_INVALID_ARG;
+    if (desc->batch < 0 || desc->seqlen < 0 || desc->dim < 0 || desc->dstate <= 0 ||
+        proj->dt_rank <= 0 || proj->reserved != 0)
+        return SSM_ERR_INVALID_ARG;
+    if (desc->io_dtype != SSM_DTYPE_BF16) return SSM_ERR_UNSUPPORTED;
+    const int64_t R = proj->dt_rank, N = desc->dstate, Dm = desc->dim;
+    const int64_t M = desc->batch * desc->seqlen;
+    const int64_t NO = R + 2 * N;
+    if (Dm % 8 != 0 || R % 8 != 0 || NO > 256 || Dm > ((int64_t)1 << 30) || M >= ((int64_t)1 << 31))
+        return SSM_ERR_UNSUPPORTED;
+    for (const void* q : std::initializer_list<const void*>{x, W_x, W_dt, dt_low, B, C, delta_raw})
+        if (!opt_aligned(q, 16)) return SSM_ERR_INVALID_ARG;
+    if (M == 0 || Dm == 0) return SSM_OK;
+    if (!x || !W_x || !dt_low || !B || !C || (delta_raw && !W_dt)) return SSM_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    ssm::GemmParams p1;
+    memset(&p1, 0, sizeof(p1));
+    p1.M = M; p1.N = (int)NO; p1.K = (int)Dm;
+    p1.seg[0] = {dt_low, R, 0, (int)R};
+    p1.seg[1] = {B, N, (int)R, (int)N};
+    p1.seg[2] = {C, N, (int)(R + N), (int)N};
+    p1.nseg = 3;
+    const int bn = (int)((NO + 31) / 32 * 32);
+    cudaError_t e = launch_xproj(bn, x, W_x, M, (int)NO, (int)Dm, p1, s);
+    if (e != cudaSuccess) return SSM_ERR_CUDA;
+    if (delta_raw) {
+        ssm::GemmParams p2;
+        memset(&p2, 0, sizeof(p2));
+        p2.M = M; p2.N = (int)Dm; p2.K = (int)R;
+        p2.seg[0] = {delta_raw, Dm, 0, (int)Dm};
+        p2.nseg = 1;
+        if (launch_gemm_persistent<SSM_DTPROJ_BN, SSM_DTPROJ_STAGES>(dt_low, W_dt, M, (int)Dm, (int)R,
+                                                                     p2, s) != cudaSuccess)
+            return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
+}
 
 // ---------------------------------------------------------------------------
 // The time-invariant model's convolution mode.

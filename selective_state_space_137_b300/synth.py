@@ -22,6 +22,12 @@ initialisation of a depthwise Conv1d layer with K taps (fan-in K):
   conv_bias[d]    ~ U[-1/sqrt(K), 1/sqrt(K)]       shape (dim,)
   conv_state      ~ N(0, 1)                        shape (batch, dim, K-1)
 
+Selection projections (own seeded stream; bf16), the default initialisation
+of the two linear layers (fan-in dim and R):
+  x               ~ N(0, 1)                        shape (batch, seqlen, dim)
+  W_x[j, k]       ~ U[-1/sqrt(dim), 1/sqrt(dim)]   shape (R + 2N, dim)
+  W_dt[d, r]      ~ U[-1/sqrt(R), 1/sqrt(R)]       shape (dim, R)
+
 On ``device="cpu"`` the draws come from numpy's PCG64 stream (bit-identical on
 every machine).  On a CUDA device they come from torch's device generator,
 which is much faster for the multi-GB workloads; both are seeded.
@@ -183,3 +189,15 @@ def make_conv_inputs(batch: int, dim: int, width: int, seed: int, device: str = 
     bias = g.uniform((dim,), -bound, bound).to(torch.float32) if with_bias else None
     state = g.normal((batch, dim, width - 1)).contiguous() if with_state else None
     return dict(conv_w=w, conv_bias=bias, conv_state=state)
+
+
+def make_proj_inputs(batch: int, seqlen: int, dim: int, dt_rank: int, dstate: int, seed: int,
+                     device: str = "cpu") -> dict:
+    """Draw x and the two projection weights, bf16."""
+    g = _Draw(seed, device)
+    x = g.normal((batch, seqlen, dim)).to(torch.bfloat16)
+    bx = 1.0 / float(dim) ** 0.5
+    bd = 1.0 / float(dt_rank) ** 0.5
+    W_x = g.uniform((dt_rank + 2 * dstate, dim), -bx, bx).to(torch.bfloat16).contiguous()
+    W_dt = g.uniform((dim, dt_rank), -bd, bd).to(torch.bfloat16).contiguous()
+    return dict(x=x, W_x=W_x, W_dt=W_dt)
