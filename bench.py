@@ -333,7 +333,8 @@ def run_ours(args, world, rank, local):
         return
     if args.only == "proj":
         w = workload_by_name(args.workload)
-        line = {"proj": run_proj(args, w, dev), "source_hash": kernel_source_hash()}
+        sinp = synth.make_scan_inputs(w, device=str(dev))
+        line = {"proj": run_proj(args, w, dev, sinp), "source_hash": kernel_source_hash()}
         if rank == 0:
             print(json.dumps(line), flush=True)
         return
@@ -432,7 +433,7 @@ def run_ours(args, world, rank, local):
     if not args.no_bwd and args.only == "all":
         line["bwd"] = run_bwd(args, w, inp, dev, peak, peak_kind)
     if not args.no_proj and args.only == "all":
-        line["proj"] = run_proj(args, w, dev)
+        line["proj"] = run_proj(args, w, dev, inp)
     if not args.no_variants and args.only == "all":
         line["zoh"] = run_zoh(args, w, inp, dev)
         line["lti"] = run_lti(args, dev)
@@ -589,7 +590,7 @@ def tensor_peak():
         return 1800.0, "fallback"
 
 
-def run_proj(args, w, dev):
+def run_proj(args, w, dev, scan_inp=None):
     """x_proj and dt_proj of a Mamba layer with w's shape (dim = d_inner;
     dt_rank = d_model / 16 = dim / 32), bf16, on the tensor cores: time of the
     x_proj launch alone and of both, each against its HBM bytes and its
@@ -602,17 +603,17 @@ def run_proj(args, w, dev):
     dt_low = torch.empty((M, R), **kw)
     Bm, Cm = torch.empty((M, N), **kw), torch.empty((M, N), **kw)
     delta = torch.empty((M, w.dim), **kw)
-    desc = binding.make_desc(w.batch, w.seqlen, w.dim, N, torch.bfloat16)
+    desc = binding.make_desc(w.batch, w.seqlen, w.dim, N, torch.bfloat16, False)   # raw step
     pd = binding.ssm_proj_desc(R, 0)
     stream = torch.cuda.current_stream(dev)
 
     def both():
-        assert binding.ssm_selection_proj_fwd(desc, pd, inp["x"], inp["W_x"], inp["W_dt"], dt_low, Bm,
-                                              Cm, delta, stream) == binding.SSM_OK
+        assert binding.ssm_selection_proj_fwd(desc, pd, inp["x"], inp["W_x"], inp["W_dt"], None, dt_low,
+                                              Bm, Cm, delta, stream) == binding.SSM_OK
 
     def xonly():
-        assert binding.ssm_selection_proj_fwd(desc, pd, inp["x"], inp["W_x"], None, dt_low, Bm, Cm,
-                                              None, stream) == binding.SSM_OK
+        assert binding.ssm_selection_proj_fwd(desc, pd, inp["x"], inp["W_x"], None, None, dt_low, Bm,
+                                              Cm, None, stream) == binding.SSM_OK
 
     steps = max(3, min(args.steps, 20))
     x_ms = _time_calls(xonly, dev, steps)
@@ -631,10 +632,58 @@ def run_proj(args, w, dev):
         tfs = fl / (ms * 1e-3) / 1e12
         return {"ms": ms, "gb_per_s": gbs, "hbm_frac": gbs / hbm, "tflops": tfs,
                 "tensor_frac": tfs / tc, "algorithmic_bytes": by, "flops": fl}
-    return {"workload": f"{w.name} x_proj ({M}x{w.dim} . {w.dim}x{NO}), dt_proj ({M}x{R} . {R}x{w.dim})",
-            "dt_rank": R, "x_proj": roof(x_ms, x_bytes, x_flops),
-            "dt_proj": roof(dt_ms, d_bytes, d_flops), "both_ms": all_ms,
-            "peaks": {"hbm_gbs": hbm, "hbm_kind": hbm_kind, "bf16_tflops": tc, "tensor_kind": tc_kind}}
+    res = {"workload": f"{w.name} x_proj ({M}x{w.dim} . {w.dim}x{NO}), dt_proj ({M}x{R} . {R}x{w.dim})",
+           "dt_rank": R, "x_proj": roof(x_ms, x_bytes, x_flops),
+           "dt_proj": roof(dt_ms, d_bytes, d_flops), "both_ms": all_ms,
+           "peaks": {"hbm_gbs": hbm, "hbm_kind": hbm_kind, "bf16_tflops": tc, "tensor_kind": tc_kind}}
+    if scan_inp is not None:
+        # projections + scan, the step finished in dt_proj's epilogue (bias,
+        # softplus) against the raw projection with softplus and bias in the scan
+        out = torch.empty_like(scan_inp["x"])
+        last = torch.empty((w.batch, w.dim, N), dtype=torch.float32, device=dev)
+        x3 = inp["x"]
+        B3, C3 = Bm.view(w.batch, w.seqlen, N), Cm.view(w.batch, w.seqlen, N)
+        d3 = delta.view(w.batch, w.seqlen, w.dim)
+        sdesc = binding.make_desc(w.batch, w.seqlen, w.dim, N, torch.bfloat16, True)
+        sdesc0 = binding.make_desc(w.batch, w.seqlen, w.dim, N, torch.bfloat16, False)
+        pdesc0 = binding.make_desc(w.batch, w.seqlen, w.dim, N, torch.bfloat16, False)
+        ws = torch.empty(max(binding.ssm_scan_workspace_size(sdesc), 16), dtype=torch.uint8,
+                         device=dev)
+        bias = scan_inp["delta_bias"]
+
+        def fused():
+            assert binding.ssm_selection_proj_fwd(desc, pd, x3, inp["W_x"], inp["W_dt"], bias, dt_low,
+                                                  Bm, Cm, delta, stream) == binding.SSM_OK
+            assert binding.ssm_scan_fwd(sdesc0, x3, d3, scan_inp["A"], B3, C3, scan_inp["D"],
+                                        scan_inp["z"], None, out, last, None, ws, ws.numel(),
+                                        stream) == binding.SSM_OK
+
+        def unfused():
+            assert binding.ssm_selection_proj_fwd(pdesc0, pd, x3, inp["W_x"], inp["W_dt"], None, dt_low,
+                                                  Bm, Cm, delta, stream) == binding.SSM_OK
+            assert binding.ssm_scan_fwd(sdesc, x3, d3, scan_inp["A"], B3, C3, scan_inp["D"],
+                                        scan_inp["z"], bias, out, last, None, ws, ws.numel(),
+                                        stream) == binding.SSM_OK
+        def scan_sp():
+            assert binding.ssm_scan_fwd(sdesc, x3, d3, scan_inp["A"], B3, C3, scan_inp["D"],
+                                        scan_inp["z"], bias, out, last, None, ws, ws.numel(),
+                                        stream) == binding.SSM_OK
+
+        def scan_nosp():
+            assert binding.ssm_scan_fwd(sdesc0, x3, d3, scan_inp["A"], B3, C3, scan_inp["D"],
+                                        scan_inp["z"], None, out, last, None, ws, ws.numel(),
+                                        stream) == binding.SSM_OK
+
+        def proj_sp():
+            assert binding.ssm_selection_proj_fwd(desc_sp, pd, x3, inp["W_x"], inp["W_dt"], bias,
+                                                  dt_low, Bm, Cm, delta, stream) == binding.SSM_OK
+        desc_sp = binding.make_desc(w.batch, w.seqlen, w.dim, N, torch.bfloat16, True)
+        res["pipeline"] = {"step_in_dt_proj_ms": _time_calls(fused, dev, steps),
+                           "step_in_scan_ms": _time_calls(unfused, dev, steps),
+                           "proj_with_softplus_epilogue_ms": _time_calls(proj_sp, dev, steps),
+                           "scan_with_softplus_ms": _time_calls(scan_sp, dev, steps),
+                           "scan_without_softplus_ms": _time_calls(scan_nosp, dev, steps)}
+    return res
 
 
 def run_zoh(args, w, inp, dev):

@@ -174,15 +174,19 @@ SSM_API ssm_status ssm_lti_conv_fwd(const ssm_scan_desc *desc, const float *K, c
 
 /* The selection projections of S6 ("Mamba的三大创新", the selection mechanism:
  * Delta, B and C are linear functions of the input), on the tensor cores:
- *   xdbl      = x W_x^T            x (batch*seqlen, dim), W_x (R + 2 dstate, dim)
- *   dt_low    = xdbl[:, 0:R]       (batch, seqlen, R)
- *   B, C      = xdbl[:, R:R+N], xdbl[:, R+N:R+2N]   (batch, seqlen, dstate) each
- *   delta_raw = dt_low W_dt^T      W_dt (dim, R) -> (batch, seqlen, dim)
- * All tensors bf16 (desc->io_dtype must be SSM_DTYPE_BF16), row-major,
+ *   xdbl   = x W_x^T            x (batch*seqlen, dim), W_x (R + 2 dstate, dim)
+ *   dt_low = xdbl[:, 0:R]       (batch, seqlen, R)
+ *   B, C   = xdbl[:, R:R+N], xdbl[:, R+N:R+2N]   (batch, seqlen, dstate) each
+ *   delta  = act(dt_low W_dt^T + delta_bias)     W_dt (dim, R) -> (batch, seqlen, dim)
+ * act = softplus when desc->delta_softplus is 1, identity when 0; delta_bias
+ * (dim) fp32 or NULL (zero).  With act = softplus, `delta` is the step Delta
+ * itself: pass it to ssm_scan_fwd with delta_softplus = 0 and no delta_bias
+ * (the scan's prologue work done in this epilogue).  With act = identity and
+ * no bias it is the raw step, for ssm_scan_fwd with softplus and bias.
+ * All other tensors bf16 (desc->io_dtype must be SSM_DTYPE_BF16), row-major,
  * 16-byte aligned, with dim and R multiples of 8 and R + 2 dstate <= 256;
- * fp32 accumulation.  delta_raw is the step before bias and softplus, i.e.
- * the `delta` input of ssm_scan_fwd; B and C are its B and C.  delta_raw may
- * be NULL (x_proj only).  Two tcgen05 GEMM launches. */
+ * fp32 accumulation, one bf16 rounding per output.  delta may be NULL
+ * (x_proj only).  Two tcgen05 GEMM launches. */
 typedef struct {
     int32_t dt_rank;      /* R */
     int32_t reserved;     /* must be 0 */
@@ -190,8 +194,8 @@ typedef struct {
 
 SSM_API ssm_status ssm_selection_proj_fwd(const ssm_scan_desc *desc, const ssm_proj_desc *proj,
                                           const void *x, const void *W_x, const void *W_dt,
-                                          void *dt_low, void *B, void *C, void *delta_raw,
-                                          void *stream);
+                                          const float *delta_bias, void *dt_low, void *B, void *C,
+                                          void *delta, void *stream);
 
 /* Gradients of ssm_scan_fwd (the backward half of training; "Mamba的三大创新",
  * stage 2, parallel training of the recurrence).  The states are recomputed

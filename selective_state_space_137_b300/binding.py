@@ -82,8 +82,8 @@ def _load():
     lib.ssm_lti_conv_fwd.restype = ctypes.c_int
     lib.ssm_lti_conv_fwd.argtypes = [dp, fp, vp, fp, vp, vp, vp]
     lib.ssm_selection_proj_fwd.restype = ctypes.c_int
-    lib.ssm_selection_proj_fwd.argtypes = [dp, ctypes.POINTER(ssm_proj_desc), vp, vp, vp, vp, vp, vp,
-                                           vp, vp]
+    lib.ssm_selection_proj_fwd.argtypes = [dp, ctypes.POINTER(ssm_proj_desc), vp, vp, vp, fp, vp, vp,
+                                           vp, vp, vp]
     lib.ssm_scan_bwd_workspace_size.restype = sz
     lib.ssm_scan_bwd_workspace_size.argtypes = [dp]
     lib.ssm_scan_bwd.restype = ctypes.c_int
@@ -280,8 +280,10 @@ def ssm_lti_conv_fwd(desc, K, x, D, z, out, stream=None) -> int:
                                 _stream(stream))
 
 
-def ssm_selection_proj_fwd(desc, proj, x, W_x, W_dt, dt_low, B, C, delta_raw, stream=None) -> int:
-    """x_proj (-> dt_low, B, C) and dt_proj (-> delta_raw) on the tensor cores."""
+def ssm_selection_proj_fwd(desc, proj, x, W_x, W_dt, delta_bias, dt_low, B, C, delta,
+                           stream=None) -> int:
+    """x_proj (-> dt_low, B, C) and dt_proj (-> delta = act(dt_low W_dt^T +
+    delta_bias), act = softplus iff desc.delta_softplus) on the tensor cores."""
     return lib.ssm_selection_proj_fwd(ctypes.byref(desc), ctypes.byref(proj), _ptr(x), _ptr(W_x),
-                                      _ptr(W_dt), _ptr(dt_low), _ptr(B), _ptr(C), _ptr(delta_raw),
-                                      _stream(stream))
+                                      _ptr(W_dt), _ptr(delta_bias), _ptr(dt_low), _ptr(B), _ptr(C),
+                                      _ptr(delta), _stream(stream))

@@ -23,6 +23,7 @@
 // and exits.
 #pragma once
 #include "common.cuh"
+#include "scan_tiled.cuh"   // softplus_tiled
 #include "tma.cuh"
 
 namespace ssm {
@@ -40,6 +41,9 @@ struct GemmParams {
     int N, K;         // columns of C (rows of B), reduction length
     GemmSeg seg[3];
     int nseg;
+    // epilogue of the persistent kernel: c = act(c + col_bias[col])
+    const float* col_bias = nullptr;   // (N) or NULL
+    int act = 0;                        // 0: none, 1: softplus
 };
 
 template <int BN, int S_>
@@ -422,10 +426,19 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
             __syncwarp();
             tc_fence_after();
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * Cfg::ACC_COLS);
+            const int n0e = (t / mtiles) * BN;
 #pragma unroll 1
             for (int c = 0; c < BN; c += 16) {
                 float v[16];
                 tmem_ld16(base + (uint32_t)c, v);
+                if (p.col_bias || p.act) {   // the step Delta = softplus(c + bias), finished here
+#pragma unroll
+                    for (int k2 = 0; k2 < 16; ++k2) {
+                        const int col = n0e + c + k2;
+                        float u = v[k2] + ((p.col_bias && col < p.N) ? __ldg(p.col_bias + col) : 0.f);
+                        v[k2] = p.act ? softplus_tiled<__nv_bfloat16>(u) : u;
+                    }
+                }
                 uint32_t w[8];
 #pragma unroll
                 for (int k2 = 0; k2 < 8; ++k2) {

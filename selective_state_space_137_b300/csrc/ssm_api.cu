@@ -950,8 +950,8 @@ cudaError_t launch_xproj(int bn, const void* A, const void* Bw, int64_t M, int N
 
 extern "C" ssm_status ssm_selection_proj_fwd(const ssm_scan_desc* desc, const ssm_proj_desc* proj,
                                              const void* x, const void* W_x, const void* W_dt,
-                                             void* dt_low, void* B, void* C, void* delta_raw,
-                                             void* stream) {
+                                             const float* delta_bias, void* dt_low, void* B,
+                                             void* C, void* delta_raw, void* stream) {
     if (!desc || !proj) return SSM_ERR_INVALID_ARG;
     if (desc->batch < 0 || desc->seqlen < 0 || desc->dim < 0 || desc->dstate <= 0 ||
         proj->dt_rank <= 0 || proj->reserved != 0)
@@ -964,6 +964,7 @@ extern "C" ssm_status ssm_selection_proj_fwd(const ssm_scan_desc* desc, const ss
         return SSM_ERR_UNSUPPORTED;
     for (const void* q : std::initializer_list<const void*>{x, W_x, W_dt, dt_low, B, C, delta_raw})
         if (!opt_aligned(q, 16)) return SSM_ERR_INVALID_ARG;
+    if (!opt_aligned(delta_bias, 4)) return SSM_ERR_INVALID_ARG;
     if (M == 0 || Dm == 0) return SSM_OK;
     if (!x || !W_x || !dt_low || !B || !C || (delta_raw && !W_dt)) return SSM_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -984,6 +985,8 @@ extern "C" ssm_status ssm_selection_proj_fwd(const ssm_scan_desc* desc, const ss
         p2.M = M; p2.N = (int)Dm; p2.K = (int)R;
         p2.seg[0] = {delta_raw, Dm, 0, (int)Dm};
         p2.nseg = 1;
+        p2.col_bias = delta_bias;
+        p2.act = desc->delta_softplus ? 1 : 0;
         if (launch_gemm_persistent<SSM_DTPROJ_BN, SSM_DTPROJ_STAGES>(dt_low, W_dt, M, (int)Dm, (int)R,
                                                                      p2, s) != cudaSuccess)
             return SSM_ERR_CUDA;

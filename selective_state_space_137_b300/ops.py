@@ -284,10 +284,13 @@ def lti_conv_fwd(K, x, D=None, z=None, out=None, stream=None):
     return out
 
 
-def selection_proj(x, W_x, W_dt, dt_rank, dstate, stream=None):
+def selection_proj(x, W_x, W_dt, dt_rank, dstate, delta_bias=None, delta_softplus=False,
+                   stream=None):
     """The selection projections: x (batch, seqlen, dim) bf16, W_x (R + 2N,
-    dim), W_dt (dim, R) bf16.  Returns ``(dt_low, B, C, delta_raw)``, bf16,
-    shapes (batch, seqlen, R | N | N | dim)."""
+    dim), W_dt (dim, R) bf16.  Returns ``(dt_low, B, C, delta)``, bf16, shapes
+    (batch, seqlen, R | N | N | dim), with delta = act(dt_low W_dt^T +
+    delta_bias), act = softplus when ``delta_softplus`` (then delta is the
+    step itself: scan it with delta_softplus=False and no bias)."""
     if not x.is_cuda:
         raise ValueError("selection_proj runs on a CUDA device only")
     bsz, seqlen, dim = x.shape
@@ -296,14 +299,15 @@ def selection_proj(x, W_x, W_dt, dt_rank, dstate, stream=None):
     _check(x, "x", (bsz, seqlen, dim), torch.bfloat16, dev)
     _check(W_x, "W_x", (R + 2 * N, dim), torch.bfloat16, dev)
     _check(W_dt, "W_dt", (dim, R), torch.bfloat16, dev)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, dev)
     kw = dict(dtype=torch.bfloat16, device=dev)
     dt_low = torch.empty((bsz, seqlen, R), **kw)
     Bm = torch.empty((bsz, seqlen, N), **kw)
     Cm = torch.empty((bsz, seqlen, N), **kw)
     delta = torch.empty((bsz, seqlen, dim), **kw)
-    desc = _b.make_desc(bsz, seqlen, dim, N, torch.bfloat16, True)
-    st = _b.ssm_selection_proj_fwd(desc, _b.ssm_proj_desc(R, 0), x, W_x, W_dt, dt_low, Bm, Cm, delta,
-                                   stream)
+    desc = _b.make_desc(bsz, seqlen, dim, N, torch.bfloat16, delta_softplus)
+    st = _b.ssm_selection_proj_fwd(desc, _b.ssm_proj_desc(R, 0), x, W_x, W_dt, delta_bias, dt_low,
+                                   Bm, Cm, delta, stream)
     if st != _b.SSM_OK:
         raise _b.SSMError(st, "ssm_selection_proj_fwd")
     return dt_low, Bm, Cm, delta

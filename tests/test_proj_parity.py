@@ -79,11 +79,34 @@ def test_proj_feeds_the_scan(cuda):
 def test_proj_rejections(cuda):
     d = binding.make_desc(1, 16, 60, 16, torch.bfloat16)      # dim not a multiple of 8
     x = torch.zeros(1, 16, 64, dtype=torch.bfloat16, device=cuda)
-    assert binding.ssm_selection_proj_fwd(d, binding.ssm_proj_desc(16, 0), x, x, x, x, x, x, None) \
-        == binding.SSM_ERR_UNSUPPORTED
+    assert binding.ssm_selection_proj_fwd(d, binding.ssm_proj_desc(16, 0), x, x, x, None, x, x, x,
+                                          None) == binding.SSM_ERR_UNSUPPORTED
     d = binding.make_desc(1, 16, 64, 128, torch.bfloat16)     # R + 2N > 256
-    assert binding.ssm_selection_proj_fwd(d, binding.ssm_proj_desc(16, 0), x, x, x, x, x, x, None) \
-        == binding.SSM_ERR_UNSUPPORTED
+    assert binding.ssm_selection_proj_fwd(d, binding.ssm_proj_desc(16, 0), x, x, x, None, x, x, x,
+                                          None) == binding.SSM_ERR_UNSUPPORTED
     d = binding.make_desc(1, 16, 64, 16, torch.float32)       # fp32 I/O
-    assert binding.ssm_selection_proj_fwd(d, binding.ssm_proj_desc(16, 0), x, x, x, x, x, x, None) \
-        == binding.SSM_ERR_UNSUPPORTED
+    assert binding.ssm_selection_proj_fwd(d, binding.ssm_proj_desc(16, 0), x, x, x, None, x, x, x,
+                                          None) == binding.SSM_ERR_UNSUPPORTED
+
+
+def test_proj_epilogue_finishes_delta(cuda):
+    """Bias and softplus in dt_proj's epilogue: delta is the step itself, and
+    the scan runs without softplus or bias; against the oracle's raw
+    projection followed by the oracle's scan with softplus and bias."""
+    bsz, L, dim, R, N = 2, 256, 256, 32, 16
+    p = synth.make_proj_inputs(bsz, L, dim, R, N, 21)
+    s = synth.make_scan_inputs(synth.ScanWorkload("proj-sp", bsz, L, dim, N, "bf16", 22))
+    dev = {k: v.to(cuda) for k, v in p.items()}
+    bias = s["delta_bias"].to(cuda)
+    _, Bm, Cm, dt = ops.selection_proj(dev["x"], dev["W_x"], dev["W_dt"], R, N, delta_bias=bias,
+                                       delta_softplus=True)
+    out, last = ops.scan_fwd(dev["x"], dt, s["A"].to(cuda), Bm, Cm, D=s["D"].to(cuda),
+                             z=s["z"].to(cuda), delta_softplus=False)
+    torch.cuda.synchronize()
+    _, rB, rC, rdelta = oracle.selection_proj(f64(p["x"]), f64(p["W_x"]), f64(p["W_dt"]), R)
+    sp = np.logaddexp(0.0, rdelta + f64(s["delta_bias"]))
+    assert rel_err(f64(dt), sp) <= TOL
+    ref, ref_last = oracle.scan_fwd(f64(p["x"]), rdelta, f64(s["A"]), rB, rC, D=f64(s["D"]),
+                                    z=f64(s["z"]), delta_bias=f64(s["delta_bias"]))
+    assert rel_err(f64(out), ref) <= 2e-2
+    assert rel_err(f64(last), ref_last) <= 2e-2
