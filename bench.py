@@ -240,20 +240,21 @@ def whole_job_rate(world, units_per_rank_step, steps, max_total_ms):
 
 
 # ----------------------------------------------------------------------------- oracle sample
-def oracle_sample_inputs(inp, w, nchan, b=0):
-    """fp64 copies of channels [0, nchan) of sequence b (all tokens)."""
+def oracle_sample_inputs(inp, w, nchan, nseq=1):
+    """fp64 copies of channels [0, nchan) of sequences [0, nseq) (all tokens)."""
     import oracle  # noqa: F401  (test/baseline infrastructure only)
     sl = slice(0, nchan)
     f64 = lambda t: None if t is None else t.detach().to("cpu", torch.float64).numpy()
-    return dict(x=f64(inp["x"][b:b + 1, :, sl]), delta=f64(inp["delta"][b:b + 1, :, sl]),
-                A=f64(inp["A"][sl]), B=f64(inp["B"][b:b + 1]), C=f64(inp["C"][b:b + 1]),
+    return dict(x=f64(inp["x"][:nseq, :, sl]), delta=f64(inp["delta"][:nseq, :, sl]),
+                A=f64(inp["A"][sl]), B=f64(inp["B"][:nseq]), C=f64(inp["C"][:nseq]),
                 D=f64(inp["D"][sl]) if inp["D"] is not None else None,
-                z=f64(inp["z"][b:b + 1, :, sl]) if inp["z"] is not None else None,
+                z=f64(inp["z"][:nseq, :, sl]) if inp["z"] is not None else None,
                 delta_bias=f64(inp["delta_bias"][sl]) if inp["delta_bias"] is not None else None)
 
 
 def calibrate_oracle(inp, w, target_s):
-    """Channel count whose oracle run takes about target_s seconds on all host cores."""
+    """(channels, sequences) whose oracle run takes about target_s seconds on
+    all host cores: channels of sequence 0 first, then whole sequences."""
     import oracle
     cores = os.cpu_count() or 1
     oracle.load()
@@ -262,22 +263,27 @@ def calibrate_oracle(inp, w, target_s):
     t = time.perf_counter()
     oracle.scan_fwd(**s, nthreads=cores)
     dt = max(time.perf_counter() - t, 1e-6)
-    nchan = int(min(w.dim, max(probe, probe * target_s / dt)))
+    per_chan = dt / probe
+    nchan = int(min(w.dim, max(probe, target_s / per_chan)))
     if nchan >= cores:
         nchan = (nchan // cores) * cores
-    return nchan, cores
+    nseq = 1
+    if nchan >= w.dim:
+        nchan = w.dim
+        nseq = int(min(w.batch, max(1, target_s / (per_chan * w.dim))))
+    return nchan, nseq, cores
 
 
 def time_oracle(inp, w, target_s):
     """Run the oracle on a sample sized for about target_s seconds; returns
-    (elements/s, seconds, channels, cores)."""
+    (elements/s, seconds, channels, sequences, cores)."""
     import oracle
-    nchan, cores = calibrate_oracle(inp, w, target_s)
-    s = oracle_sample_inputs(inp, w, nchan)
+    nchan, nseq, cores = calibrate_oracle(inp, w, target_s)
+    s = oracle_sample_inputs(inp, w, nchan, nseq)
     t = time.perf_counter()
     oracle.scan_fwd(**s, nthreads=cores)
     dt = time.perf_counter() - t
-    return w.seqlen * nchan / dt, dt, nchan, cores
+    return w.seqlen * nchan * nseq / dt, dt, nchan, nseq, cores
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -290,8 +296,8 @@ def run_reference(args, world, rank):
     w = workload_by_name(args.workload)
     gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = synth.make_scan_inputs(w, device=gen_dev)
-    nchan, cores = calibrate_oracle(inp, w, 2.0)
-    s = oracle_sample_inputs(inp, w, nchan)
+    nchan, nseq, cores = calibrate_oracle(inp, w, 2.0)
+    s = oracle_sample_inputs(inp, w, nchan, nseq)
     del inp
     for _ in range(args.warmup):
         oracle.scan_fwd(**s, nthreads=cores)
@@ -299,8 +305,9 @@ def run_reference(args, world, rank):
     for _ in range(args.steps):
         oracle.scan_fwd(**s, nthreads=cores)
     el = time.perf_counter() - t
-    value = w.seqlen * nchan * args.steps / el
-    sample = f"sequence 0, channels 0..{nchan - 1} of {w.dim}, all {w.seqlen} tokens, per step"
+    value = w.seqlen * nchan * nseq * args.steps / el
+    sample = (f"sequences 0..{nseq - 1} of {w.batch}, channels 0..{nchan - 1} of {w.dim}, "
+              f"all {w.seqlen} tokens, per step")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -438,10 +445,11 @@ def run_ours(args, world, rank, local):
         line["zoh"] = run_zoh(args, w, inp, dev)
         line["lti"] = run_lti(args, dev)
     if rank == 0 and world == 1 and not args.no_cpu:
-        val, dt, nchan, cores = time_oracle(inp, w, args.cpu_seconds)
+        val, dt, nchan, nseq, cores = time_oracle(inp, w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"sequence 0, channels 0..{nchan - 1} of {w.dim}, "
-                                          f"all {w.seqlen} tokens ({dt:.1f} s wall)"}
+                                "sample": f"sequences 0..{nseq - 1} of {w.batch}, channels "
+                                          f"0..{nchan - 1} of {w.dim}, all {w.seqlen} tokens "
+                                          f"({dt:.1f} s wall)"}
     elif rank == 0:
         line["cpu_baseline"] = None
     line["source_hash"] = kernel_source_hash()
