@@ -116,6 +116,8 @@ _KERNEL_SOURCES = {
     "state_update": ("common.cuh", "scan_tiled.cuh", "decode.cuh", "ssm_api.cu"),
     "conv1d_fwd": ("common.cuh", "scan_generic.cuh", "scan_tiled.cuh", "conv.cuh", "ssm_api.cu"),
     "scan_bwd": ("common.cuh", "tma.cuh", "scan_tiled.cuh", "scan_bwd.cuh", "ssm_api.cu"),
+    "x_proj": ("common.cuh", "tma.cuh", "scan_tiled.cuh", "gemm.cuh", "ssm_api.cu"),
+    "dt_proj": ("common.cuh", "tma.cuh", "scan_tiled.cuh", "gemm.cuh", "ssm_api.cu"),
 }
 
 
@@ -640,9 +642,11 @@ def run_proj(args, w, dev, scan_inp=None):
         tfs = fl / (ms * 1e-3) / 1e12
         return {"ms": ms, "gb_per_s": gbs, "hbm_frac": gbs / hbm, "tflops": tfs,
                 "tensor_frac": tfs / tc, "algorithmic_bytes": by, "flops": fl}
+    xr, dr = roof(x_ms, x_bytes, x_flops), roof(dt_ms, d_bytes, d_flops)
+    xr["traffic"] = profiled_traffic("x_proj_" + w.name)
+    dr["traffic"] = profiled_traffic("dt_proj_" + w.name)
     res = {"workload": f"{w.name} x_proj ({M}x{w.dim} . {w.dim}x{NO}), dt_proj ({M}x{R} . {R}x{w.dim})",
-           "dt_rank": R, "x_proj": roof(x_ms, x_bytes, x_flops),
-           "dt_proj": roof(dt_ms, d_bytes, d_flops), "both_ms": all_ms,
+           "dt_rank": R, "x_proj": xr, "dt_proj": dr, "both_ms": all_ms,
            "peaks": {"hbm_gbs": hbm, "hbm_kind": hbm_kind, "bf16_tflops": tc, "tensor_kind": tc_kind}}
     if scan_inp is not None:
         # projections + scan, the step finished in dt_proj's epilogue (bias,
