@@ -280,6 +280,28 @@ SSM_API ssm_status ssm_conv_state_update(const ssm_scan_desc *desc, const ssm_co
                                          const void *C, const float *D, const void *z,
                                          const float *delta_bias, void *out, void *stream);
 
+/* The scan over tensors that live in host memory: the batch is cut into
+ * slices of `slice_batch` sequences, and each slice's inputs are copied in,
+ * scanned and its outputs copied back in a three-stage pipeline (copies in,
+ * the scan, copies out on their own streams, double-buffered), so the
+ * host-device transfers overlap one another and the kernels.  Sequences are
+ * independent, so the result equals one ssm_scan_fwd over the whole batch.
+ *   host (pinned for overlap; pageable memory works but serialises):
+ *     x, delta, z, out (batch, seqlen, dim) io; B, C (batch, seqlen, dstate) io;
+ *     initial_state, last_state (batch, dim, dstate) fp32 (NULL: zeros / not returned)
+ *   device: A (dim, dstate), D, delta_bias (dim) fp32
+ *   workspace: device memory of ssm_scan_fwd_host_workspace_size(desc,
+ *     slice_batch) bytes, 256-byte aligned.
+ * Asynchronous on `stream`: when the stream reaches this call's end, every
+ * output has landed in host memory.  slice_batch <= 0 picks one. */
+SSM_API size_t ssm_scan_fwd_host_workspace_size(const ssm_scan_desc *desc, int64_t slice_batch);
+SSM_API ssm_status ssm_scan_fwd_host(const ssm_scan_desc *desc, int64_t slice_batch,
+                                     const void *x, const void *delta, const float *A,
+                                     const void *B, const void *C, const float *D, const void *z,
+                                     const float *delta_bias, void *out, float *last_state,
+                                     const float *initial_state, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
 /* Capacity of the fixed scratch buffer used by ssm_scan_fwd_noalloc. */
 #define SSM_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -17,7 +17,7 @@ from __future__ import annotations
 import importlib
 
 _OPS = ("scan_fwd", "scan_bwd", "state_update", "conv1d_fwd", "conv_scan_fwd",
-        "conv_state_update", "lti_kernel", "lti_conv_fwd", "selection_proj")
+        "conv_state_update", "lti_kernel", "lti_conv_fwd", "selection_proj", "scan_fwd_host")
 __all__ = list(_OPS) + ["binding", "synth", "ops"]
 
 

@@ -23,7 +23,8 @@ EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
             "ssm_get_device_status", "ssm_selftest_wait_timeout", "ssm_conv1d_fwd",
             "ssm_conv_scan_fwd", "ssm_conv_state_update", "ssm_scan_bwd_workspace_size",
             "ssm_scan_bwd", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_lti_kernel",
-            "ssm_lti_conv_fwd", "ssm_selection_proj_fwd")
+            "ssm_lti_conv_fwd", "ssm_selection_proj_fwd", "ssm_scan_fwd_host_workspace_size",
+            "ssm_scan_fwd_host")
 SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -84,6 +85,11 @@ def _load():
     lib.ssm_selection_proj_fwd.restype = ctypes.c_int
     lib.ssm_selection_proj_fwd.argtypes = [dp, ctypes.POINTER(ssm_proj_desc), vp, vp, vp, fp, vp, vp,
                                            vp, vp, vp]
+    lib.ssm_scan_fwd_host_workspace_size.restype = sz
+    lib.ssm_scan_fwd_host_workspace_size.argtypes = [dp, ctypes.c_int64]
+    lib.ssm_scan_fwd_host.restype = ctypes.c_int
+    lib.ssm_scan_fwd_host.argtypes = [dp, ctypes.c_int64, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp,
+                                      vp, sz, vp]
     lib.ssm_scan_bwd_workspace_size.restype = sz
     lib.ssm_scan_bwd_workspace_size.argtypes = [dp]
     lib.ssm_scan_bwd.restype = ctypes.c_int
@@ -287,3 +293,18 @@ def ssm_selection_proj_fwd(desc, proj, x, W_x, W_dt, delta_bias, dt_low, B, C, d
     return lib.ssm_selection_proj_fwd(ctypes.byref(desc), ctypes.byref(proj), _ptr(x), _ptr(W_x),
                                       _ptr(W_dt), _ptr(delta_bias), _ptr(dt_low), _ptr(B), _ptr(C),
                                       _ptr(delta), _stream(stream))
+
+
+def ssm_scan_fwd_host_workspace_size(desc, slice_batch=0) -> int:
+    return int(lib.ssm_scan_fwd_host_workspace_size(ctypes.byref(desc), int(slice_batch)))
+
+
+def ssm_scan_fwd_host(desc, slice_batch, x, delta, A, B, C, D, z, delta_bias, out, last_state,
+                      initial_state, workspace, workspace_bytes, stream=None) -> int:
+    """The scan over host tensors (x, delta, z, B, C, out, states: host
+    memory, pinned for overlap; A, D, delta_bias: device), pipelined over
+    batch slices through a device workspace."""
+    return lib.ssm_scan_fwd_host(ctypes.byref(desc), int(slice_batch), _ptr(x), _ptr(delta), _ptr(A),
+                                 _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out),
+                                 _ptr(last_state), _ptr(initial_state), _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream))

@@ -1298,6 +1298,192 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
+// The scan over host-resident tensors, pipelined over batch slices.
+namespace {
+
+constexpr int kHostBufs = 2;   // slices in flight per stage
+constexpr int kMaxDevices = 256;
+
+struct HostLayout {
+    int64_t bs = 0;                   // sequences per slice
+    size_t tok = 0, bc = 0, st = 0;   // bytes per slice: (bs, L, D) io, (bs, L, N) io, (bs, D, N) fp32
+    size_t scan_ws = 0;               // ssm_scan_fwd workspace of one slice
+    size_t per_buf = 0, total = 0;
+    // offsets inside one buffer
+    size_t o_x = 0, o_dl = 0, o_z = 0, o_b = 0, o_c = 0, o_out = 0, o_h0 = 0, o_h1 = 0, o_ws = 0;
+};
+
+int64_t host_slice(const ssm_scan_desc* d, int64_t slice_batch) {
+    if (slice_batch > 0) return slice_batch < d->batch ? slice_batch : d->batch;
+    // about 64 MB of token data per slice, and at least 2 slices when there are 2 sequences
+    const int64_t per_seq = d->seqlen * d->dim * (int64_t)io_size(d);
+    int64_t bs = per_seq > 0 ? (int64_t)(64u << 20) / per_seq : d->batch;
+    if (bs < 1) bs = 1;
+    if (d->batch >= 2 && bs > d->batch / 2) bs = d->batch / 2;
+    return bs < 1 ? 1 : bs;
+}
+
+HostLayout host_layout(const ssm_scan_desc* d, int64_t slice_batch) {
+    HostLayout h;
+    h.bs = host_slice(d, slice_batch);
+    const size_t e = io_size(d);
+    h.tok = (size_t)h.bs * (size_t)d->seqlen * (size_t)d->dim * e;
+    h.bc = (size_t)h.bs * (size_t)d->seqlen * (size_t)d->dstate * e;
+    h.st = (size_t)h.bs * (size_t)d->dim * (size_t)d->dstate * sizeof(float);
+    ssm_scan_desc sd = *d;
+    sd.batch = h.bs;
+    h.scan_ws = ssm_scan_workspace_size(&sd);
+    size_t o = 0;
+    h.o_x = o;   o = align256(o + h.tok);
+    h.o_dl = o;  o = align256(o + h.tok);
+    h.o_z = o;   o = align256(o + h.tok);
+    h.o_b = o;   o = align256(o + h.bc);
+    h.o_c = o;   o = align256(o + h.bc);
+    h.o_out = o; o = align256(o + h.tok);
+    h.o_h0 = o;  o = align256(o + h.st);
+    h.o_h1 = o;  o = align256(o + h.st);
+    h.o_ws = o;  o = align256(o + h.scan_ws);
+    h.per_buf = o;
+    h.total = o * kHostBufs;
+    return h;
+}
+
+// Two copy streams of this device, made once and kept.
+struct CopyStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+};
+std::mutex g_copy_mutex;
+CopyStreams g_copy_streams[kMaxDevices];
+
+cudaError_t copy_streams(CopyStreams* cs) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_copy_mutex);
+    CopyStreams& c = g_copy_streams[dev];
+    if (!c.in) {
+        e = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return e;
+    }
+    *cs = c;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" size_t ssm_scan_fwd_host_workspace_size(const ssm_scan_desc* desc, int64_t slice_batch) {
+    if (check_desc(desc) != SSM_OK || desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) return 0;
+    return host_layout(desc, slice_batch).total;
+}
+
+extern "C" ssm_status ssm_scan_fwd_host(const ssm_scan_desc* desc, int64_t slice_batch, const void* x,
+                                        const void* delta, const float* A, const void* B,
+                                        const void* C, const float* D, const void* z,
+                                        const float* delta_bias, void* out, float* last_state,
+                                        const float* initial_state, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+    const ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    if (desc->batch == 0 || desc->dim == 0) return SSM_OK;
+    if (desc->seqlen == 0) {
+        if (last_state) {
+            const size_t sb = (size_t)desc->batch * (size_t)desc->dim * (size_t)desc->dstate * 4;
+            if (initial_state) memcpy(last_state, initial_state, sb);
+            else memset(last_state, 0, sb);
+        }
+        return SSM_OK;
+    }
+    if (!x || !delta || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
+    const HostLayout h = host_layout(desc, slice_batch);
+    if (!workspace || workspace_bytes < h.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return SSM_ERR_INVALID_ARG;
+    CopyStreams cs;
+    if (copy_streams(&cs) != cudaSuccess) return SSM_ERR_CUDA;
+    cudaStream_t comp = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    const size_t e = io_size(desc);
+    const int64_t nsl = (desc->batch + h.bs - 1) / h.bs;
+
+    // events: start; per buffer "inputs in", "scanned", "outputs out"
+    cudaEvent_t ev_start, ev_in[kHostBufs], ev_done[kHostBufs], ev_out[kHostBufs];
+    bool made = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < kHostBufs && made; ++i)
+        made = cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+               cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming) == cudaSuccess &&
+               cudaEventCreateWithFlags(&ev_out[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!made) return SSM_ERR_CUDA;
+
+    cudaError_t err = cudaEventRecord(ev_start, comp);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(cs.in, ev_start, 0);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(cs.out, ev_start, 0);
+    ssm_status res = SSM_OK;
+    for (int64_t i = 0; i < nsl && err == cudaSuccess && res == SSM_OK; ++i) {
+        const int bi = (int)(i % kHostBufs);
+        char* buf = ws + (size_t)bi * h.per_buf;
+        const int64_t b0 = i * h.bs;
+        const int64_t nb = desc->batch - b0 < h.bs ? desc->batch - b0 : h.bs;
+        const size_t tok = (size_t)nb * (size_t)desc->seqlen * (size_t)desc->dim * e;
+        const size_t tok_off = (size_t)b0 * (size_t)desc->seqlen * (size_t)desc->dim * e;
+        const size_t bc = (size_t)nb * (size_t)desc->seqlen * (size_t)desc->dstate * e;
+        const size_t bc_off = (size_t)b0 * (size_t)desc->seqlen * (size_t)desc->dstate * e;
+        const size_t sb = (size_t)nb * (size_t)desc->dim * (size_t)desc->dstate * 4;
+        const size_t sb_off = (size_t)b0 * (size_t)desc->dim * (size_t)desc->dstate * 4;
+        // copies in: the buffer's previous slice must have been scanned and copied out
+        if (i >= kHostBufs) err = cudaStreamWaitEvent(cs.in, ev_out[bi], 0);
+        auto h2d = [&](size_t off, const void* src, size_t n) {
+            if (err == cudaSuccess && src && n)
+                err = cudaMemcpyAsync(buf + off, static_cast<const char*>(src), n,
+                                      cudaMemcpyHostToDevice, cs.in);
+        };
+        h2d(h.o_x, static_cast<const char*>(x) + tok_off, tok);
+        h2d(h.o_dl, static_cast<const char*>(delta) + tok_off, tok);
+        if (z) h2d(h.o_z, static_cast<const char*>(z) + tok_off, tok);
+        h2d(h.o_b, static_cast<const char*>(B) + bc_off, bc);
+        h2d(h.o_c, static_cast<const char*>(C) + bc_off, bc);
+        if (initial_state) h2d(h.o_h0, reinterpret_cast<const char*>(initial_state) + sb_off, sb);
+        if (err == cudaSuccess) err = cudaEventRecord(ev_in[bi], cs.in);
+        // the scan of the slice on the caller's stream
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(comp, ev_in[bi], 0);
+        if (err != cudaSuccess) break;
+        ssm_scan_desc sd = *desc;
+        sd.batch = nb;
+        res = ssm_scan_fwd(&sd, buf + h.o_x, buf + h.o_dl, A, buf + h.o_b, buf + h.o_c, D,
+                           z ? buf + h.o_z : nullptr, delta_bias, buf + h.o_out,
+                           last_state ? reinterpret_cast<float*>(buf + h.o_h1) : nullptr,
+                           initial_state ? reinterpret_cast<const float*>(buf + h.o_h0) : nullptr,
+                           h.scan_ws ? buf + h.o_ws : nullptr, h.scan_ws, comp);
+        if (res != SSM_OK) break;
+        err = cudaEventRecord(ev_done[bi], comp);
+        // copies out
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(cs.out, ev_done[bi], 0);
+        if (err == cudaSuccess)
+            err = cudaMemcpyAsync(static_cast<char*>(out) + tok_off, buf + h.o_out, tok,
+                                  cudaMemcpyDeviceToHost, cs.out);
+        if (err == cudaSuccess && last_state)
+            err = cudaMemcpyAsync(reinterpret_cast<char*>(last_state) + sb_off, buf + h.o_h1, sb,
+                                  cudaMemcpyDeviceToHost, cs.out);
+        if (err == cudaSuccess) err = cudaEventRecord(ev_out[bi], cs.out);
+    }
+    // the caller's stream reaches the end of this call once everything has landed
+    if (err == cudaSuccess && res == SSM_OK) {
+        const int last = (int)((nsl - 1) % kHostBufs);
+        err = cudaStreamWaitEvent(comp, ev_out[last], 0);
+        if (err == cudaSuccess && nsl > 1)
+            err = cudaStreamWaitEvent(comp, ev_out[(last + 1) % kHostBufs], 0);
+    }
+    cudaEventDestroy(ev_start);
+    for (int i = 0; i < kHostBufs; ++i) {
+        cudaEventDestroy(ev_in[i]);
+        cudaEventDestroy(ev_done[i]);
+        cudaEventDestroy(ev_out[i]);
+    }
+    if (res != SSM_OK) return res;
+    return err == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
 // ssm_scan_fwd_noalloc: the scan for callers that cannot allocate device
 // memory.  Its chunk-carry scratch is this file-scope device array instead of
 // a caller workspace; see include/ssm.h for the contract.

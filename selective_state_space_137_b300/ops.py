@@ -311,3 +311,44 @@ def selection_proj(x, W_x, W_dt, dt_rank, dstate, delta_bias=None, delta_softplu
     if st != _b.SSM_OK:
         raise _b.SSMError(st, "ssm_selection_proj_fwd")
     return dt_low, Bm, Cm, delta
+
+
+def scan_fwd_host(x, delta, A, B, C, D=None, z=None, delta_bias=None, initial_state=None,
+                  delta_softplus=True, slice_batch=0, out=None, last_state=None, workspace=None,
+                  stream=None):
+    """The scan of host-resident tensors (x, delta, z, B, C, initial_state on
+    the CPU, ideally pinned) with A, D, delta_bias on the GPU: batch slices are
+    copied in, scanned and copied back in an overlapped pipeline.  Returns
+    ``(out, last_state)`` as CPU tensors (pinned) once the stream reaches the
+    end of the call; synchronise the stream before reading them."""
+    if x.is_cuda or not A.is_cuda:
+        raise ValueError("scan_fwd_host takes host x/delta/z/B/C and device A/D/delta_bias")
+    bsz, seqlen, dim = x.shape
+    dstate = A.shape[1]
+    cpu, dev, io = x.device, A.device, x.dtype
+    for t, name, shp in ((delta, "delta", x.shape), (z, "z", x.shape),
+                         (B, "B", (bsz, seqlen, dstate)), (C, "C", (bsz, seqlen, dstate))):
+        _check(t, name, shp, io, cpu)
+    _check(initial_state, "initial_state", (bsz, dim, dstate), torch.float32, cpu)
+    _check(A, "A", (dim, dstate), torch.float32, dev)
+    _check(D, "D", (dim,), torch.float32, dev)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    if out is None:
+        out = torch.empty(x.shape, dtype=io, pin_memory=True)
+    if last_state is None:
+        last_state = torch.empty((bsz, dim, dstate), dtype=torch.float32, pin_memory=True)
+    desc = _b.make_desc(bsz, seqlen, dim, dstate, io, delta_softplus)
+    need = _b.ssm_scan_fwd_host_workspace_size(desc, slice_batch)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need + 256, dtype=torch.uint8, device=dev)
+    ws = workspace
+    if ws is not None and ws.data_ptr() % 256:
+        off = 256 - ws.data_ptr() % 256
+        ws = ws[off:]
+    wbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = _b.ssm_scan_fwd_host(desc, slice_batch, x, delta, A, B, C, D, z, delta_bias, out,
+                              last_state, initial_state, ws if need else None,
+                              wbytes if need else 0, stream)
+    if st != _b.SSM_OK:
+        raise _b.SSMError(st, "ssm_scan_fwd_host")
+    return out, last_state
