@@ -812,6 +812,31 @@ def run_bwd(args, w, inp, dev, peak, peak_kind):
         ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     ms = float(np.mean([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]))
+    # the training pair: the forward keeps the state every 16 tokens, the
+    # backward reads it instead of recomputing it
+    ck = torch.empty(binding.ssm_scan_checkpoint_size(desc) // 4, dtype=torch.float32, device=dev)
+    fout = torch.empty_like(inp["x"])
+    flast = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device=dev)
+    fws = torch.empty(max(binding.ssm_scan_workspace_size(desc), 16), dtype=torch.uint8, device=dev)
+    need_ck = binding.ssm_scan_bwd_ex_workspace_size(desc, True)
+    ws_ck = torch.empty(max(need_ck, 16), dtype=torch.uint8, device=dev)
+
+    def fwd_train():
+        st = binding.ssm_scan_fwd_train(desc, inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                        inp["D"], inp["z"], inp["delta_bias"], fout, flast, None, ck,
+                                        fws, fws.numel(), stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_scan_fwd_train")
+
+    def bwd_ck():
+        st = binding.ssm_scan_bwd_ex(desc, inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"],
+                                     inp["D"], inp["z"], inp["delta_bias"], None, dout, None, ck, dx,
+                                     ddelta, dA, dB, dC, dD, dz, dbias, None, ws_ck, ws_ck.numel(),
+                                     stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_scan_bwd_ex")
+    fwd_train_ms = _time_calls(fwd_train, dev, steps)
+    bwd_ck_ms = _time_calls(bwd_ck, dev, steps)
     e = inp["x"].element_size()
     # read x, delta, z, dout, B, C; write dx, ddelta, dz (io) and dB, dC (fp32)
     algo = (4 + 3) * w.tokens * e + 2 * w.batch * w.seqlen * w.dstate * (e + 4)
@@ -819,7 +844,11 @@ def run_bwd(args, w, inp, dev, peak, peak_kind):
             "items_per_s": w.items / (ms * 1e-3), "workspace_bytes": need,
             "algorithmic_bytes_per_call": algo, "gb_per_s": algo / (ms * 1e-3) / 1e9,
             "hbm_frac": algo / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
-            "ms_vs_forward_note": "forward of the same workload: roofline.kernel_ms"}
+            "ms_vs_forward_note": "forward of the same workload: roofline.kernel_ms",
+            "training_pair": {"fwd_with_checkpoints_ms": fwd_train_ms,
+                              "bwd_from_checkpoints_ms": bwd_ck_ms,
+                              "workspace_bytes": need_ck,
+                              "checkpoint_bytes": ck.numel() * 4}}
 
 
 def run_decode(args, dev, peak, peak_kind):

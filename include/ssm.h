@@ -153,6 +153,33 @@ SSM_API ssm_status ssm_state_update_ex(const ssm_scan_desc *desc, const ssm_scan
                                        const float *D, const void *z, const float *delta_bias,
                                        void *out, void *stream);
 
+/* Training pair: the forward also keeps the state before every 16th token,
+ * and the backward reads those checkpoints instead of recomputing them.
+ *   checkpoints: (batch, ceil(seqlen / 16), dim, dstate) fp32, 16-byte aligned,
+ *                ssm_scan_checkpoint_size(desc) bytes; entry j is the state
+ *                before token 16 j (entry 0 = initial_state).
+ * ssm_scan_fwd_train: ssm_scan_fwd plus the checkpoints (dstate 16 in the
+ *   warp-specialised kernel, other sizes in the general one).
+ * ssm_scan_bwd_ex: ssm_scan_bwd with checkpoints (NULL: recompute, exactly
+ *   ssm_scan_bwd); the inputs must be those of the forward that wrote them.
+ *   Workspace: ssm_scan_bwd_ex_workspace_size(desc, with_checkpoints). */
+SSM_API size_t ssm_scan_checkpoint_size(const ssm_scan_desc *desc);
+SSM_API ssm_status ssm_scan_fwd_train(const ssm_scan_desc *desc, const void *x, const void *delta,
+                                      const float *A, const void *B, const void *C,
+                                      const float *D, const void *z, const float *delta_bias,
+                                      void *out, float *last_state, const float *initial_state,
+                                      float *checkpoints, void *workspace, size_t workspace_bytes,
+                                      void *stream);
+SSM_API size_t ssm_scan_bwd_ex_workspace_size(const ssm_scan_desc *desc, int with_checkpoints);
+SSM_API ssm_status ssm_scan_bwd_ex(const ssm_scan_desc *desc, const void *x, const void *delta,
+                                   const float *A, const void *B, const void *C, const float *D,
+                                   const void *z, const float *delta_bias,
+                                   const float *initial_state, const void *dout,
+                                   const float *dlast_state, const float *checkpoints, void *dx,
+                                   void *ddelta, float *dA, float *dB, float *dC, float *dD,
+                                   void *dz, float *ddelta_bias, float *dinitial_state,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
 /* The time-invariant (LTI, S4) model in its convolution mode ("Mamba的三大创新",
  * stage 3).  With a constant per-channel step delta[d] (> 0, used as given:
  * no bias, no softplus) and input-independent per-channel B, C, the

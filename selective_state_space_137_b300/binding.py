@@ -24,7 +24,8 @@ EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
             "ssm_conv_scan_fwd", "ssm_conv_state_update", "ssm_scan_bwd_workspace_size",
             "ssm_scan_bwd", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_lti_kernel",
             "ssm_lti_conv_fwd", "ssm_selection_proj_fwd", "ssm_scan_fwd_host_workspace_size",
-            "ssm_scan_fwd_host")
+            "ssm_scan_fwd_host", "ssm_scan_checkpoint_size", "ssm_scan_fwd_train",
+            "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex")
 SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -90,6 +91,15 @@ def _load():
     lib.ssm_scan_fwd_host.restype = ctypes.c_int
     lib.ssm_scan_fwd_host.argtypes = [dp, ctypes.c_int64, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp,
                                       vp, sz, vp]
+    lib.ssm_scan_checkpoint_size.restype = sz
+    lib.ssm_scan_checkpoint_size.argtypes = [dp]
+    lib.ssm_scan_fwd_train.restype = ctypes.c_int
+    lib.ssm_scan_fwd_train.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, vp, fp, fp, fp, vp, sz, vp]
+    lib.ssm_scan_bwd_ex_workspace_size.restype = sz
+    lib.ssm_scan_bwd_ex_workspace_size.argtypes = [dp, ctypes.c_int]
+    lib.ssm_scan_bwd_ex.restype = ctypes.c_int
+    lib.ssm_scan_bwd_ex.argtypes = [dp, vp, vp, fp, vp, vp, fp, vp, fp, fp, vp, fp, fp, vp, vp, fp, fp,
+                                    fp, fp, vp, fp, fp, vp, sz, vp]
     lib.ssm_scan_bwd_workspace_size.restype = sz
     lib.ssm_scan_bwd_workspace_size.argtypes = [dp]
     lib.ssm_scan_bwd.restype = ctypes.c_int
@@ -308,3 +318,32 @@ def ssm_scan_fwd_host(desc, slice_batch, x, delta, A, B, C, D, z, delta_bias, ou
                                  _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out),
                                  _ptr(last_state), _ptr(initial_state), _ptr(workspace),
                                  int(workspace_bytes), _stream(stream))
+
+
+def ssm_scan_checkpoint_size(desc) -> int:
+    return int(lib.ssm_scan_checkpoint_size(ctypes.byref(desc)))
+
+
+def ssm_scan_fwd_train(desc, x, delta, A, B, C, D, z, delta_bias, out, last_state, initial_state,
+                       checkpoints, workspace, workspace_bytes, stream=None) -> int:
+    """ssm_scan_fwd that also keeps the state before every 16th token."""
+    return lib.ssm_scan_fwd_train(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(B),
+                                  _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out),
+                                  _ptr(last_state), _ptr(initial_state), _ptr(checkpoints),
+                                  _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def ssm_scan_bwd_ex_workspace_size(desc, with_checkpoints) -> int:
+    return int(lib.ssm_scan_bwd_ex_workspace_size(ctypes.byref(desc), int(bool(with_checkpoints))))
+
+
+def ssm_scan_bwd_ex(desc, x, delta, A, B, C, D, z, delta_bias, initial_state, dout, dlast_state,
+                    checkpoints, dx, ddelta, dA, dB, dC, dD, dz, ddelta_bias, dinitial_state,
+                    workspace, workspace_bytes, stream=None) -> int:
+    """ssm_scan_bwd reading the forward's checkpoints (NULL: recompute)."""
+    return lib.ssm_scan_bwd_ex(ctypes.byref(desc), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                               _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(initial_state), _ptr(dout),
+                               _ptr(dlast_state), _ptr(checkpoints), _ptr(dx), _ptr(ddelta),
+                               _ptr(dA), _ptr(dB), _ptr(dC), _ptr(dD), _ptr(dz),
+                               _ptr(ddelta_bias), _ptr(dinitial_state), _ptr(workspace),
+                               int(workspace_bytes), _stream(stream))

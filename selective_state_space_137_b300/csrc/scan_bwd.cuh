@@ -59,6 +59,7 @@ struct BwdParams {
     float* ebuf;           // (batch, K, dim, N): E_k, then the incoming term e_k
     float* bdsum;          // (batch, K, dim): sum of Delta over chunk k
     float* ckpt;           // (batch, ntiles, dim, N): state at each tile start
+    int ckpt_given;        // 1: ckpt was written by the training forward (no forward sweep)
     float* pBC;            // (nblk, batch, seqlen, 2N): per-CTA dB | dC
     float* pA;             // (batch * K, dim, N)
     float* pD;             // (batch * K, dim)
@@ -266,7 +267,8 @@ __global__ void __launch_bounds__(256, 2) scan_bwd_kernel(BwdParams p) {
         dAacc[j] = 0.f;
         const int64_t si = (b * p.dim + d) * N + n0 + j;
         const int64_t ci = ((b * p.nchunk + k) * p.dim + d) * N + n0 + j;
-        h[j] = p.nchunk > 1 ? p.fstart[ci] : (p.initial_state ? __ldg(p.initial_state + si) : 0.f);
+        h[j] = p.ckpt_given ? 0.f   // the tile states come from the checkpoints
+             : p.nchunk > 1 ? p.fstart[ci] : (p.initial_state ? __ldg(p.initial_state + si) : 0.f);
         G[j] = p.nchunk > 1 ? p.ebuf[ci] : (p.dlast ? __ldg(p.dlast + si) : 0.f);
     }
     const float bias = p.delta_bias ? __ldg(p.delta_bias + d) : 0.f;
@@ -279,8 +281,8 @@ __global__ void __launch_bounds__(256, 2) scan_bwd_kernel(BwdParams p) {
         return p.softplus ? softplus_tiled<IO>(u) : u;
     };
 
-    // ---- forward sweep: the state at every tile start
-    for (int j = 0; j < ntile; ++j) {
+    // ---- forward sweep: the state at every tile start (unless the forward kept them)
+    for (int j = 0; j < ntile && !p.ckpt_given; ++j) {
         const int64_t ts = t0 + (int64_t)j * T;
         if (valid) {
             float* ck = ckpt_at(j);
@@ -438,9 +440,10 @@ __global__ void __launch_bounds__(256, 2) scan_bwd_kernel(BwdParams p) {
 // when the rows are 16-byte multiples and the tensors 16-byte aligned; the
 // arithmetic is that of scan_bwd_kernel.
 //
-// Load sequence u = 0 .. 2 ntile - 1: u < ntile is forward-sweep tile u
-// (x, delta, B); u >= ntile is reverse tile 2 ntile - 1 - u (x, delta, dout,
-// z, B, C).  Stage u % 2, parity (u / 2) & 1.
+// Load sequence u = 0 .. nfwd + ntile - 1: u < nfwd is forward-sweep tile u
+// (x, delta, B); u >= nfwd is reverse tile nfwd + ntile - 1 - u (x, delta,
+// dout, z, B, C); nfwd = 0 when the training forward kept the checkpoints.
+// Stage u % 2, parity (u / 2) & 1.
 struct BwdMaps {
     CUtensorMap x, delta, dout, z, B, C, dx, ddelta, dz;
 };
@@ -496,7 +499,8 @@ __global__ void __launch_bounds__(256, 2)
     if (t1 > p.seqlen) t1 = p.seqlen;
     const int n0 = sub * SPL;
     const int ntile = (int)((t1 - t0 + T - 1) / T);
-    const int nload = 2 * ntile;
+    const int nfwd = p.ckpt_given ? 0 : ntile;   // forward-sweep loads
+    const int nload = nfwd + ntile;
     const bool z_on = p.z != nullptr;
     const bool dz_on = p.dz != nullptr;
 
@@ -504,8 +508,8 @@ __global__ void __launch_bounds__(256, 2)
     auto issue = [&](int u) {   // one thread
         issued = u + 1;
         unsigned char* st = smem + (u % NST) * Cfg::STAGE;
-        const bool fwd = u < ntile;
-        const int j = fwd ? u : 2 * ntile - 1 - u;
+        const bool fwd = u < nfwd;
+        const int j = fwd ? u : nfwd + ntile - 1 - u;
         const int r = (int)(t0 + (int64_t)j * T);
         uint64_t* bar = &full[u % NST];
         const uint32_t tx = fwd ? (uint32_t)(2 * Cfg::TOK + Cfg::ROW)
@@ -542,7 +546,8 @@ __global__ void __launch_bounds__(256, 2)
         dAacc[j] = 0.f;
         const int64_t si = ((int64_t)b * p.dim + d) * N + n0 + j;
         const int64_t ci = (((int64_t)b * p.nchunk + k) * p.dim + d) * N + n0 + j;
-        h[j] = p.nchunk > 1 ? p.fstart[ci] : (p.initial_state ? __ldg(p.initial_state + si) : 0.f);
+        h[j] = p.ckpt_given ? 0.f   // the tile states come from the checkpoints
+             : p.nchunk > 1 ? p.fstart[ci] : (p.initial_state ? __ldg(p.initial_state + si) : 0.f);
         G[j] = p.nchunk > 1 ? p.ebuf[ci] : (p.dlast ? __ldg(p.dlast + si) : 0.f);
     }
     const float bias = p.delta_bias ? __ldg(p.delta_bias + d) : 0.f;
@@ -560,8 +565,8 @@ __global__ void __launch_bounds__(256, 2)
         if (threadIdx.x == 0 && u + NST < nload) issue(u + NST);
     };
 
-    // ---- forward sweep: the state at every tile start
-    for (int j = 0; j < ntile; ++j) {
+    // ---- forward sweep: the state at every tile start (unless the forward kept them)
+    for (int j = 0; j < nfwd; ++j) {
         const int u = j;
         wait_stage(u);
         if (valid) {
@@ -611,7 +616,7 @@ __global__ void __launch_bounds__(256, 2)
     }
     for (int jj = 0; jj < ntile && !aborted(); ++jj) {
         const int j = ntile - 1 - jj;
-        const int u = ntile + jj;
+        const int u = nfwd + jj;
         const int64_t ts = t0 + (int64_t)j * T;
         const int steps = (int)((t1 - ts) < T ? (t1 - ts) : T);
         float hs[SPL];

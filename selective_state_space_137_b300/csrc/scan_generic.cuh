@@ -38,7 +38,12 @@ struct ScanParams {
     float* conv_state_out = nullptr;        // (batch, dim, conv_width - 1) or NULL
     int conv_width = 1;
     int conv_act = 0;
+    // training forward: the state before every 16th token, (batch, ceil(L/16), dim, N)
+    float* ckpt = nullptr;
+    int64_t ckpt_tiles = 0;
 };
+
+constexpr int kCkptSteps = 16;
 
 constexpr int kMaxConvWidth = 8;
 
@@ -106,6 +111,11 @@ __global__ void __launch_bounds__(128) scan_generic_kernel(ScanParams p) {
 
     float dsum = 0.f;
     for (int64_t t = t0; t < t1; ++t) {
+        if (MODE == MODE_FULL && p.ckpt && t % kCkptSteps == 0) {
+            float* ck = p.ckpt + ((b * p.ckpt_tiles + t / kCkptSteps) * p.dim + d) * N;
+#pragma unroll
+            for (int n = 0; n < N; ++n) ck[n] = h[n];
+        }
         const int64_t tok = (b * p.seqlen + t) * p.dim + d;
         const int64_t row = (b * p.seqlen + t) * N;
         float xv = load_f32(x + tok);

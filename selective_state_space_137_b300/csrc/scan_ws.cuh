@@ -359,6 +359,13 @@ __global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
     float dsum = 0.f;
     for (int j = 0; j < ntiles; ++j) {
         const int i = j % R;
+        if (FULL && p.ckpt && dval) {
+            // training forward: the state before this tile (T = 16 steps)
+            float* ck = p.ckpt + (((int64_t)b * p.ckpt_tiles + (t_begin / T) + j) * p.dim + d) * N + s * NS;
+#pragma unroll
+            for (int q = 0; q < NS / 2; q += 2)
+                *reinterpret_cast<float4*>(ck + 2 * q) = make_float4(h[q].x, h[q].y, h[q + 1].x, h[q + 1].y);
+        }
         if (!mbar_wait_bounded(&ready[i], (uint32_t)((j / R) & 1))) return;
         const unsigned char* slot = slot_ptr(i);
         const float2* dd = reinterpret_cast<const float2*>(slot + Cfg::SL_DD);

@@ -428,7 +428,7 @@ ssm_status scan_fwd_impl(const ssm_scan_desc* desc, bool zoh, const void* x, con
                          const float* A, const void* B, const void* C, const float* D,
                          const void* z, const float* delta_bias, void* out, float* last_state,
                          const float* initial_state, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+                         void* stream, float* ckpt = nullptr) {
     const ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -455,9 +455,12 @@ ssm_status scan_fwd_impl(const ssm_scan_desc* desc, bool zoh, const void* x, con
     }
     if (!x || !delta || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
 
-    const bool tiled = tiled_shape_ok(desc) && aligned16(x) && aligned16(delta) &&
-                       aligned16(B) && aligned16(C) && aligned16(out) && opt_aligned(z, 16) &&
-                       opt_aligned(last_state, 16);
+    bool tiled = tiled_shape_ok(desc) && aligned16(x) && aligned16(delta) &&
+                 aligned16(B) && aligned16(C) && aligned16(out) && opt_aligned(z, 16) &&
+                 opt_aligned(last_state, 16);
+    // checkpoints every 16 tokens: the warp-specialised kernel (16-step tiles)
+    // or the general one
+    if (ckpt && !(ws_path(desc) && SSM_WS_T == ssm::kCkptSteps)) tiled = false;
     int nchunk;
     int64_t chunk_len;
     if (tiled) {
@@ -465,12 +468,17 @@ ssm_status scan_fwd_impl(const ssm_scan_desc* desc, bool zoh, const void* x, con
     } else {
         nchunk = generic_nchunk(desc);
         chunk_len = (desc->seqlen + nchunk - 1) / nchunk;
+        if (ckpt && nchunk > 1)   // chunk starts on a checkpoint
+            chunk_len = (chunk_len + ssm::kCkptSteps - 1) / ssm::kCkptSteps * ssm::kCkptSteps;
+        if (ckpt) nchunk = (int)((desc->seqlen + chunk_len - 1) / chunk_len);
     }
     const size_t need = workspace_for(desc, nchunk);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
         return SSM_ERR_INVALID_ARG;
 
     ScanParams p;
+    p.ckpt = ckpt;
+    p.ckpt_tiles = (desc->seqlen + ssm::kCkptSteps - 1) / ssm::kCkptSteps;
     p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
     p.delta_bias = delta_bias; p.out = out; p.last_state = last_state;
     p.initial_state = initial_state;
@@ -528,6 +536,22 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
                         void* stream) {
     return scan_fwd_impl(desc, false, x, delta, A, B, C, D, z, delta_bias, out, last_state,
                          initial_state, workspace, workspace_bytes, stream);
+}
+
+size_t ssm_scan_checkpoint_size(const ssm_scan_desc* desc) {
+    if (check_desc(desc) != SSM_OK) return 0;
+    return (size_t)desc->batch * (size_t)((desc->seqlen + ssm::kCkptSteps - 1) / ssm::kCkptSteps) *
+           (size_t)desc->dim * (size_t)desc->dstate * sizeof(float);
+}
+
+ssm_status ssm_scan_fwd_train(const ssm_scan_desc* desc, const void* x, const void* delta,
+                              const float* A, const void* B, const void* C, const float* D,
+                              const void* z, const float* delta_bias, void* out, float* last_state,
+                              const float* initial_state, float* checkpoints, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    if (!checkpoints || !aligned16(checkpoints)) return SSM_ERR_INVALID_ARG;
+    return scan_fwd_impl(desc, false, x, delta, A, B, C, D, z, delta_bias, out, last_state,
+                         initial_state, workspace, workspace_bytes, stream, checkpoints);
 }
 
 ssm_status ssm_scan_fwd_ex(const ssm_scan_desc* desc, const ssm_scan_opts* opts, const void* x,
@@ -1076,7 +1100,7 @@ int bwd_channels_per_cta(int64_t n) {
 // Chunks of the time axis: one chunk unless the (sequence, channel-block)
 // CTAs fill less than half of the GPU's 2 x 148 slots (each chunk beyond the
 // first costs an aggregate pass forward and one backward).
-BwdPlan bwd_plan(const ssm_scan_desc* d) {
+BwdPlan bwd_plan(const ssm_scan_desc* d, bool with_ckpt = false) {
     BwdPlan pl;
     const int64_t N = d->dstate, L = d->seqlen;
     const int64_t ch = bwd_channels_per_cta(N);
@@ -1101,12 +1125,15 @@ BwdPlan bwd_plan(const ssm_scan_desc* d) {
     const size_t B = (size_t)d->batch, D = (size_t)d->dim, K = (size_t)pl.nchunk;
     size_t o = 0;
     if (pl.nchunk > 1) {
-        pl.off_fstart = o; o = align256(o + B * K * D * N * 4);
-        pl.off_fdsum = o;  o = align256(o + B * K * D * 4);
+        if (!with_ckpt) {   // chunk start states (the checkpoints hold them otherwise)
+            pl.off_fstart = o; o = align256(o + B * K * D * N * 4);
+            pl.off_fdsum = o;  o = align256(o + B * K * D * 4);
+        }
         pl.off_ebuf = o;   o = align256(o + B * K * D * N * 4);
         pl.off_bdsum = o;  o = align256(o + B * K * D * 4);
     }
-    pl.off_ckpt = o;  o = align256(o + B * (size_t)pl.ntiles * D * N * 4);
+    pl.off_ckpt = o;
+    if (!with_ckpt) o = align256(o + B * (size_t)pl.ntiles * D * N * 4);
     pl.off_pbc = o;   o = align256(o + (size_t)pl.nblk * B * (size_t)L * 2 * N * 4);
     pl.off_pa = o;    o = align256(o + B * K * D * N * 4);
     pl.off_pd = o;    o = align256(o + B * K * D * 4);
@@ -1122,12 +1149,14 @@ cudaError_t launch_bwd(const BwdPlan& pl, ssm::BwdParams p, const ScanParams& fp
                        float* dC, float* dA, float* dD, float* dbias, bool tma, cudaStream_t s) {
     using S = ssm::BwdShape<N>;
     if (p.nchunk > 1) {
-        // chunk start states, as the forward's chunked path computes them
         dim3 grid((unsigned)((p.dim + 127) / 128), (unsigned)p.batch, (unsigned)(p.nchunk - 1));
-        ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG><<<grid, 128, 0, s>>>(fp);
         const int64_t total = p.batch * p.dim * N;
-        ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-            p.A, p.initial_state, fp.carry, fp.dsum, p.batch, p.dim, N, p.nchunk);
+        if (!p.ckpt_given) {
+            // chunk start states, as the forward's chunked path computes them
+            ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG><<<grid, 128, 0, s>>>(fp);
+            ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+                p.A, p.initial_state, fp.carry, fp.dsum, p.batch, p.dim, N, p.nchunk);
+        }
         ssm::scan_bwd_agg_kernel<IO, N><<<grid, 128, 0, s>>>(p);
         ssm::scan_bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
             p.A, p.dlast, p.ebuf, p.bdsum, p.batch, p.dim, N, p.nchunk);
@@ -1207,6 +1236,12 @@ size_t ssm_scan_bwd_workspace_size(const ssm_scan_desc* desc) {
     return bwd_plan(desc).bytes;
 }
 
+size_t ssm_scan_bwd_ex_workspace_size(const ssm_scan_desc* desc, int with_checkpoints) {
+    if (check_desc(desc) != SSM_OK) return 0;
+    if (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) return 0;
+    return bwd_plan(desc, with_checkpoints != 0).bytes;
+}
+
 ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* delta,
                         const float* A, const void* B, const void* C, const float* D,
                         const void* z, const float* delta_bias, const float* initial_state,
@@ -1214,6 +1249,18 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
                         float* dA, float* dB, float* dC, float* dD, void* dz,
                         float* ddelta_bias, float* dinitial_state, void* workspace,
                         size_t workspace_bytes, void* stream) {
+    return ssm_scan_bwd_ex(desc, x, delta, A, B, C, D, z, delta_bias, initial_state, dout,
+                           dlast_state, nullptr, dx, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
+                           dinitial_state, workspace, workspace_bytes, stream);
+}
+
+ssm_status ssm_scan_bwd_ex(const ssm_scan_desc* desc, const void* x, const void* delta,
+                           const float* A, const void* B, const void* C, const float* D,
+                           const void* z, const float* delta_bias, const float* initial_state,
+                           const void* dout, const float* dlast_state, const float* checkpoints,
+                           void* dx, void* ddelta, float* dA, float* dB, float* dC, float* dD,
+                           void* dz, float* ddelta_bias, float* dinitial_state, void* workspace,
+                           size_t workspace_bytes, void* stream) {
     const ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     const size_t esz = io_size(desc);
@@ -1226,6 +1273,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
         !opt_aligned(ddelta_bias, 4) || !opt_aligned(dinitial_state, 4))
         return SSM_ERR_INVALID_ARG;
     if (dz && !z) return SSM_ERR_INVALID_ARG;
+    if (checkpoints && !aligned16(checkpoints)) return SSM_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t N = desc->dstate;
     const size_t Bz = (size_t)desc->batch, L = (size_t)desc->seqlen, Dm = (size_t)desc->dim;
@@ -1254,7 +1302,8 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
     if (!x || !delta || !A || !B || !C || !dout || !dx || !ddelta || !dA || !dB || !dC)
         return SSM_ERR_INVALID_ARG;
     if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
-    const BwdPlan pl = bwd_plan(desc);
+    const bool with_ckpt = checkpoints != nullptr;
+    const BwdPlan pl = bwd_plan(desc, with_ckpt);
     if (pl.nblk > 0x7fffffff || pl.nchunk > 65535) return SSM_ERR_UNSUPPORTED;
     if (workspace == nullptr || workspace_bytes < pl.bytes || !aligned16(workspace))
         return SSM_ERR_INVALID_ARG;
@@ -1267,8 +1316,8 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
     fp.batch = desc->batch; fp.seqlen = desc->seqlen; fp.dim = desc->dim;
     fp.nchunk = pl.nchunk; fp.chunk_len = pl.chunk_len;
     fp.softplus = desc->delta_softplus ? 1 : 0;
-    fp.carry = pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.off_fstart) : nullptr;
-    fp.dsum = pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.off_fdsum) : nullptr;
+    fp.carry = (pl.nchunk > 1 && !with_ckpt) ? reinterpret_cast<float*>(w + pl.off_fstart) : nullptr;
+    fp.dsum = (pl.nchunk > 1 && !with_ckpt) ? reinterpret_cast<float*>(w + pl.off_fdsum) : nullptr;
 
     ssm::BwdParams p;
     p.x = x; p.delta = delta; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
@@ -1277,7 +1326,8 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
     p.fstart = fp.carry;
     p.ebuf = pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.off_ebuf) : nullptr;
     p.bdsum = pl.nchunk > 1 ? reinterpret_cast<float*>(w + pl.off_bdsum) : nullptr;
-    p.ckpt = reinterpret_cast<float*>(w + pl.off_ckpt);
+    p.ckpt = with_ckpt ? const_cast<float*>(checkpoints) : reinterpret_cast<float*>(w + pl.off_ckpt);
+    p.ckpt_given = with_ckpt ? 1 : 0;
     p.pBC = reinterpret_cast<float*>(w + pl.off_pbc);
     p.pA = reinterpret_cast<float*>(w + pl.off_pa);
     p.pD = reinterpret_cast<float*>(w + pl.off_pd);

@@ -27,11 +27,13 @@ def _check(t, name, shape, dtype, device):
 
 def scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, initial_state=None,
              delta_softplus=True, out=None, last_state=None, workspace=None, stream=None,
-             discretization="euler"):
+             discretization="euler", checkpoints=None):
     """Selective scan forward.  x, delta, z: (batch, seqlen, dim); B, C:
     (batch, seqlen, dstate); A: (dim, dstate) fp32; D, delta_bias: (dim,) fp32;
     initial_state: (batch, dim, dstate) fp32 or None.  ``discretization``:
     "euler" (input term Delta B x) or "zoh" (exact zero-order hold).
+    ``checkpoints``: an fp32 device buffer of ssm_scan_checkpoint_size bytes
+    to keep the state before every 16th token for scan_bwd (training).
     Returns ``(out, last_state)``."""
     if not x.is_cuda:
         raise ValueError("scan_fwd runs on a CUDA device only")
@@ -55,10 +57,15 @@ def scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, initial_state=N
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if checkpoints is not None and discretization != "euler":
+        raise ValueError("checkpoints are kept by the first-order scan only")
     if discretization == "euler":
         st = _b.ssm_scan_fwd(desc, x, delta, A, B, C, D, z, delta_bias, out, last_state,
                              initial_state, workspace if need else None, wbytes if need else 0,
-                             stream)
+                             stream) if checkpoints is None else \
+        _b.ssm_scan_fwd_train(desc, x, delta, A, B, C, D, z, delta_bias, out, last_state,
+                              initial_state, checkpoints, workspace if need else None,
+                              wbytes if need else 0, stream)
     else:
         st = _b.ssm_scan_fwd_ex(desc, _b.make_opts(discretization), x, delta, A, B, C, D, z,
                                 delta_bias, out, last_state, initial_state,
@@ -206,8 +213,16 @@ def conv_state_update(conv_state, conv_w, state, x, delta, A, B, C, D=None, z=No
     return out
 
 
+def checkpoint_buffer(x, A):
+    """A device buffer for the training forward's checkpoints."""
+    bsz, seqlen, dim = x.shape
+    desc = _b.make_desc(bsz, seqlen, dim, A.shape[1], x.dtype)
+    n = _b.ssm_scan_checkpoint_size(desc) // 4
+    return torch.empty(max(n, 4), dtype=torch.float32, device=x.device)
+
+
 def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, delta_bias=None, initial_state=None,
-             dlast_state=None, delta_softplus=True, workspace=None, stream=None):
+             dlast_state=None, delta_softplus=True, workspace=None, stream=None, checkpoints=None):
     """Gradients of ``scan_fwd`` for dout = dL/dout (batch, seqlen, dim) and
     optionally dlast_state = dL/dlast_state (batch, dim, dstate) fp32.
     Returns a dict: dx, ddelta, dz (or None without z) in the I/O dtype; dA,
@@ -235,14 +250,14 @@ def scan_bwd(x, delta, A, B, C, dout, D=None, z=None, delta_bias=None, initial_s
          "ddelta_bias": torch.empty((dim,), **f32),
          "dinitial_state": torch.empty((bsz, dim, dstate), **f32)}
     desc = _b.make_desc(bsz, seqlen, dim, dstate, io, delta_softplus)
-    need = _b.ssm_scan_bwd_workspace_size(desc)
+    need = _b.ssm_scan_bwd_ex_workspace_size(desc, checkpoints is not None)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = _b.ssm_scan_bwd(desc, x, delta, A, B, C, D, z, delta_bias, initial_state, dout,
-                         dlast_state, g["dx"], g["ddelta"], g["dA"], g["dB"], g["dC"], g["dD"],
-                         g["dz"], g["ddelta_bias"], g["dinitial_state"],
-                         workspace if need else None, wbytes if need else 0, stream)
+    st = _b.ssm_scan_bwd_ex(desc, x, delta, A, B, C, D, z, delta_bias, initial_state, dout,
+                            dlast_state, checkpoints, g["dx"], g["ddelta"], g["dA"], g["dB"],
+                            g["dC"], g["dD"], g["dz"], g["ddelta_bias"], g["dinitial_state"],
+                            workspace if need else None, wbytes if need else 0, stream)
     if st != _b.SSM_OK:
         raise _b.SSMError(st, "ssm_scan_bwd")
     return g

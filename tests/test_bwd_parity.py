@@ -205,3 +205,45 @@ def test_bwd_workspace_checks(cuda):
                               f(w.batch, w.seqlen, w.dstate), None, None, None, None, small,
                               small.numel())
     assert st == binding.SSM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("case", ["small-bf16", "small-f32", "chunked", "n8", "ragged"])
+def test_bwd_with_training_checkpoints(cuda, case):
+    """The training pair: the forward keeps the state before every 16th
+    token; the checkpoints match the oracle's states there; the backward that
+    reads them matches the oracle's gradients."""
+    w = {"small-bf16": SMALL, "small-f32": dataclasses.replace(SMALL, io="f32"),
+         "chunked": synth.ScanWorkload("ck-chunked", 1, 6000, 48, 16, "bf16", 21, dt_lo=1e-4,
+                                       dt_hi=1e-2, init_state=True),
+         "n8": dataclasses.replace(SMALL, dstate=8, io="f32", seed=5),
+         "ragged": dataclasses.replace(SMALL, dim=40, seqlen=257, seed=6)}[case]
+    inp, dout, dl = make_case(w)
+    dev = to_device(inp, cuda)
+    ck = ops.checkpoint_buffer(dev["x"], dev["A"])
+    ops.scan_fwd(**dev, checkpoints=ck)
+    torch.cuda.synchronize()
+    ntiles = (w.seqlen + 15) // 16
+    ckv = ck[: w.batch * ntiles * w.dim * w.dstate].view(w.batch, ntiles, w.dim, w.dstate)
+    tol = TOL[inp["x"].dtype]
+    for j in sorted({0, 1, ntiles // 2, ntiles - 1}):
+        cut = lambda t: None if t is None else t[:, :16 * j]
+        if j == 0:
+            ref_state = f64(inp["initial_state"])
+        else:
+            _, ref_state = oracle.scan_fwd(f64(cut(inp["x"])), f64(cut(inp["delta"])), f64(inp["A"]),
+                                           f64(cut(inp["B"])), f64(cut(inp["C"])), D=f64(inp["D"]),
+                                           z=f64(cut(inp["z"])), delta_bias=f64(inp["delta_bias"]),
+                                           initial_state=f64(inp["initial_state"]))
+        assert rel_err(f64(ckv[:, j]), ref_state) <= tol, j
+    got = ops.scan_bwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"], dout.to(cuda),
+                       D=dev["D"], z=dev["z"], delta_bias=dev["delta_bias"],
+                       initial_state=dev["initial_state"], dlast_state=dl.to(cuda), checkpoints=ck)
+    torch.cuda.synchronize()
+    ref = oracle.scan_bwd(f64(inp["x"]), f64(inp["delta"]), f64(inp["A"]), f64(inp["B"]),
+                          f64(inp["C"]), f64(dout), D=f64(inp["D"]), z=f64(inp["z"]),
+                          delta_bias=f64(inp["delta_bias"]), initial_state=f64(inp["initial_state"]),
+                          dlast_state=f64(dl))
+    for k in PER_TOKEN:
+        assert rel_err(f64(got[k]), ref[k]) <= tol, k
+    for k in SUMMED:
+        assert norm_err(f64(got[k]), ref[k]) <= SUM_TOL[inp["x"].dtype], k
