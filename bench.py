@@ -918,6 +918,31 @@ def run_decode(args, dev, peak, peak_kind):
         times.append(e0.elapsed_time(e1))
     cold_ms = float(np.median(times))
     by = w.step_bytes()
+    # the same step with the width-4 causal conv in front (ssm_conv_state_update):
+    # conv state (batch, dim, 3) fp32 read and shifted in place, taps (dim, 4)
+    K = 4
+    conv = synth.make_conv_inputs(w.batch, w.dim, K, seed=w.seed + 3, device=str(dev),
+                                  with_state=True)
+    cdesc = binding.make_conv_desc(K, True)
+
+    def one_conv(s):
+        st = binding.ssm_conv_state_update(desc, cdesc, conv["conv_state"], conv["conv_w"],
+                                           conv["conv_bias"], state, inp["x"][s], inp["delta"][s],
+                                           inp["A"], inp["B"][s], inp["C"][s], inp["D"], inp["z"][s],
+                                           inp["delta_bias"], out, stream)
+        if st != binding.SSM_OK:
+            raise binding.SSMError(st, "ssm_conv_state_update")
+    ctimes = []
+    for s in range(32):
+        flush.fill_(s & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one_conv(s)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ctimes.append(e0.elapsed_time(e1))
+    conv_ms = float(np.median(ctimes))
+    conv_by = by + 2 * w.batch * w.dim * (K - 1) * 4 + w.dim * (K + 1) * 4
     return {"workload": w.name, "steps_chained": w.steps,
             "warm": {"ms_per_step": warm_ms, "gb_per_s": by / (warm_ms * 1e-3) / 1e9,
                      "steps_per_s": 1e3 / warm_ms},
@@ -926,6 +951,9 @@ def run_decode(args, dev, peak, peak_kind):
                            else graph_ms),
             "flushed": {"ms_per_step": cold_ms, "gb_per_s": by / (cold_ms * 1e-3) / 1e9,
                         "steps_per_s": 1e3 / cold_ms},
+            "conv_step_flushed": {"ms_per_step": conv_ms,
+                                  "gb_per_s": conv_by / (conv_ms * 1e-3) / 1e9,
+                                  "algorithmic_bytes": conv_by, "width": K},
             "roofline": {"bound": "hbm", "achieved": by / (cold_ms * 1e-3) / 1e9, "peak": peak,
                          "unit": "GB/s", "frac": by / (cold_ms * 1e-3) / 1e9 / peak,
                          "peak_kind": peak_kind, "algorithmic_bytes_per_launch": by,

@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "scan_generic.cuh"   // kMaxConvWidth
 #include "scan_tiled.cuh"     // silu_tiled, unpack / pack
+#include "tma.cuh"
 
 #ifndef SSM_CONV_UNROLL
 #define SSM_CONV_UNROLL 4    // rows loaded ahead per thread
@@ -145,6 +146,130 @@ __global__ void __launch_bounds__(128, SSM_CONV_MINBLOCKS) conv1d_kernel(ConvPar
         for (int q = 0; q < H; ++q)
 #pragma unroll
             for (int v = 0; v < VEC; ++v) p.state_out[(b * p.dim + d0 + v) * H + q] = wnd[q][v];
+    }
+}
+
+}  // namespace ssm
+
+// ---------------------------------------------------------------------------
+// The same convolution streamed through shared memory by TMA: a CTA owns
+// kConvCC channels of one sequence over a chunk of time and walks it in
+// kConvTT-step tiles.  Each tile's x box starts H = K-1 rows early (the
+// history; rows before t = 0 read as zeros and are replaced by the conv
+// state), lands in an S-stage mbarrier ring, and thread c slides the K-tap
+// window of channel c down the tile; the output tile leaves by TMA store
+// (two buffers).  Every byte of x is read once from DRAM (the halo rows of a
+// tile were the previous tile's rows, from L2), every output written once.
+namespace ssm {
+
+constexpr int kConvCC = 128, kConvTT = 32, kConvStages = 4;
+
+struct ConvMaps {
+    CUtensorMap x, out;   // (dim, seqlen, batch); boxes [TT + H][CC] and [TT][CC]
+};
+
+template <typename IO, int K>
+struct ConvTmaCfg {
+    static constexpr int H = K - 1, ESZ = (int)sizeof(IO);
+    static constexpr int IN_ROWS = kConvTT + H;
+    static constexpr int STAGE = round_up(IN_ROWS * kConvCC * ESZ, 128);
+    static constexpr int OUT = kConvTT * kConvCC * ESZ;
+    static constexpr int OFF_OUT = kConvStages * STAGE;
+    static constexpr int OFF_BAR = round_up(OFF_OUT + 2 * OUT, 128);
+    static constexpr int SMEM = OFF_BAR + kConvStages * 8;
+};
+
+template <typename IO, int K>
+__global__ void __launch_bounds__(kConvCC) conv1d_tma_kernel(const __grid_constant__ ConvMaps maps,
+                                                             ConvParams p) {
+    using Cfg = ConvTmaCfg<IO, K>;
+    constexpr int H = Cfg::H, S = kConvStages, TT = kConvTT, CC = kConvCC;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+    const int c = threadIdx.x;
+    const int d0 = blockIdx.x * CC;
+    const int64_t d = (int64_t)d0 + c;
+    const bool dval = d < p.dim;
+    const int b = blockIdx.z;
+    const int64_t c0 = (int64_t)blockIdx.y * p.chunk;
+    int64_t c1 = c0 + p.chunk;
+    if (c1 > p.seqlen) c1 = p.seqlen;
+    const int ntiles = c1 > c0 ? (int)((c1 - c0 + TT - 1) / TT) : 0;
+
+    int issued = 0;   // thread 0's count of tiles whose loads went out
+    auto issue = [&](int j) {
+        issued = j + 1;
+        const int t0 = (int)(c0 + (int64_t)j * TT);
+        mbar_arrive_expect_tx(&full[j % S], (uint32_t)(Cfg::IN_ROWS * CC * Cfg::ESZ));
+        tma_load_3d(smem + (j % S) * Cfg::STAGE, &maps.x, &full[j % S], d0, t0 - H, b);
+    };
+    if (c == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (c == 0) {
+        prefetch_tmap(&maps.x);
+        prefetch_tmap(&maps.out);
+        for (int j = 0; j < S && j < ntiles; ++j) issue(j);
+    }
+    float w[K], bias = 0.f;
+#pragma unroll
+    for (int q = 0; q < K; ++q) w[q] = dval ? __ldg(p.w + d * K + q) : 0.f;
+    if (p.bias && dval) bias = __ldg(p.bias + d);
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+        const bool landed = mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1));
+        if (c == 0) bulk_wait_read<1>();   // the store that last read this tile's output buffer
+        // one decision for the whole block: a timed-out wait ends every thread's loop
+        if (!__syncthreads_and(landed)) { ok = false; break; }
+        const IO* xs = reinterpret_cast<const IO*>(smem + (j % S) * Cfg::STAGE);
+        IO* os = reinterpret_cast<IO*>(smem + Cfg::OFF_OUT + (j & 1) * Cfg::OUT);
+        const int64_t t0 = c0 + (int64_t)j * TT;
+        // the window: raw inputs at times t0 - H .. t0 - 1 (stage rows 0 .. H-1)
+        float win[H > 0 ? H : 1];
+#pragma unroll
+        for (int q = 0; q < H; ++q) {
+            const int64_t tt = t0 - H + q;
+            win[q] = tt >= 0 ? load1(xs + q * CC + c)
+                             : ((p.state_in && dval) ? __ldg(p.state_in + ((int64_t)b * p.dim + d) * H + H + tt) : 0.f);
+        }
+#pragma unroll 8
+        for (int r = 0; r < TT; ++r) {
+            const float xv = load1(xs + (H + r) * CC + c);
+            float acc = bias;
+#pragma unroll
+            for (int q = 0; q < H; ++q) acc = fmaf(w[q], win[q], acc);
+            acc = fmaf(w[H], xv, acc);
+            store_io(os + r * CC + c, p.act ? silu_tiled<IO>(acc) : acc);
+#pragma unroll
+            for (int q = 0; q < H; ++q) win[q] = q + 1 < H ? win[q + 1] : xv;
+        }
+        // the final conv state: the last H raw inputs of the sequence
+        if (p.state_out && dval && c1 == p.seqlen && j == ntiles - 1) {
+            const int last = (int)(c1 - t0);   // rows of this tile that exist
+#pragma unroll
+            for (int q = 0; q < H; ++q) {
+                const int64_t tt = p.seqlen - H + q;
+                const float v = tt >= 0 ? load1(xs + (last + q) * CC + c)
+                                        : (p.state_in ? __ldg(p.state_in + ((int64_t)b * p.dim + d) * H + H + tt) : 0.f);
+                p.state_out[((int64_t)b * p.dim + d) * H + q] = v;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();   // the tile's inputs are read and its outputs written
+        if (c == 0) {
+            tma_store_3d(&maps.out, os, d0, (int)t0, b);
+            bulk_commit();
+            if (j + S < ntiles) issue(j + S);
+        }
+    }
+    if (c == 0) {
+        bulk_wait<0>();
+        if (!ok) {   // the loads still in flight land before the CTA exits
+            for (int j = issued - S > 0 ? issued - S : 0; j < issued; ++j)
+                mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), 100000000ull);
+        }
     }
 }
 

@@ -9,7 +9,8 @@
 // run of the state with 128-bit accesses (SPL = 4).
 #pragma once
 #include "common.cuh"
-#include "scan_tiled.cuh"   // softplus_tiled / silu_tiled
+#include "scan_generic.cuh"   // kMaxConvWidth
+#include "scan_tiled.cuh"     // softplus_tiled / silu_tiled
 
 namespace ssm {
 
@@ -77,7 +78,7 @@ __device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f) {
 // of the state, the matching A row slice and B/C slices with vector loads, and
 // the channel's x, delta, z; no integer division is needed to locate them.
 template <typename IO, int N, bool CONV = false, bool ZOH = false, bool VEC = true>
-__global__ void __launch_bounds__(256, (CONV || ZOH) ? 4 : 8) state_update_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(256, CONV ? 5 : (ZOH ? 4 : 8)) state_update_kernel(DecodeParams p) {
     constexpr int LPC = DecodeShape<N>::LPC;
     constexpr int SPL = DecodeShape<N>::SPL;
     const int lin = blockIdx.x * blockDim.x + threadIdx.x;    // lane index within the sequence
@@ -111,20 +112,47 @@ __global__ void __launch_bounds__(256, (CONV || ZOH) ? 4 : 8) state_update_kerne
     load_vec<SPL, VEC>(Cm + b * N + sub * SPL, cv);
     float xv = load_f32(x + ch);
     if (CONV) {
-        // x_conv from the K-1 stored inputs and the new one; the state shift is
-        // written below by the channel's first lane (all lanes read it first)
+        // x_conv from the K-1 stored inputs and the new one.
+        constexpr int HM = kMaxConvWidth - 1;
         const int H = p.conv_width - 1;
-        float acc = p.conv_bias ? __ldg(p.conv_bias + d) : 0.f;
-        for (int q = 0; q < H; ++q)
-            acc = fmaf(__ldg(p.conv_w + (int64_t)d * p.conv_width + q), p.conv_state[ch * H + q], acc);
-        acc = fmaf(__ldg(p.conv_w + (int64_t)d * p.conv_width + H), xv, acc);
         const float raw = xv;
-        xv = p.conv_act ? silu_tiled<IO>(acc) : acc;
-        __syncwarp();   // every lane of the warp has read the state before it is shifted
-        if (valid && sub == 0) {
-            for (int q = 0; q + 1 < H; ++q) p.conv_state[ch * H + q] = p.conv_state[ch * H + q + 1];
-            if (H > 0) p.conv_state[ch * H + H - 1] = raw;
+        float cw[kMaxConvWidth];
+#pragma unroll
+        for (int q = 0; q < kMaxConvWidth; ++q)
+            cw[q] = q <= H ? __ldg(p.conv_w + (int64_t)d * p.conv_width + q) : 0.f;
+        float acc = p.conv_bias ? __ldg(p.conv_bias + d) : 0.f;
+        if (H <= LPC) {
+            // lane `sub` of the channel holds history slot `sub`: one load and
+            // one store per lane, the other slots by shuffle
+            const int base = (threadIdx.x & 31) - sub;
+            const float v = sub < H ? p.conv_state[ch * H + sub] : 0.f;
+#pragma unroll
+            for (int q = 0; q < HM; ++q) {
+                const float cq = __shfl_sync(0xffffffffu, v, (base + (q < LPC ? q : 0)) & 31);
+                if (q < H) acc = fmaf(cw[q], cq, acc);
+            }
+            const float nxt = __shfl_sync(0xffffffffu, v, (base + (sub + 1 < LPC ? sub + 1 : 0)) & 31);
+            if (valid && sub < H) p.conv_state[ch * H + sub] = sub + 1 < H ? nxt : raw;
+        } else {
+            // longer histories: every lane reads them (one batch of loads), the
+            // channel's first lane writes the shifted state after a warp sync
+            float cs[HM];
+#pragma unroll
+            for (int q = 0; q < HM; ++q) cs[q] = q < H ? p.conv_state[ch * H + q] : 0.f;
+#pragma unroll
+            for (int q = 0; q < HM; ++q)
+                if (q < H) acc = fmaf(cw[q], cs[q], acc);
+            __syncwarp();
+            if (valid && sub == 0) {
+#pragma unroll
+                for (int q = 0; q < HM; ++q)
+                    if (q < H) p.conv_state[ch * H + q] = q + 1 < H ? cs[q + 1] : raw;
+            }
         }
+#pragma unroll
+        for (int q = 0; q < kMaxConvWidth; ++q)
+            if (q == H) acc = fmaf(cw[q], xv, acc);
+        xv = p.conv_act ? silu_tiled<IO>(acc) : acc;
     }
     const float u = load_f32(dl + ch) + (p.delta_bias ? __ldg(p.delta_bias + d) : 0.f);
     const float zv = z ? load_f32(z + ch) : 0.f;

@@ -704,6 +704,53 @@ cudaError_t launch_conv(const ssm::ConvParams& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// The TMA-streamed form (16-byte rows and 16-byte aligned x, out).
+template <typename IO, int K>
+cudaError_t launch_conv_tma_k(const ssm::ConvMaps& maps, const ssm::ConvParams& p, cudaStream_t s) {
+    using Cfg = ssm::ConvTmaCfg<IO, K>;
+    auto k = ssm::conv1d_tma_kernel<IO, K>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((p.dim + ssm::kConvCC - 1) / ssm::kConvCC),
+                    (unsigned)((p.seqlen + p.chunk - 1) / p.chunk), (unsigned)p.batch);
+    k<<<grid, ssm::kConvCC, Cfg::SMEM, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_conv_tma(ssm::ConvParams p, cudaStream_t s) {
+    const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int e = (int)sizeof(IO);
+    // time chunks: multiples of the tile, about four waves of CTAs
+    const int64_t blocks = ((p.dim + ssm::kConvCC - 1) / ssm::kConvCC) * p.batch;
+    int64_t nch = blocks > 0 ? ((int64_t)kPlanSMs * 4 * 4 + blocks - 1) / blocks : 1;
+    const int64_t most = p.seqlen / 128 > 1 ? p.seqlen / 128 : 1;
+    if (nch > most) nch = most;
+    if (nch > 65535) nch = 65535;
+    if (nch < 1) nch = 1;
+    int64_t chunk = (p.seqlen + nch - 1) / nch;
+    chunk = (chunk + ssm::kConvTT - 1) / ssm::kConvTT * ssm::kConvTT;
+    p.chunk = chunk;
+    ssm::ConvMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    const int H = p.width - 1;
+    if (!encode_3d(&maps.x, p.x, dt, e, p.dim, p.seqlen, p.batch, ssm::kConvCC, ssm::kConvTT + H) ||
+        !encode_3d(&maps.out, p.out, dt, e, p.dim, p.seqlen, p.batch, ssm::kConvCC, ssm::kConvTT))
+        return cudaErrorInvalidValue;
+    switch (p.width) {
+        case 1: return launch_conv_tma_k<IO, 1>(maps, p, s);
+        case 2: return launch_conv_tma_k<IO, 2>(maps, p, s);
+        case 3: return launch_conv_tma_k<IO, 3>(maps, p, s);
+        case 4: return launch_conv_tma_k<IO, 4>(maps, p, s);
+        case 5: return launch_conv_tma_k<IO, 5>(maps, p, s);
+        case 6: return launch_conv_tma_k<IO, 6>(maps, p, s);
+        case 7: return launch_conv_tma_k<IO, 7>(maps, p, s);
+        case 8: return launch_conv_tma_k<IO, 8>(maps, p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
 // Copy (or zero) the conv state when there are no tokens to push through it.
 cudaError_t conv_state_passthrough(float* out, const float* in, size_t bytes, cudaStream_t s) {
     if (!out || out == in || bytes == 0) return cudaSuccess;
@@ -741,6 +788,18 @@ ssm_status ssm_conv1d_fwd(const ssm_scan_desc* desc, const ssm_conv_desc* conv, 
     if (overlaps(x, out, io_bytes)) return SSM_ERR_INVALID_ARG;
     if (desc->batch > 65535) return SSM_ERR_UNSUPPORTED;
 
+    // the TMA-streamed kernel when rows are 16-byte multiples and x, out aligned
+    if ((desc->dim * (int64_t)esz) % 16 == 0 && aligned16(x) && aligned16(out) &&
+        desc->seqlen < ((int64_t)1 << 31) - 64 && desc->dim < ((int64_t)1 << 31)) {
+        ssm::ConvParams pt;
+        pt.x = x; pt.w = w; pt.bias = bias; pt.state_in = conv_state_in; pt.out = out;
+        pt.state_out = conv_state_out;
+        pt.batch = desc->batch; pt.seqlen = desc->seqlen; pt.dim = desc->dim;
+        pt.width = conv->width; pt.act = conv->activation; pt.chunk = 0;
+        const cudaError_t et = desc->io_dtype == SSM_DTYPE_F32 ? launch_conv_tma<float>(pt, s)
+                                                              : launch_conv_tma<__nv_bfloat16>(pt, s);
+        return et == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    }
     const int vec = desc->io_dtype == SSM_DTYPE_F32 ? 4 : SSM_CONV_VEC16;
     const bool wide = desc->dim % vec == 0 && aligned16(x) && aligned16(out);   // vector rows
     ssm::ConvParams p;
