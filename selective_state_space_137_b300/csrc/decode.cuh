@@ -77,8 +77,11 @@ __device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float* f) {
 // threads per block), y is the sequence.  Each thread loads its 16-byte slice
 // of the state, the matching A row slice and B/C slices with vector loads, and
 // the channel's x, delta, z; no integer division is needed to locate them.
-template <typename IO, int N, bool CONV = false, bool ZOH = false, bool VEC = true>
-__global__ void __launch_bounds__(256, CONV ? 5 : (ZOH ? 4 : 8)) state_update_kernel(DecodeParams p) {
+// KW: the conv width as a compile-time constant (0: read from p.conv_width,
+// up to kMaxConvWidth); a fixed width keeps the conv step within 32 registers.
+template <typename IO, int N, bool CONV = false, bool ZOH = false, bool VEC = true, int KW = 0>
+__global__ void __launch_bounds__(256, CONV ? (KW > 0 ? (sizeof(IO) == 2 ? 8 : 6) : 5) : (ZOH ? 4 : 8))
+state_update_kernel(DecodeParams p) {
     constexpr int LPC = DecodeShape<N>::LPC;
     constexpr int SPL = DecodeShape<N>::SPL;
     const int lin = blockIdx.x * blockDim.x + threadIdx.x;    // lane index within the sequence
@@ -111,15 +114,21 @@ __global__ void __launch_bounds__(256, CONV ? 5 : (ZOH ? 4 : 8)) state_update_ke
     load_vec<SPL, VEC>(Bm + b * N + sub * SPL, bv);
     load_vec<SPL, VEC>(Cm + b * N + sub * SPL, cv);
     float xv = load_f32(x + ch);
+    // every input is loaded before the conv history is rewritten in place, so
+    // all loads of the step go out together
+    const float u = load_f32(dl + ch) + (p.delta_bias ? __ldg(p.delta_bias + d) : 0.f);
+    const float zv = z ? load_f32(z + ch) : 0.f;
+    const float dsk = p.D ? __ldg(p.D + d) : 0.f;
     if (CONV) {
         // x_conv from the K-1 stored inputs and the new one.
-        constexpr int HM = kMaxConvWidth - 1;
-        const int H = p.conv_width - 1;
+        constexpr int KM = KW > 0 ? KW : kMaxConvWidth;
+        constexpr int HM = KM - 1;
+        const int H = KW > 0 ? KW - 1 : p.conv_width - 1;
         const float raw = xv;
-        float cw[kMaxConvWidth];
+        float cw[KM];
 #pragma unroll
-        for (int q = 0; q < kMaxConvWidth; ++q)
-            cw[q] = q <= H ? __ldg(p.conv_w + (int64_t)d * p.conv_width + q) : 0.f;
+        for (int q = 0; q < KM; ++q)
+            cw[q] = q <= H ? __ldg(p.conv_w + (int64_t)d * (H + 1) + q) : 0.f;
         float acc = p.conv_bias ? __ldg(p.conv_bias + d) : 0.f;
         if (H <= LPC) {
             // lane `sub` of the channel holds history slot `sub`: one load and
@@ -150,13 +159,10 @@ __global__ void __launch_bounds__(256, CONV ? 5 : (ZOH ? 4 : 8)) state_update_ke
             }
         }
 #pragma unroll
-        for (int q = 0; q < kMaxConvWidth; ++q)
+        for (int q = 0; q < KM; ++q)
             if (q == H) acc = fmaf(cw[q], xv, acc);
         xv = p.conv_act ? silu_tiled<IO>(acc) : acc;
     }
-    const float u = load_f32(dl + ch) + (p.delta_bias ? __ldg(p.delta_bias + d) : 0.f);
-    const float zv = z ? load_f32(z + ch) : 0.f;
-    const float dsk = p.D ? __ldg(p.D + d) : 0.f;
 
     const float dt = p.softplus ? softplus_tiled<IO>(u) : u;
     const float dx = dt * xv;

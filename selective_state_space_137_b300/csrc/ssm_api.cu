@@ -111,7 +111,9 @@ template <typename IO, int N, bool CONV = false, bool ZOH = false>
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
     const int64_t lanes = p.dim * ssm::DecodeShape<N>::LPC;   // per sequence
     const dim3 grid((unsigned)((lanes + 255) / 256), (unsigned)p.batch);
-    if (p.vec)
+    if (CONV && !ZOH && p.vec && p.conv_width == 4)   // the usual width, fixed at compile time
+        ssm::state_update_kernel<IO, N, CONV, ZOH, true, CONV && !ZOH ? 4 : 0><<<grid, 256, 0, s>>>(p);
+    else if (p.vec)
         ssm::state_update_kernel<IO, N, CONV, ZOH, true><<<grid, 256, 0, s>>>(p);
     else
         ssm::state_update_kernel<IO, N, CONV, ZOH, false><<<grid, 256, 0, s>>>(p);

@@ -210,14 +210,23 @@ def test_conv_scan_matches_conv_then_scan_on_gpu(cuda):
 
 # ------------------------------------------------------------- decode + conv
 
-@pytest.mark.parametrize("n", [1, 4, 16, 64])
-@pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_conv_decode_chain(cuda, n, io):
-    bsz, dim, steps, width = 3, 72, 8, 4
-    w = synth.DecodeWorkload("conv-decode", bsz, dim, n, steps, io, 140 + n)
+def element_aligned(t):
+    """t's values one element past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = buf[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def run_conv_decode_chain(cuda, n, io, width, shift=False):
+    bsz, dim, steps = 3, 72, 8
+    w = synth.DecodeWorkload("conv-decode", bsz, dim, n, steps, io, 140 + n + 7 * width)
     inp = synth.make_decode_inputs(w)
-    conv = synth.make_conv_inputs(bsz, dim, width, seed=150 + n, with_state=True)
+    conv = synth.make_conv_inputs(bsz, dim, width, seed=150 + n + width, with_state=True)
     dev, cd = to_device(inp, cuda), to_device(conv, cuda)
+    if shift:   # element loads instead of vector loads for A, B, C
+        dev = dict(dev, A=element_aligned(dev["A"]), B=element_aligned(dev["B"]),
+                   C=element_aligned(dev["C"]))
     tol = TOL[synth.io_dtype(io)]
     state, cstate = dev["state"].clone(), cd["conv_state"].clone()
     ref_state, ref_cstate = f64(inp["state"]), f64(conv["conv_state"])
@@ -235,6 +244,28 @@ def test_conv_decode_chain(cuda, n, io):
         assert rel_err(f64(out), ref_out) <= tol, (s, rel_err(f64(out), ref_out))
         assert rel_err(f64(state), ref_state) <= tol
         assert np.array_equal(f64(cstate), ref_cstate), s
+
+
+@pytest.mark.parametrize("n", [1, 4, 16, 64])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_conv_decode_chain(cuda, n, io):
+    """Width 4 (the kernel with the width fixed at compile time)."""
+    run_conv_decode_chain(cuda, n, io, 4)
+
+
+@pytest.mark.parametrize("width", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("n", [4, 16])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_conv_decode_widths(cuda, width, n, io):
+    """Other widths take the runtime-width kernel: histories that fit the
+    channel's lanes (shuffle shift) and longer ones (per-lane reads)."""
+    run_conv_decode_chain(cuda, n, io, width)
+
+
+@pytest.mark.parametrize("width", [3, 4])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_conv_decode_element_aligned(cuda, width, io):
+    run_conv_decode_chain(cuda, 16, io, width, shift=True)
 
 
 def test_conv_decode_continues_prefill(cuda):
