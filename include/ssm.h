@@ -247,6 +247,29 @@ SSM_API ssm_status ssm_selection_proj_fwd(const ssm_scan_desc *desc, const ssm_p
  * Elements must be aligned to their size; B and C at 4-element alignment take
  * vector loads. */
 SSM_API size_t ssm_scan_bwd_workspace_size(const ssm_scan_desc *desc);
+
+/* How ssm_scan_bwd (with_checkpoints = 0) or ssm_scan_bwd_ex with checkpoints
+ * (with_checkpoints = 1) will execute `desc` (host-side query, no GPU work).
+ *   nchunk    : pieces the time axis is cut into (1 = one reverse sweep per
+ *               (sequence, channel block))
+ *   warps     : warps per CTA of the reverse sweep, 4 .. 8, chosen so that
+ *               the CTAs spread evenly over the 148 SMs
+ *   channels  : channels per CTA (warps x 32 / lanes per channel)
+ *   ctas      : CTAs of the reverse sweep
+ *   workspace : bytes of workspace the call needs
+ * Returns SSM_ERR_INVALID_ARG for a NULL `info` and the descriptor checks'
+ * status (as ssm_scan_bwd would) for a bad descriptor. */
+typedef struct {
+    int32_t nchunk;
+    int32_t warps;
+    int32_t channels;
+    int32_t reserved;
+    int64_t ctas;
+    int64_t workspace;
+} ssm_scan_bwd_plan_info;
+
+SSM_API ssm_status ssm_scan_bwd_plan(const ssm_scan_desc *desc, int with_checkpoints,
+                                     ssm_scan_bwd_plan_info *info);
 SSM_API ssm_status ssm_scan_bwd(const ssm_scan_desc *desc, const void *x, const void *delta,
                                 const float *A, const void *B, const void *C, const float *D,
                                 const void *z, const float *delta_bias,

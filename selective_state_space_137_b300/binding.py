@@ -25,7 +25,7 @@ EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
             "ssm_scan_bwd", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_lti_kernel",
             "ssm_lti_conv_fwd", "ssm_selection_proj_fwd", "ssm_scan_fwd_host_workspace_size",
             "ssm_scan_fwd_host", "ssm_scan_checkpoint_size", "ssm_scan_fwd_train",
-            "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex")
+            "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex", "ssm_scan_bwd_plan")
 SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
 SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -51,6 +51,11 @@ class ssm_proj_desc(ctypes.Structure):
 class ssm_scan_plan_info(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("nchunk", ctypes.c_int32), ("launches", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("workspace", ctypes.c_int64)]
+
+
+class ssm_scan_bwd_plan_info(ctypes.Structure):
+    _fields_ = [("nchunk", ctypes.c_int32), ("warps", ctypes.c_int32), ("channels", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("ctas", ctypes.c_int64), ("workspace", ctypes.c_int64)]
 
 
 class SSMError(RuntimeError):
@@ -116,6 +121,8 @@ def _load():
                                           vp, vp]
     lib.ssm_scan_plan.restype = ctypes.c_int
     lib.ssm_scan_plan.argtypes = [dp, ctypes.POINTER(ssm_scan_plan_info)]
+    lib.ssm_scan_bwd_plan.restype = ctypes.c_int
+    lib.ssm_scan_bwd_plan.argtypes = [dp, ctypes.c_int, ctypes.POINTER(ssm_scan_bwd_plan_info)]
     lib.ssm_selftest_wait_timeout.restype = ctypes.c_int
     lib.ssm_selftest_wait_timeout.argtypes = [ctypes.c_int64, vp]
     lib.ssm_get_device_status.restype = ctypes.c_int
@@ -185,6 +192,14 @@ def ssm_scan_plan(desc: ssm_scan_desc) -> ssm_scan_plan_info:
     st = lib.ssm_scan_plan(ctypes.byref(desc), ctypes.byref(info))
     if st != SSM_OK:
         raise SSMError(st, "ssm_scan_plan")
+    return info
+
+
+def ssm_scan_bwd_plan(desc: ssm_scan_desc, with_checkpoints: bool = False) -> ssm_scan_bwd_plan_info:
+    info = ssm_scan_bwd_plan_info()
+    st = lib.ssm_scan_bwd_plan(ctypes.byref(desc), int(bool(with_checkpoints)), ctypes.byref(info))
+    if st != SSM_OK:
+        raise SSMError(st, "ssm_scan_bwd_plan")
     return info
 
 

@@ -71,16 +71,19 @@ struct BwdParams {
 };
 
 constexpr int kBwdT = 16;       // steps per tile (checkpoint spacing)
-constexpr int kBwdWarps = 8;
+constexpr int kBwdWarps = 8;    // warps per CTA of the register-path sweep
 
-template <int N>
+// W: warps per CTA (the host picks it so that the CTAs spread evenly over the SMs)
+template <int N, int W_ = kBwdWarps>
 struct BwdShape {
     static constexpr int LPC = N >= 4 ? (N / 4 > 32 ? 32 : N / 4) : 1;   // lanes per channel
     static constexpr int SPL = N / LPC;                                  // states per lane
     static constexpr int CPW = 32 / LPC;                                 // channels per warp
-    static constexpr int CH = CPW * kBwdWarps;                           // channels per CTA
+    static constexpr int W = W_;                                         // warps per CTA
+    static constexpr int CH = CPW * W;                                   // channels per CTA
+    static constexpr int MINB = 65536 / (W * 32 * 128);                  // CTAs per SM at 128 registers
     static constexpr int V = 2 * SPL;                                    // dB | dC values per lane
-    static constexpr int SMEM = kBwdWarps * kBwdT * 2 * N * 4;
+    static constexpr int SMEM = W * kBwdT * 2 * N * 4;
 };
 
 template <int SPL, typename IO>
@@ -234,11 +237,11 @@ __global__ void scan_bwd_carry_kernel(const float* __restrict__ A, const float* 
 }
 
 // 4. The reverse sweep of one chunk for CH channels of one sequence.
-template <typename IO, int N>
-__global__ void __launch_bounds__(256, 2) scan_bwd_kernel(BwdParams p) {
-    using S = BwdShape<N>;
+template <typename IO, int N, int W = kBwdWarps>
+__global__ void __launch_bounds__(W * 32, BwdShape<N, W>::MINB) scan_bwd_kernel(BwdParams p) {
+    using S = BwdShape<N, W>;
     constexpr int LPC = S::LPC, SPL = S::SPL, CPW = S::CPW, CH = S::CH, V = S::V, T = kBwdT;
-    extern __shared__ float red[];   // [kBwdWarps][T][2N]
+    extern __shared__ float red[];   // [W][T][2N]
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int sub = lane % LPC;
@@ -411,7 +414,7 @@ __global__ void __launch_bounds__(256, 2) scan_bwd_kernel(BwdParams p) {
         for (int e = threadIdx.x; e < steps * 2 * N; e += blockDim.x) {
             float acc = 0.f;
 #pragma unroll
-            for (int w = 0; w < kBwdWarps; ++w) acc += red[w * T * 2 * N + e];
+            for (int w = 0; w < S::W; ++w) acc += red[w * T * 2 * N + e];
             const int s = e / (2 * N), v = e % (2 * N);
             p.pBC[(((int64_t)blockIdx.x * p.batch + b) * p.seqlen + ts + s) * 2 * N + v] = acc;
         }
@@ -448,9 +451,9 @@ struct BwdMaps {
     CUtensorMap x, delta, dout, z, B, C, dx, ddelta, dz;
 };
 
-template <typename IO, int N>
+template <typename IO, int N, int W>
 struct BwdTmaCfg {
-    using S = BwdShape<N>;
+    using S = BwdShape<N, W>;
     static constexpr int CH = S::CH, T = kBwdT, ESZ = (int)sizeof(IO), NST = 2;
     static constexpr int TOK = T * CH * ESZ;                 // one [T][CH] tile
     static constexpr int ROW = T * N * ESZ;                  // one [T][N] tile
@@ -464,18 +467,24 @@ struct BwdTmaCfg {
     // of a channel write different steps without bank conflicts)
     static constexpr int SROW = CH + 8, NSCR = 6;
     enum { S_DT = 0, S_DX, S_X, S_DYC, S_ZF, S_SGU };
-    static constexpr int OFF_SCR = OFF_RED + kBwdWarps * T * 2 * N * 4;
-    static constexpr int OFF_BAR = OFF_SCR + NSCR * T * SROW * 4;
+    static constexpr int OFF_SCR = OFF_RED + S::W * T * 2 * N * 4;
+    // per warp, two buffers of [CPW][RS] fp32: the step's dB | dC terms of the
+    // warp's channels, summed over the channels by lane o = output o.  RS = N
+    // mod 32 puts the rows that a quarter-warp writes on disjoint banks.
+    static constexpr int RS = 2 * N + (32 - N % 32) % 32;
+    static constexpr int WSUM = S::CPW * RS;
+    static constexpr int OFF_WSUM = OFF_SCR + NSCR * T * SROW * 4;
+    static constexpr int OFF_BAR = OFF_WSUM + S::W * 2 * WSUM * 4;
     static constexpr int OFF_FLAG = OFF_BAR + NST * 8;
     static constexpr int SMEM = OFF_FLAG + 16;
     static_assert((CH * ESZ) % 16 == 0 && (N * ESZ) % 16 == 0, "TMA rows are 16-byte multiples");
 };
 
-template <typename IO, int N>
-__global__ void __launch_bounds__(256, 2)
+template <typename IO, int N, int W>
+__global__ void __launch_bounds__(W * 32, BwdShape<N, W>::MINB)
     scan_bwd_tma_kernel(const __grid_constant__ BwdMaps maps, BwdParams p) {
-    using Cfg = BwdTmaCfg<IO, N>;
-    using S = BwdShape<N>;
+    using Cfg = BwdTmaCfg<IO, N, W>;
+    using S = BwdShape<N, W>;
     constexpr int LPC = S::LPC, SPL = S::SPL, CPW = S::CPW, CH = S::CH, V = S::V, T = kBwdT;
     constexpr int NST = Cfg::NST;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -486,6 +495,7 @@ __global__ void __launch_bounds__(256, 2)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    float* wsum = reinterpret_cast<float*>(smem + Cfg::OFF_WSUM) + warp * 2 * Cfg::WSUM;
     const int sub = lane % LPC;
     const int cl = warp * CPW + lane / LPC;                 // channel within the CTA
     const int d0 = blockIdx.x * CH;
@@ -652,9 +662,14 @@ __global__ void __launch_bounds__(256, 2)
                     dyc = dov * zv * sg;
                     zf = dov * sg * (1.f + zv * (1.f - sg));
                 }
+                // a channel past the last one: Delta x = dyc = 0 makes its dB and dC
+                // terms exactly 0 (its inputs are channel 0's, finite), so the
+                // per-step channel sums need no masking
+                if (!valid) dyc = 0.f;
+                const float dxs = valid ? dt * xv : 0.f;
                 float* sc = scr + sl * Cfg::SROW + cl;
                 sc[Cfg::S_DT * T * Cfg::SROW] = dt;
-                sc[Cfg::S_DX * T * Cfg::SROW] = dt * xv;
+                sc[Cfg::S_DX * T * Cfg::SROW] = dxs;
                 sc[Cfg::S_X * T * Cfg::SROW] = xv;
                 sc[Cfg::S_DYC * T * Cfg::SROW] = dyc;
                 sc[Cfg::S_ZF * T * Cfg::SROW] = zf;
@@ -675,10 +690,16 @@ __global__ void __launch_bounds__(256, 2)
                         const float dx = sv(Cfg::S_DX, s);
                         float bv[SPL];
                         bwd_load_smem<SPL>(Bs + s * N + n0, bv);
+                        const f32x2 dt2 = pk2(dt, dt), dx2 = pk2(dx, dx);
 #pragma unroll
-                        for (int q = 0; q < SPL; ++q) {
-                            hc[q] = fmaf(ex2_sfu(dt * a2[q]), hc[q], dx * bv[q]);
+                        for (int q = 0; q < SPL; q += 2) {
+                            float e0, e1;
+                            upk2(mul2(dt2, pk2(a2[q], a2[q + 1])), e0, e1);
+                            const f32x2 hn = fma2(pk2(ex2_sfu(e0), ex2_sfu(e1)), pk2(hc[q], hc[q + 1]),
+                                                  mul2(dx2, pk2(bv[q], bv[q + 1])));
+                            upk2(hn, hc[q], hc[q + 1]);
                             hist[s][q] = hc[q];
+                            hist[s][q + 1] = hc[q + 1];
                         }
                     }
                 }
@@ -702,18 +723,31 @@ __global__ void __launch_bounds__(256, 2)
                     }
                     float vals[V];
                     float s1 = 0.f, s2 = 0.f;
+                    {   // the same per-state terms on pairs of states (f32x2)
+                        const f32x2 dyc2 = pk2(dyc, dyc), dt2 = pk2(dt, dt), dx2 = pk2(dx, dx);
+                        f32x2 s1v = pk2(0.f, 0.f), s2v = pk2(0.f, 0.f);
 #pragma unroll
-                    for (int q = 0; q < SPL; ++q) {
-                        const float hprev = s > 0 ? hist[s > 0 ? s - 1 : 0][q] : hs[q];
-                        const float g = fmaf(dyc, cv[q], G[q]);
-                        const float dA = ex2_sfu(dt * a2[q]);
-                        const float qv = g * dA * hprev;
-                        s1 = fmaf(g, bv[q], s1);
-                        s2 = fmaf(an[q], qv, s2);
-                        dAacc[q] = fmaf(dt, qv, dAacc[q]);
-                        vals[q] = g * dx;                     // dB
-                        vals[SPL + q] = dyc * hist[s][q];     // dC
-                        G[q] = dA * g;
+                        for (int q = 0; q < SPL; q += 2) {
+                            const int sp = s > 0 ? s - 1 : 0;
+                            const f32x2 hprev = s > 0 ? pk2(hist[sp][q], hist[sp][q + 1]) : pk2(hs[q], hs[q + 1]);
+                            const f32x2 g = fma2(dyc2, pk2(cv[q], cv[q + 1]), pk2(G[q], G[q + 1]));
+                            float e0, e1;
+                            upk2(mul2(dt2, pk2(a2[q], a2[q + 1])), e0, e1);
+                            const f32x2 gd = mul2(g, pk2(ex2_sfu(e0), ex2_sfu(e1)));
+                            const f32x2 qv = mul2(gd, hprev);
+                            s1v = fma2(g, pk2(bv[q], bv[q + 1]), s1v);
+                            s2v = fma2(pk2(an[q], an[q + 1]), qv, s2v);
+                            upk2(fma2(dt2, qv, pk2(dAacc[q], dAacc[q + 1])), dAacc[q], dAacc[q + 1]);
+                            upk2(mul2(g, dx2), vals[q], vals[q + 1]);                       // dB
+                            upk2(mul2(dyc2, pk2(hist[s][q], hist[s][q + 1])), vals[SPL + q],
+                                 vals[SPL + q + 1]);                                      // dC
+                            upk2(gd, G[q], G[q + 1]);
+                        }
+                        float a_, b_;
+                        upk2(s1v, a_, b_);
+                        s1 = a_ + b_;
+                        upk2(s2v, a_, b_);
+                        s2 = a_ + b_;
                     }
                     s1 = reduce_slices<LPC>(s1);
                     s2 = reduce_slices<LPC>(s2);
@@ -724,18 +758,30 @@ __global__ void __launch_bounds__(256, 2)
                         store_io(ob + Cfg::TOK / Cfg::ESZ + s * CH + cl, du);
                         store_io(ob + 2 * (Cfg::TOK / Cfg::ESZ) + s * CH + cl, dzv);
                     }
-                    if (!valid) {
+                    {   // sums over the warp's channels through shared memory: lane
+                        // (channel c, slice sub) writes its terms to row c, then lane o
+                        // adds output o down the CPW rows (one conflict-free load each)
+                        float* wb = wsum + (s & 1) * Cfg::WSUM;
+                        static_assert(SPL % 4 == 0, "float4 rows");
+                        float* row = wb + (lane / LPC) * Cfg::RS + n0;
 #pragma unroll
-                        for (int i = 0; i < V; ++i) vals[i] = 0.f;
-                    }
-                    const int base = reduce_channels<V, LPC>(vals, lane);
-                    constexpr int HOLD = V / CPW > 0 ? V / CPW : 1;
-                    const bool writer = CPW <= V || ((lane / LPC) % (CPW / (V < CPW ? V : CPW))) == 0;
-                    if (writer) {
+                        for (int q = 0; q < SPL; q += 4) {
+                            *reinterpret_cast<float4*>(row + q) =
+                                make_float4(vals[q], vals[q + 1], vals[q + 2], vals[q + 3]);
+                            *reinterpret_cast<float4*>(row + N + q) =
+                                make_float4(vals[SPL + q], vals[SPL + q + 1], vals[SPL + q + 2],
+                                            vals[SPL + q + 3]);
+                        }
+                        __syncwarp();
 #pragma unroll
-                        for (int i = 0; i < HOLD; ++i) {
-                            const int vi = base + i;
-                            myred[s * 2 * N + (vi / SPL) * N + n0 + vi % SPL] = vals[i];
+                        for (int o0 = 0; o0 < 2 * N; o0 += 32) {
+                            const int o = o0 + lane;
+                            if (o < 2 * N) {
+                                float acc = wb[o];
+#pragma unroll
+                                for (int c = 1; c < CPW; ++c) acc += wb[c * Cfg::RS + o];
+                                myred[s * 2 * N + o] = acc;
+                            }
                         }
                     }
                 }
@@ -748,7 +794,7 @@ __global__ void __launch_bounds__(256, 2)
         for (int e = threadIdx.x; e < steps * 2 * N; e += blockDim.x) {
             float acc = 0.f;
 #pragma unroll
-            for (int w = 0; w < kBwdWarps; ++w) acc += red[w * T * 2 * N + e];
+            for (int w = 0; w < S::W; ++w) acc += red[w * T * 2 * N + e];
             const int s = e / (2 * N), v = e % (2 * N);
             p.pBC[(((int64_t)blockIdx.x * p.batch + b) * p.seqlen + ts + s) * 2 * N + v] = acc;
         }

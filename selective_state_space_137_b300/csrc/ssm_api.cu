@@ -1138,6 +1138,7 @@ namespace {
 
 struct BwdPlan {
     int nchunk = 1;
+    int warps = ssm::kBwdWarps;   // warps per CTA of the sweep
     int64_t chunk_len = 0, ntiles = 0, nblk = 0;
     size_t off_fstart = 0, off_fdsum = 0, off_ebuf = 0, off_bdsum = 0, off_ckpt = 0, off_pbc = 0,
            off_pa = 0, off_pd = 0, off_pbias = 0, bytes = 0;
@@ -1145,17 +1146,81 @@ struct BwdPlan {
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-int bwd_channels_per_cta(int64_t n) {
-    switch (n) {
-        case 1: return ssm::BwdShape<1>::CH;
-        case 2: return ssm::BwdShape<2>::CH;
-        case 4: return ssm::BwdShape<4>::CH;
-        case 8: return ssm::BwdShape<8>::CH;
-        case 16: return ssm::BwdShape<16>::CH;
-        case 32: return ssm::BwdShape<32>::CH;
-        case 64: return ssm::BwdShape<64>::CH;
+// Warps per CTA of the sweep that are compiled: 5..8 for dstate 8 and 16,
+// 6 or 8 for 32, 4 or 8 for 64 (the counts the picker below chooses for
+// realistic shapes; the CTA's channel block stays a 16-byte TMA row), 8 for
+// dstate below 8.
+constexpr bool bwd_warps_ok(int n, int w) {
+    return n < 8 ? w == ssm::kBwdWarps
+                 : (n <= 16 ? (w >= 5 && w <= 8) : (n == 32 ? (w == 6 || w == 8) : (w == 4 || w == 8)));
+}
+
+int bwd_channels_per_cta(int64_t n, int w) {
+    if (n != 1 && n != 2 && n != 4 && n != 8 && n != 16 && n != 32 && n != 64) return 0;
+    const int lpc = n >= 4 ? (n / 4 > 32 ? 32 : (int)(n / 4)) : 1;
+    return (32 / lpc) * w;
+}
+
+// Shared memory of the TMA-staged sweep (bytes), for the residency estimate.
+template <int N, int W>
+int bwd_smem_of(bool f32) {
+    if constexpr (N < 8 || !bwd_warps_ok(N, W)) {
+        return 0;
+    } else {
+        return f32 ? ssm::BwdTmaCfg<float, N, W>::SMEM : ssm::BwdTmaCfg<__nv_bfloat16, N, W>::SMEM;
+    }
+}
+template <int N>
+int bwd_smem_n(int w, bool f32) {
+    switch (w) {
+        case 4: return bwd_smem_of<N, 4>(f32);
+        case 5: return bwd_smem_of<N, 5>(f32);
+        case 6: return bwd_smem_of<N, 6>(f32);
+        case 7: return bwd_smem_of<N, 7>(f32);
+        case 8: return bwd_smem_of<N, 8>(f32);
     }
     return 0;
+}
+int bwd_sweep_smem(int64_t n, int w, bool f32) {
+    switch (n) {
+        case 8: return bwd_smem_n<8>(w, f32);
+        case 16: return bwd_smem_n<16>(w, f32);
+        case 32: return bwd_smem_n<32>(w, f32);
+        case 64: return bwd_smem_n<64>(w, f32);
+    }
+    return 0;
+}
+
+// Warps per CTA for a grid of batch x channel blocks: the count that gives the
+// busiest SM the fewest channels.  The CTAs of one wave land round-robin, so
+// an SM holds ceil(ctas / 148) of them; a grid that needs a second wave (more
+// CTAs than 148 x the CTAs that fit an SM at 128 registers) is charged for the
+// wave.  Four-warp CTAs run about 15% slower per channel (measured), ties go
+// to more warps.
+int bwd_pick_warps(int64_t batch, int64_t dim, int64_t n, bool f32) {
+    int best = ssm::kBwdWarps;
+    double best_cost = 1e300;
+    for (int w = 8; w >= 4; --w) {
+        if (!bwd_warps_ok((int)n, w)) continue;
+        const int64_t ch = bwd_channels_per_cta(n, w);
+        const int64_t ctas = batch * ((dim + ch - 1) / ch);
+        // CTAs per SM: registers (128 per thread) and shared memory (228 KB per
+        // SM, 1 KB of it reserved per CTA)
+        int64_t per_sm = 65536 / (w * 32 * 128);
+        const int64_t sm_bytes = bwd_sweep_smem(n, w, f32);
+        if (sm_bytes > 0 && 233472 / (sm_bytes + 1024) < per_sm) per_sm = 233472 / (sm_bytes + 1024);
+        if (per_sm < 1) per_sm = 1;
+        const int64_t slots = (int64_t)kPlanSMs * per_sm;
+        const double slow = w == 4 ? 1.15 : 1.0;
+        const double cost = ctas <= slots
+                                ? (double)((ctas + kPlanSMs - 1) / kPlanSMs) * ch * slow
+                                : (double)((ctas + slots - 1) / slots) * per_sm * ch * slow * 1.25;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = w;
+        }
+    }
+    return best;
 }
 
 // Chunks of the time axis: one chunk unless the (sequence, channel-block)
@@ -1164,12 +1229,16 @@ int bwd_channels_per_cta(int64_t n) {
 BwdPlan bwd_plan(const ssm_scan_desc* d, bool with_ckpt = false) {
     BwdPlan pl;
     const int64_t N = d->dstate, L = d->seqlen;
-    const int64_t ch = bwd_channels_per_cta(N);
+    const int64_t ch = bwd_channels_per_cta(N, pl.warps);
     pl.nblk = ch > 0 ? (d->dim + ch - 1) / ch : 0;
     const int64_t groups = d->batch * pl.nblk;
     const int64_t slots = (int64_t)kPlanSMs * 2;
     int64_t k = 1;
-    if (groups > 0 && groups * 2 < slots) {
+    if (groups > 0 && groups * 2 >= slots) {   // one chunk: spread the CTAs evenly
+        pl.warps = bwd_pick_warps(d->batch, d->dim, N, d->io_dtype == SSM_DTYPE_F32);
+        const int64_t chw = bwd_channels_per_cta(N, pl.warps);
+        pl.nblk = (d->dim + chw - 1) / chw;
+    } else if (groups > 0) {
         k = (slots + groups - 1) / groups;
         const int64_t kmax = L / 512;
         if (k > kmax) k = kmax;
@@ -1205,10 +1274,53 @@ BwdPlan bwd_plan(const ssm_scan_desc* d, bool with_ckpt = false) {
 
 // The TMA-staged reverse sweep (scan_bwd_tma_kernel) applies to dstate 8..64
 // with 16-byte rows and 16-byte aligned token tensors (checked by the caller).
+// The reverse sweep with W warps per CTA: TMA-staged when `tma`, else the
+// register path.
+template <typename IO, int N, int W>
+cudaError_t launch_sweep(const BwdPlan& pl, const ssm::BwdParams& p, bool tma, cudaStream_t s) {
+    if constexpr (!bwd_warps_ok(N, W)) {
+        return cudaErrorInvalidValue;
+    } else {
+        using S = ssm::BwdShape<N, W>;
+        const dim3 grid((unsigned)pl.nblk, (unsigned)p.batch, (unsigned)p.nchunk);
+        if constexpr (N >= 8) {
+            if (tma) {
+                using Cfg = ssm::BwdTmaCfg<IO, N, W>;
+                const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+                const int e = (int)sizeof(IO);
+                ssm::BwdMaps maps;
+                memset(&maps, 0, sizeof(maps));
+                const int64_t Dm = p.dim, L = p.seqlen, Bz = p.batch;
+                bool ok = encode_3d(&maps.x, p.x, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
+                          encode_3d(&maps.delta, p.delta, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
+                          encode_3d(&maps.dout, p.dout, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
+                          encode_3d(&maps.B, p.B, dt, e, N, L, Bz, N, Cfg::T) &&
+                          encode_3d(&maps.C, p.C, dt, e, N, L, Bz, N, Cfg::T) &&
+                          encode_3d(&maps.dx, p.dx, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
+                          encode_3d(&maps.ddelta, p.ddelta, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T);
+                if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T);
+                if (ok && p.dz) ok = encode_3d(&maps.dz, p.dz, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T);
+                if (!ok) return cudaErrorInvalidValue;
+                auto kt = ssm::scan_bwd_tma_kernel<IO, N, W>;
+                cudaError_t err =
+                    cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+                if (err != cudaSuccess) return err;
+                kt<<<grid, W * 32, Cfg::SMEM, s>>>(maps, p);
+                return cudaGetLastError();
+            }
+        }
+        auto kb = ssm::scan_bwd_kernel<IO, N, W>;
+        cudaError_t err = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+        if (err != cudaSuccess) return err;
+        kb<<<grid, W * 32, S::SMEM, s>>>(p);
+        return cudaGetLastError();
+    }
+}
+
 template <typename IO, int N>
 cudaError_t launch_bwd(const BwdPlan& pl, ssm::BwdParams p, const ScanParams& fp, float* dB,
                        float* dC, float* dA, float* dD, float* dbias, bool tma, cudaStream_t s) {
-    using S = ssm::BwdShape<N>;
     if (p.nchunk > 1) {
         dim3 grid((unsigned)((p.dim + 127) / 128), (unsigned)p.batch, (unsigned)(p.nchunk - 1));
         const int64_t total = p.batch * p.dim * N;
@@ -1222,38 +1334,16 @@ cudaError_t launch_bwd(const BwdPlan& pl, ssm::BwdParams p, const ScanParams& fp
         ssm::scan_bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
             p.A, p.dlast, p.ebuf, p.bdsum, p.batch, p.dim, N, p.nchunk);
     }
-    const dim3 grid((unsigned)pl.nblk, (unsigned)p.batch, (unsigned)p.nchunk);
-    if constexpr (N >= 8) {
-        if (tma) {
-            using Cfg = ssm::BwdTmaCfg<IO, N>;
-            const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-            const int e = (int)sizeof(IO);
-            ssm::BwdMaps maps;
-            memset(&maps, 0, sizeof(maps));
-            const int64_t Dm = p.dim, L = p.seqlen, Bz = p.batch;
-            bool ok = encode_3d(&maps.x, p.x, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
-                      encode_3d(&maps.delta, p.delta, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
-                      encode_3d(&maps.dout, p.dout, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
-                      encode_3d(&maps.B, p.B, dt, e, N, L, Bz, N, Cfg::T) &&
-                      encode_3d(&maps.C, p.C, dt, e, N, L, Bz, N, Cfg::T) &&
-                      encode_3d(&maps.dx, p.dx, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T) &&
-                      encode_3d(&maps.ddelta, p.ddelta, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T);
-            if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T);
-            if (ok && p.dz) ok = encode_3d(&maps.dz, p.dz, dt, e, Dm, L, Bz, Cfg::CH, Cfg::T);
-            if (!ok) return cudaErrorInvalidValue;
-            auto kt = ssm::scan_bwd_tma_kernel<IO, N>;
-            cudaError_t err = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-            if (err != cudaSuccess) return err;
-            kt<<<grid, 256, Cfg::SMEM, s>>>(maps, p);
-        }
+    cudaError_t err;
+    switch (pl.warps) {
+        case 4: err = launch_sweep<IO, N, 4>(pl, p, tma, s); break;
+        case 5: err = launch_sweep<IO, N, 5>(pl, p, tma, s); break;
+        case 6: err = launch_sweep<IO, N, 6>(pl, p, tma, s); break;
+        case 7: err = launch_sweep<IO, N, 7>(pl, p, tma, s); break;
+        case 8: err = launch_sweep<IO, N, 8>(pl, p, tma, s); break;
+        default: err = cudaErrorInvalidValue;
     }
-    if (!tma || N < 8) {
-        auto kb = ssm::scan_bwd_kernel<IO, N>;
-        cudaError_t err = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
-        if (err != cudaSuccess) return err;
-        kb<<<grid, 256, S::SMEM, s>>>(p);
-    }
+    if (err != cudaSuccess) return err;
     const int64_t nout = p.batch * p.seqlen * 2 * N + p.dim * N + 2 * p.dim;
     ssm::scan_bwd_reduce_kernel<N><<<(unsigned)((nout + 255) / 256), 256, 0, s>>>(
         p, (int)pl.nblk, dB, dC, dA, dD, dbias);
@@ -1301,6 +1391,22 @@ size_t ssm_scan_bwd_ex_workspace_size(const ssm_scan_desc* desc, int with_checkp
     if (check_desc(desc) != SSM_OK) return 0;
     if (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) return 0;
     return bwd_plan(desc, with_checkpoints != 0).bytes;
+}
+
+ssm_status ssm_scan_bwd_plan(const ssm_scan_desc* desc, int with_checkpoints,
+                             ssm_scan_bwd_plan_info* info) {
+    if (!info) return SSM_ERR_INVALID_ARG;
+    const ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    memset(info, 0, sizeof(*info));
+    if (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) return SSM_OK;
+    const BwdPlan pl = bwd_plan(desc, with_checkpoints != 0);
+    info->nchunk = pl.nchunk;
+    info->warps = pl.warps;
+    info->channels = bwd_channels_per_cta(desc->dstate, pl.warps);
+    info->ctas = pl.nblk * desc->batch * pl.nchunk;
+    info->workspace = (int64_t)pl.bytes;
+    return SSM_OK;
 }
 
 ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* delta,

@@ -183,3 +183,30 @@ def test_lti_rejections_before_launch(ssm_lib):
     assert L.ssm_lti_conv_fwd(d, A16, A16 + 2, None, None, A16) == L.SSM_ERR_INVALID_ARG
     assert L.ssm_lti_conv_fwd(d, None, A16, None, None, A16) == L.SSM_ERR_INVALID_ARG
     assert L.ssm_lti_conv_fwd(L.make_desc(0, 64, 16, 1, 0), A16, A16, None, None, A16) == L.SSM_OK
+
+
+def test_bwd_plan_query(ssm_lib):
+    """ssm_scan_bwd_plan: warps per CTA chosen so the CTAs spread evenly over
+    the 148 SMs (one wave), its workspace equals the size query's, and it
+    rejects what the size query rejects."""
+    bf = torch.bfloat16
+    big = ssm_lib.make_desc(4, 8192, 4096, 16, bf)         # Mamba-1.4B layer
+    pl = ssm_lib.ssm_scan_bwd_plan(big)
+    assert (pl.nchunk, pl.warps, pl.channels, pl.ctas) == (1, 7, 56, 296)
+    pl = ssm_lib.ssm_scan_bwd_plan(ssm_lib.make_desc(8, 2048, 1536, 16, bf))   # Mamba-130M layer
+    assert (pl.nchunk, pl.warps, pl.channels, pl.ctas) == (1, 6, 48, 256)
+    pl = ssm_lib.ssm_scan_bwd_plan(ssm_lib.make_desc(1, 262144, 2048, 16, bf))  # few channels, long
+    assert pl.nchunk > 1 and pl.warps == 8
+    for d in (big, ssm_lib.make_desc(2, 300, 72, 16, torch.float32),
+              ssm_lib.make_desc(4, 8192, 4096, 64, bf), ssm_lib.make_desc(1, 40, 5000, 8, bf)):
+        for ck in (False, True):
+            pl = ssm_lib.ssm_scan_bwd_plan(d, ck)
+            assert pl.workspace == ssm_lib.ssm_scan_bwd_ex_workspace_size(d, ck)
+            assert pl.ctas == pl.nchunk * d.batch * -(-d.dim // pl.channels)
+            assert pl.ctas <= 148 * (65536 // (pl.warps * 32 * 128)) or pl.warps == 8
+    empty = ssm_lib.ssm_scan_bwd_plan(ssm_lib.make_desc(0, 10, 16, 16, bf))
+    assert empty.ctas == 0 and empty.workspace == 0
+    bad = ssm_lib.make_desc(1, 10, 16, 3, bf)
+    info = ssm_lib.ssm_scan_bwd_plan_info()
+    assert ssm_lib.lib.ssm_scan_bwd_plan(ctypes.byref(bad), 0, ctypes.byref(info)) == ssm_lib.SSM_ERR_UNSUPPORTED
+    assert ssm_lib.lib.ssm_scan_bwd_plan(ctypes.byref(big), 0, None) == ssm_lib.SSM_ERR_INVALID_ARG

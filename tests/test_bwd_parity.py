@@ -247,3 +247,31 @@ def test_bwd_with_training_checkpoints(cuda, case):
         assert rel_err(f64(got[k]), ref[k]) <= tol, k
     for k in SUMMED:
         assert norm_err(f64(got[k]), ref[k]) <= SUM_TOL[inp["x"].dtype], k
+
+
+def shape_for_warps(warps, n, io, L=40):
+    """The smallest (batch, dim) whose backward plan sweeps in one chunk with
+    `warps` warps per CTA and, where the channel block allows it, a partial
+    last block of channels (found through the plan query)."""
+    dt = synth.io_dtype(io)
+    for total in range(148 * 8, 60000, 8):
+        for b in (1, 2, 4):
+            if total % b or (total // b) % 8:
+                continue
+            d = total // b
+            pl = binding.ssm_scan_bwd_plan(binding.make_desc(b, L, d, n, dt))
+            if pl.nchunk == 1 and pl.warps == warps and (d % pl.channels or pl.channels <= 8):
+                return b, d
+    raise AssertionError(f"no shape selects {warps} warps at dstate {n}")
+
+
+@pytest.mark.parametrize("n,warps,io", [(16, 5, "bf16"), (16, 6, "bf16"), (16, 6, "f32"),
+                                        (16, 7, "bf16"), (8, 5, "bf16"), (8, 7, "f32"),
+                                        (32, 6, "bf16"), (64, 4, "bf16")])
+def test_bwd_warps_per_cta(cuda, n, warps, io):
+    """Every compiled CTA width of the reverse sweep, on a shape that selects
+    it (one chunk; 40 steps = two full tiles and a ragged one)."""
+    b, d = shape_for_warps(warps, n, io)
+    w = synth.ScanWorkload(f"bwd-w{warps}-n{n}-{io}", b, 40, d, n, io, 30 + warps + n,
+                           init_state=True)
+    check_bwd(w, cuda)
