@@ -176,10 +176,22 @@ __device__ __forceinline__ float sigmoid_fast(float u) {
 
 // ---------------------------------------------------------------------------
 // 2. Backward aggregate of chunk k >= 1: E_k with nothing from the right.
+// LPC lanes per channel, SPL states per lane (the sweep's layout).  Steps go
+// in groups of LPC from the chunk's end: lane j of a channel evaluates the
+// per-token values (Delta, dyc) of step t - j, and the group's values reach
+// the channel's other lanes by shuffle, so each is computed once.  Delta and
+// dyc use the sweep's formulas.
 template <typename IO, int N>
 __global__ void __launch_bounds__(128) scan_bwd_agg_kernel(BwdParams p) {
-    const int64_t d = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (d >= p.dim) return;
+    using S = BwdShape<N>;
+    constexpr int LPC = S::LPC, SPL = S::SPL;
+    const int64_t lin = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t d_raw = lin / LPC;
+    const int sub = (int)(lin % LPC);
+    const bool valid = d_raw < p.dim;
+    const int64_t d = valid ? d_raw : 0;        // idle lanes stay for the shuffles
+    const int base = (int)(threadIdx.x & 31) - sub;
+    const int n0 = sub * SPL;
     const int64_t b = blockIdx.y;
     const int k = blockIdx.z + 1;
     const int64_t t0 = (int64_t)k * p.chunk_len;
@@ -189,32 +201,50 @@ __global__ void __launch_bounds__(128) scan_bwd_agg_kernel(BwdParams p) {
     const IO* Cm = static_cast<const IO*>(p.C);
     const IO* z = static_cast<const IO*>(p.z);
     const IO* dout = static_cast<const IO*>(p.dout);
-    float a2[N], G[N];
+    float a2[SPL], G[SPL];
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-        a2[n] = __ldg(p.A + d * N + n) * kLog2e;
-        G[n] = 0.f;
+    for (int q = 0; q < SPL; ++q) {
+        a2[q] = __ldg(p.A + d * N + n0 + q) * kLog2e;
+        G[q] = 0.f;
     }
     const float bias = p.delta_bias ? __ldg(p.delta_bias + d) : 0.f;
     float dsum = 0.f;
-    for (int64_t t = t1 - 1; t >= t0; --t) {
-        const int64_t tok = (b * p.seqlen + t) * p.dim + d;
-        const float u = load_f32(delta + tok) + bias;
-        const float dt = p.softplus ? softplus_accurate(u) : u;
-        float dyc = load_f32(dout + tok);
-        if (z) dyc *= silu_accurate(load_f32(z + tok));
-        const IO* crow = Cm + (b * p.seqlen + t) * N;
-#pragma unroll
-        for (int n = 0; n < N; ++n) {
-            const float g = fmaf(dyc, load_f32(crow + n), G[n]);
-            G[n] = ex2_sfu(dt * a2[n]) * g;
+    for (int64_t tg = t1 - 1; tg >= t0; tg -= LPC) {
+        const int64_t tm = tg - sub;
+        float dt_m = 0.f, dyc_m = 0.f;
+        if (tm >= t0) {
+            const int64_t tok = (b * p.seqlen + tm) * p.dim + d;
+            const float u = load_f32(delta + tok) + bias;
+            dt_m = p.softplus ? softplus_tiled<IO>(u) : u;
+            dyc_m = load_f32(dout + tok);
+            if (z) {
+                const float zv = load_f32(z + tok);
+                dyc_m *= zv * sigmoid_fast(zv);
+            }
         }
-        dsum += dt;
-    }
-    float* e = p.ebuf + ((b * p.nchunk + k) * p.dim + d) * N;
+        dsum += dt_m;
 #pragma unroll
-    for (int n = 0; n < N; ++n) e[n] = G[n];
-    p.bdsum[(b * p.nchunk + k) * p.dim + d] = dsum;
+        for (int j = 0; j < LPC; ++j) {
+            const float dt = __shfl_sync(0xffffffffu, dt_m, base + j);
+            const float dyc = __shfl_sync(0xffffffffu, dyc_m, base + j);
+            const int64_t t = tg - j;
+            if (t >= t0) {   // the same for every lane of the warp
+                float cv[SPL];
+                bwd_load<SPL>(Cm + (b * p.seqlen + t) * N + n0, cv, p.vec);
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) {
+                    const float g = fmaf(dyc, cv[q], G[q]);
+                    G[q] = ex2_sfu(dt * a2[q]) * g;
+                }
+            }
+        }
+    }
+    dsum = reduce_slices<LPC>(dsum);
+    if (!valid) return;
+    float* e = p.ebuf + ((b * p.nchunk + k) * p.dim + d) * N + n0;
+#pragma unroll
+    for (int q = 0; q < SPL; ++q) e[q] = G[q];
+    if (sub == 0) p.bdsum[(b * p.nchunk + k) * p.dim + d] = dsum;
 }
 
 // 3. Right-to-left combine of the chunk terms, per (b, d, n).

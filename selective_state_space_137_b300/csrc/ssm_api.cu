@@ -238,7 +238,7 @@ void tiled_chunks(const ssm_scan_desc* d, int* nchunk, int64_t* chunk_len) {
     const int64_t target = (int64_t)kPlanSMs * per_sm;
     int64_t k = 1;
     if (groups > 0 && groups * 2 < target) {
-        k = (target + groups - 1) / groups;
+        k = target / groups;   // rounded down: every CTA of the pass in one wave
         const int64_t kmax = d->seqlen / (4 * kTileT);
         if (k > kmax) k = kmax;
         if (k > 4096) k = 4096;
@@ -312,8 +312,10 @@ cudaError_t launch_tiled(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// agg_only: the chunk aggregates and carries alone (the chunk start states
+// that the backward's recompute needs); out and z are not read.
 template <typename IO, int CK = 0, bool ZOH = false>
-cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
+cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s, bool agg_only = false) {
     using Cfg = WsConfig<IO, CK>;
     const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -325,9 +327,11 @@ cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
     bool ok = encode_3d(&maps.x, p.x, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, x_rows) &&
               encode_3d(&maps.delta, p.delta, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
               encode_3d(&maps.B, p.B, dt, e, Cfg::N, d->seqlen, d->batch, Cfg::N, Cfg::T) &&
-              encode_3d(&maps.C, p.C, dt, e, Cfg::N, d->seqlen, d->batch, Cfg::N, Cfg::T) &&
-              encode_3d(&maps.out, p.out, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
-    if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+              encode_3d(&maps.C, p.C, dt, e, Cfg::N, d->seqlen, d->batch, Cfg::N, Cfg::T);
+    if (ok && !agg_only)
+        ok = encode_3d(&maps.out, p.out, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+    if (ok && p.z && !agg_only)
+        ok = encode_3d(&maps.z, p.z, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
     if (!ok) return cudaErrorInvalidValue;
     auto kfull = ssm::scan_ws_kernel<IO, Cfg, ssm::MODE_FULL, ZOH>;
     auto kagg = ssm::scan_ws_kernel<IO, Cfg, ssm::MODE_AGG, ZOH>;
@@ -342,6 +346,7 @@ cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
         ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
             p.A, p.initial_state, p.carry, p.dsum, p.batch, p.dim, Cfg::N, p.nchunk);
     }
+    if (agg_only) return cudaGetLastError();
     kfull<<<dim3(gx, (unsigned)d->batch, (unsigned)p.nchunk), Cfg::THREADS, Cfg::SMEM, s>>>(maps, p);
     return cudaGetLastError();
 }
@@ -1239,7 +1244,7 @@ BwdPlan bwd_plan(const ssm_scan_desc* d, bool with_ckpt = false) {
         const int64_t chw = bwd_channels_per_cta(N, pl.warps);
         pl.nblk = (d->dim + chw - 1) / chw;
     } else if (groups > 0) {
-        k = (slots + groups - 1) / groups;
+        k = slots / groups;   // rounded down: every CTA of the sweep in one wave
         const int64_t kmax = L / 512;
         if (k > kmax) k = kmax;
         if (k > 4096) k = 4096;
@@ -1319,18 +1324,34 @@ cudaError_t launch_sweep(const BwdPlan& pl, const ssm::BwdParams& p, bool tma, c
 }
 
 template <typename IO, int N>
-cudaError_t launch_bwd(const BwdPlan& pl, ssm::BwdParams p, const ScanParams& fp, float* dB,
-                       float* dC, float* dA, float* dD, float* dbias, bool tma, cudaStream_t s) {
+cudaError_t launch_bwd(const ssm_scan_desc* desc, const BwdPlan& pl, ssm::BwdParams p,
+                       const ScanParams& fp, float* dB, float* dC, float* dA, float* dD,
+                       float* dbias, bool tma, cudaStream_t s) {
     if (p.nchunk > 1) {
         dim3 grid((unsigned)((p.dim + 127) / 128), (unsigned)p.batch, (unsigned)(p.nchunk - 1));
         const int64_t total = p.batch * p.dim * N;
         if (!p.ckpt_given) {
-            // chunk start states, as the forward's chunked path computes them
-            ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG><<<grid, 128, 0, s>>>(fp);
-            ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-                p.A, p.initial_state, fp.carry, fp.dsum, p.batch, p.dim, N, p.nchunk);
+            // chunk start states, as the forward's chunked path computes them: the
+            // warp-specialised kernel's aggregate pass where it applies (16-byte
+            // rows and bases, which the TMA-staged sweep needs too; chunk lengths
+            // are multiples of its 16-step tile), else the general kernel's
+            bool done = false;
+            if constexpr (N == 16) {
+                if (tma && ws_path(desc) && tiled_shape_ok(desc)) {
+                    const cudaError_t e = launch_ws<IO>(desc, fp, s, true);
+                    if (e != cudaSuccess) return e;
+                    done = true;
+                }
+            }
+            if (!done) {
+                ssm::scan_generic_kernel<IO, N, ssm::MODE_AGG><<<grid, 128, 0, s>>>(fp);
+                ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+                    p.A, p.initial_state, fp.carry, fp.dsum, p.batch, p.dim, N, p.nchunk);
+            }
         }
-        ssm::scan_bwd_agg_kernel<IO, N><<<grid, 128, 0, s>>>(p);
+        const dim3 agrid((unsigned)((p.dim * ssm::BwdShape<N>::LPC + 127) / 128), (unsigned)p.batch,
+                         (unsigned)(p.nchunk - 1));
+        ssm::scan_bwd_agg_kernel<IO, N><<<agrid, 128, 0, s>>>(p);
         ssm::scan_bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
             p.A, p.dlast, p.ebuf, p.bdsum, p.batch, p.dim, N, p.nchunk);
     }
@@ -1351,17 +1372,17 @@ cudaError_t launch_bwd(const BwdPlan& pl, ssm::BwdParams p, const ScanParams& fp
 }
 
 template <typename IO>
-cudaError_t dispatch_bwd(int64_t n, const BwdPlan& pl, const ssm::BwdParams& p, const ScanParams& fp,
+cudaError_t dispatch_bwd(const ssm_scan_desc* desc, int64_t n, const BwdPlan& pl, const ssm::BwdParams& p, const ScanParams& fp,
                          float* dB, float* dC, float* dA, float* dD, float* dbias, bool tma,
                          cudaStream_t s) {
     switch (n) {
-        case 1: return launch_bwd<IO, 1>(pl, p, fp, dB, dC, dA, dD, dbias, false, s);
-        case 2: return launch_bwd<IO, 2>(pl, p, fp, dB, dC, dA, dD, dbias, false, s);
-        case 4: return launch_bwd<IO, 4>(pl, p, fp, dB, dC, dA, dD, dbias, false, s);
-        case 8: return launch_bwd<IO, 8>(pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
-        case 16: return launch_bwd<IO, 16>(pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
-        case 32: return launch_bwd<IO, 32>(pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
-        case 64: return launch_bwd<IO, 64>(pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
+        case 1: return launch_bwd<IO, 1>(desc, pl, p, fp, dB, dC, dA, dD, dbias, false, s);
+        case 2: return launch_bwd<IO, 2>(desc, pl, p, fp, dB, dC, dA, dD, dbias, false, s);
+        case 4: return launch_bwd<IO, 4>(desc, pl, p, fp, dB, dC, dA, dD, dbias, false, s);
+        case 8: return launch_bwd<IO, 8>(desc, pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
+        case 16: return launch_bwd<IO, 16>(desc, pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
+        case 32: return launch_bwd<IO, 32>(desc, pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
+        case 64: return launch_bwd<IO, 64>(desc, pl, p, fp, dB, dC, dA, dD, dbias, tma, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -1507,8 +1528,8 @@ ssm_status ssm_scan_bwd_ex(const ssm_scan_desc* desc, const void* x, const void*
 
     const bool tma = bwd_tma_ok(desc, {x, delta, B, C, z, dout, dx, ddelta, dz});
     const cudaError_t e = desc->io_dtype == SSM_DTYPE_F32
-        ? dispatch_bwd<float>(N, pl, p, fp, dB, dC, dA, dD, ddelta_bias, tma, s)
-        : dispatch_bwd<__nv_bfloat16>(N, pl, p, fp, dB, dC, dA, dD, ddelta_bias, tma, s);
+        ? dispatch_bwd<float>(desc, N, pl, p, fp, dB, dC, dA, dD, ddelta_bias, tma, s)
+        : dispatch_bwd<__nv_bfloat16>(desc, N, pl, p, fp, dB, dC, dA, dD, ddelta_bias, tma, s);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 

@@ -124,6 +124,19 @@ def test_bwd_chunked_long_sequence(cuda, io):
     check_bwd(w, cuda)
 
 
+@pytest.mark.parametrize("n,dim", [(1, 40), (2, 40), (4, 40), (8, 40), (32, 40), (64, 40),
+                                   (16, 36)])
+def test_bwd_chunked_dstates(cuda, n, dim):
+    """The chunked path (aggregate passes and carries) for every dstate; dim 36
+    in bf16 gives rows that are not 16-byte multiples (register sweep and the
+    general kernel's forward aggregate)."""
+    w = synth.ScanWorkload(f"bwd-chunked-n{n}-d{dim}", 1, 3000, dim, n, "bf16" if dim == 36 else "f32",
+                           300 + n, dt_lo=1e-3, dt_hi=2e-2, init_state=True)
+    d = binding.make_desc(w.batch, w.seqlen, w.dim, w.dstate, synth.io_dtype(w.io))
+    assert binding.ssm_scan_bwd_plan(d).nchunk > 1
+    check_bwd(w, cuda)
+
+
 def test_bwd_empty_sequence(cuda):
     w = dataclasses.replace(SMALL, seqlen=0)
     inp, dout, dl = make_case(w)
