@@ -176,20 +176,26 @@ __device__ __forceinline__ float sigmoid_fast(float u) {
 
 // ---------------------------------------------------------------------------
 // 2. Backward aggregate of chunk k >= 1: E_k with nothing from the right.
-// LPC lanes per channel, SPL states per lane (the sweep's layout).  Steps go
-// in groups of LPC from the chunk's end: lane j of a channel evaluates the
-// per-token values (Delta, dyc) of step t - j, and the group's values reach
-// the channel's other lanes by shuffle, so each is computed once.  Delta and
-// dyc use the sweep's formulas.
+// LPC lanes per channel, SPL states per lane (the sweep's layout).  The chunk
+// is walked from its end in groups of kAggGS steps: the CTA stages the
+// group's C rows (shared by its channels) in fp32 shared memory (two
+// buffers, one barrier per group), and lane j of a channel evaluates the
+// per-token values (Delta, dyc) of steps t - j, t - j - LPC, ..., all loads
+// of the group issued together; the values reach the channel's other lanes by
+// shuffle.  Delta and dyc use the sweep's formulas.
+constexpr int kAggGS = 32;
+constexpr int kAggThreads = 128;
+
 template <typename IO, int N>
-__global__ void __launch_bounds__(128) scan_bwd_agg_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kAggThreads) scan_bwd_agg_kernel(BwdParams p) {
     using S = BwdShape<N>;
-    constexpr int LPC = S::LPC, SPL = S::SPL;
+    constexpr int LPC = S::LPC, SPL = S::SPL, GS = kAggGS, R = GS / LPC;
+    __shared__ __align__(16) float cs[2][GS][N];
     const int64_t lin = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t d_raw = lin / LPC;
     const int sub = (int)(lin % LPC);
     const bool valid = d_raw < p.dim;
-    const int64_t d = valid ? d_raw : 0;        // idle lanes stay for the shuffles
+    const int64_t d = valid ? d_raw : 0;        // idle lanes stay for the shuffles and barriers
     const int base = (int)(threadIdx.x & 31) - sub;
     const int n0 = sub * SPL;
     const int64_t b = blockIdx.y;
@@ -209,28 +215,41 @@ __global__ void __launch_bounds__(128) scan_bwd_agg_kernel(BwdParams p) {
     }
     const float bias = p.delta_bias ? __ldg(p.delta_bias + d) : 0.f;
     float dsum = 0.f;
-    for (int64_t tg = t1 - 1; tg >= t0; tg -= LPC) {
-        const int64_t tm = tg - sub;
-        float dt_m = 0.f, dyc_m = 0.f;
-        if (tm >= t0) {
-            const int64_t tok = (b * p.seqlen + tm) * p.dim + d;
-            const float u = load_f32(delta + tok) + bias;
-            dt_m = p.softplus ? softplus_tiled<IO>(u) : u;
-            dyc_m = load_f32(dout + tok);
-            if (z) {
-                const float zv = load_f32(z + tok);
-                dyc_m *= zv * sigmoid_fast(zv);
-            }
+    int buf = 0;
+    for (int64_t tg = t1 - 1; tg >= t0; tg -= GS, buf ^= 1) {
+        // the group's C rows, row j = step tg - j (zero before the chunk)
+        for (int e = threadIdx.x; e < GS * N; e += kAggThreads) {
+            const int64_t t = tg - e / N;
+            cs[buf][e / N][e % N] = t >= t0 ? load_f32(Cm + (b * p.seqlen + t) * N + e % N) : 0.f;
         }
-        dsum += dt_m;
+        // this lane's steps of the group: raw loads first, then the formulas
+        float u[R], dy[R], zz[R];
 #pragma unroll
-        for (int j = 0; j < LPC; ++j) {
-            const float dt = __shfl_sync(0xffffffffu, dt_m, base + j);
-            const float dyc = __shfl_sync(0xffffffffu, dyc_m, base + j);
-            const int64_t t = tg - j;
-            if (t >= t0) {   // the same for every lane of the warp
+        for (int r = 0; r < R; ++r) {
+            const int64_t tm = tg - sub - LPC * r;
+            const int64_t tok = (b * p.seqlen + (tm >= t0 ? tm : t0)) * p.dim + d;
+            u[r] = load_f32(delta + tok);
+            dy[r] = load_f32(dout + tok);
+            zz[r] = z ? load_f32(z + tok) : 0.f;
+        }
+        float dt_m[R], dyc_m[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const bool in = tg - sub - LPC * r >= t0;
+            const float uu = u[r] + bias;
+            dt_m[r] = in ? (p.softplus ? softplus_tiled<IO>(uu) : uu) : 0.f;
+            dyc_m[r] = in ? (z ? dy[r] * (zz[r] * sigmoid_fast(zz[r])) : dy[r]) : 0.f;
+            dsum += dt_m[r];
+        }
+        __syncthreads();   // cs[buf] is complete (and cs[buf ^ 1] is no longer read)
+#pragma unroll
+        for (int j = 0; j < GS; ++j) {
+            const float dt = __shfl_sync(0xffffffffu, dt_m[j / LPC], base + j % LPC);
+            const float dyc = __shfl_sync(0xffffffffu, dyc_m[j / LPC], base + j % LPC);
+            if (tg - j >= t0) {   // the same for every thread of the CTA
                 float cv[SPL];
-                bwd_load<SPL>(Cm + (b * p.seqlen + t) * N + n0, cv, p.vec);
+#pragma unroll
+                for (int q = 0; q < SPL; ++q) cv[q] = cs[buf][j][n0 + q];
 #pragma unroll
                 for (int q = 0; q < SPL; ++q) {
                     const float g = fmaf(dyc, cv[q], G[q]);

@@ -1349,9 +1349,10 @@ cudaError_t launch_bwd(const ssm_scan_desc* desc, const BwdPlan& pl, ssm::BwdPar
                     p.A, p.initial_state, fp.carry, fp.dsum, p.batch, p.dim, N, p.nchunk);
             }
         }
-        const dim3 agrid((unsigned)((p.dim * ssm::BwdShape<N>::LPC + 127) / 128), (unsigned)p.batch,
+        const int at = ssm::kAggThreads;
+        const dim3 agrid((unsigned)((p.dim * ssm::BwdShape<N>::LPC + at - 1) / at), (unsigned)p.batch,
                          (unsigned)(p.nchunk - 1));
-        ssm::scan_bwd_agg_kernel<IO, N><<<agrid, 128, 0, s>>>(p);
+        ssm::scan_bwd_agg_kernel<IO, N><<<agrid, at, 0, s>>>(p);
         ssm::scan_bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
             p.A, p.dlast, p.ebuf, p.bdsum, p.batch, p.dim, N, p.nchunk);
     }
