@@ -294,10 +294,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // already on tile j + 1.
 //   warp 0 lane 0: TMA producer (stage ring continues across tiles)
 //   warp 1 lane 0: MMA issuer; acc_full[a] <- commit, waits acc_empty[a]
-//   warps 2..5   : epilogue; warp w reads TMEM lanes 32 (w % 4) ..; rows go
-//                  through a padded shared-memory tile and leave as whole
-//                  rows (coalesced), then acc_empty[a] is released.
-constexpr int kGemmPThreads = 192;
+//   warps 2..9   : epilogue; warp w reads TMEM lanes 32 (w % 4) .. and half
+//                  of the tile's columns (two warps per lane quarter: the
+//                  epilogue, not the MMA, bounds this output-heavy GEMM, and
+//                  8 warps beat 4 and 16, measured); rows go through a
+//                  padded shared-memory tile and leave as whole row pieces
+//                  (coalesced), then acc_empty[a] is released.
+#ifndef SSM_GP_EPI
+#define SSM_GP_EPI 8
+#endif
+constexpr int kGemmPEpi = SSM_GP_EPI;
+static_assert(kGemmPEpi % 4 == 0, "whole lane quarters");
+constexpr int kGemmPThreads = 64 + 32 * kGemmPEpi;
 
 template <int BN, int STAGES>
 struct GemmPCfg {
@@ -342,7 +350,7 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 128);
+            mbar_init(&acc_empty[a], 32 * kGemmPEpi);
         }
         *fail = 0;
         fence_barrier_init();
@@ -413,6 +421,9 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
     } else if (warp >= 2) {
         // ---- epilogue
         const int q = warp & 3;                               // TMEM lane quarter of this warp
+        constexpr int HALVES = kGemmPEpi / 4;                 // warps per lane quarter
+        constexpr int CW = BN / HALVES;                       // columns of this warp
+        const int c0 = ((warp - 2) / 4) * CW;
         unsigned char* outrow = smem + Cfg::OFF_OUT + (q * 32 + lane) * Cfg::ROWB;
         __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.seg[0].ptr);
         const int64_t ld = p.seg[0].ld;
@@ -428,21 +439,21 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * Cfg::ACC_COLS);
             const int n0e = (t / mtiles) * BN;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
-                float v[16];
-                tmem_ld16(base + (uint32_t)c, v);
+            for (int c = c0; c < c0 + CW; c += 16) {
+                float vv[16];
+                tmem_ld16(base + (uint32_t)c, vv);
                 if (p.col_bias || p.act) {   // the step Delta = softplus(c + bias), finished here
 #pragma unroll
                     for (int k2 = 0; k2 < 16; ++k2) {
                         const int col = n0e + c + k2;
-                        float u = v[k2] + ((p.col_bias && col < p.N) ? __ldg(p.col_bias + col) : 0.f);
-                        v[k2] = p.act ? softplus_tiled<__nv_bfloat16>(u) : u;
+                        float u = vv[k2] + ((p.col_bias && col < p.N) ? __ldg(p.col_bias + col) : 0.f);
+                        vv[k2] = p.act ? softplus_tiled<__nv_bfloat16>(u) : u;
                     }
                 }
                 uint32_t w[8];
 #pragma unroll
                 for (int k2 = 0; k2 < 8; ++k2) {
-                    __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * k2], v[2 * k2 + 1]);
+                    __nv_bfloat162 pr = __floats2bfloat162_rn(vv[2 * k2], vv[2 * k2 + 1]);
                     w[k2] = *reinterpret_cast<uint32_t*>(&pr);
                 }
                 reinterpret_cast<uint4*>(outrow + c * 2)[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -451,20 +462,21 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
             tc_fence_before();
             mbar_arrive(&acc_empty[a]);   // TMEM buffer a may be overwritten now
             __syncwarp();
-            // the warp's 32 rows leave as whole rows: lane l writes 16 bytes of a row
+            // the warp's 32 rows leave as whole pieces of CW columns: lane l writes 16 bytes
             const int64_t m0 = (int64_t)(t % mtiles) * kGemmBM;
             const int n0 = (t / mtiles) * BN;
-            constexpr int CH16 = BN * 2 / 16;                 // 16-byte chunks per row
+            constexpr int CH16 = CW * 2 / 16;                 // 16-byte chunks per row piece
             constexpr int RPI = 32 / CH16 > 0 ? 32 / CH16 : 1;   // rows per warp instruction
+#pragma unroll 4
             for (int r0 = 0; r0 < 32; r0 += RPI) {
                 const int r = r0 + lane / CH16;
                 const int ch = lane % CH16;
                 if (lane / CH16 >= RPI) continue;
                 const int64_t row = m0 + q * 32 + r;
-                const int col = n0 + ch * 8;
+                const int col = n0 + c0 + ch * 8;
                 if (row >= p.M || col >= p.N) continue;
                 const uint4 val = *reinterpret_cast<const uint4*>(
-                    smem + Cfg::OFF_OUT + (q * 32 + r) * Cfg::ROWB + ch * 16);
+                    smem + Cfg::OFF_OUT + (q * 32 + r) * Cfg::ROWB + (c0 + ch * 8) * 2);
                 __nv_bfloat16* dst = C + row * ld + col;
                 if (col + 8 <= p.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
                     *reinterpret_cast<uint4*>(dst) = val;

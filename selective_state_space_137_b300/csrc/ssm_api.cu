@@ -1010,6 +1010,7 @@ cudaError_t launch_gemm_persistent(const void* A, const void* Bw, int64_t M, int
     if (e != cudaSuccess) return e;
     int per_sm = (228 * 1024) / (Cfg::SMEM + 1024);
     if (per_sm > 512 / Cfg::TMEM_COLS) per_sm = 512 / Cfg::TMEM_COLS;
+    if (per_sm > 2048 / ssm::kGemmPThreads) per_sm = 2048 / ssm::kGemmPThreads;
     if (per_sm < 1) per_sm = 1;
     const int64_t tiles = ((M + ssm::kGemmBM - 1) / ssm::kGemmBM) * ((N + BN - 1) / BN);
     if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
