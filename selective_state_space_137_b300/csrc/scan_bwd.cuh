@@ -25,12 +25,14 @@
 //      channel blocks) and dA, dD, dbias (sums over sequences and chunks).
 // Every sum is formed in a fixed order: the result does not depend on timing.
 //
-// Thread layout of scan_bwd_kernel: LPC lanes per channel, SPL states per lane
-// (N = 16: 4 x 4), CPW channels per warp, 8 warps (CH channels) per CTA.  The
-// per-step dB/dC contributions are summed over the warp's channels by
-// recursive halving (each round a lane keeps half of its values and adds the
-// partner's half), then over the CTA's warps through shared memory at the end
-// of each tile.
+// Thread layout of the sweeps: LPC lanes per channel, SPL states per lane
+// (N = 16: 4 x 4), CPW channels per warp, W warps (CH channels) per CTA, W
+// chosen by the host per shape (8 on the register path).  The per-step dB/dC
+// contributions are summed over the warp's channels -- by recursive halving
+// of shuffles on the register path (each round a lane keeps half of its values
+// and adds the partner's half), through a per-warp shared-memory block in the
+// TMA-staged sweep -- then over the CTA's warps through shared memory at the
+// end of each tile.
 #pragma once
 #include "common.cuh"
 #include "scan_tiled.cuh"   // softplus_tiled, silu_tiled, round_up, load1
