@@ -917,6 +917,22 @@ def run_decode(args, dev, peak, peak_kind):
         torch.cuda.synchronize(dev)
         times.append(e0.elapsed_time(e1))
     cold_ms = float(np.median(times))
+    # the same after the write flush plus a read sweep of another buffer larger
+    # than L2: L2 then holds clean lines, so the step does not also pay for
+    # writing the flush buffer's dirty lines back to HBM
+    sweep = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
+    ctimes_clean = []
+    for s in range(32):
+        flush.fill_(s & 0xFF)
+        sweep.sum(dtype=torch.int64)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one(s)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ctimes_clean.append(e0.elapsed_time(e1))
+    del sweep
+    clean_ms = float(np.median(ctimes_clean))
     by = w.step_bytes()
     # the same step with the width-4 causal conv in front (ssm_conv_state_update):
     # conv state (batch, dim, 3) fp32 read and shifted in place, taps (dim, 4)
@@ -951,6 +967,9 @@ def run_decode(args, dev, peak, peak_kind):
                            else graph_ms),
             "flushed": {"ms_per_step": cold_ms, "gb_per_s": by / (cold_ms * 1e-3) / 1e9,
                         "steps_per_s": 1e3 / cold_ms},
+            "flushed_clean_l2": {"ms_per_step": clean_ms, "gb_per_s": by / (clean_ms * 1e-3) / 1e9,
+                                 "frac": by / (clean_ms * 1e-3) / 1e9 / peak,
+                                 "note": "write flush then a read sweep: no dirty lines to write back"},
             "conv_step_flushed": {"ms_per_step": conv_ms,
                                   "gb_per_s": conv_by / (conv_ms * 1e-3) / 1e9,
                                   "algorithmic_bytes": conv_by, "width": K},
