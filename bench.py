@@ -288,6 +288,33 @@ def time_oracle(inp, w, target_s):
     return w.seqlen * nchan * nseq / dt, dt, nchan, nseq, cores
 
 
+def time_oracle_single(inp, w, target_s):
+    """The oracle on one host thread, on channels of sequence 0 sized for about
+    target_s seconds; returns (elements/s, channels)."""
+    import oracle
+    oracle.load()
+    probe = min(w.dim, 8)
+    s = oracle_sample_inputs(inp, w, probe)
+    t = time.perf_counter()
+    oracle.scan_fwd(**s, nthreads=1)
+    per_chan = max(time.perf_counter() - t, 1e-6) / probe
+    nchan = int(min(w.dim, max(probe, target_s / per_chan)))
+    s = oracle_sample_inputs(inp, w, nchan)
+    t = time.perf_counter()
+    oracle.scan_fwd(**s, nthreads=1)
+    return w.seqlen * nchan / (time.perf_counter() - t), nchan
+
+
+def cpu_model():
+    try:
+        for l in open("/proc/cpuinfo"):
+            if l.startswith("model name"):
+                return l.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, world, rank):
     """The reference arm: the fp64 oracle as it stands, on the host cores, each
@@ -451,7 +478,12 @@ def run_ours(args, world, rank, local):
         line["cpu_baseline"] = {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"sequences 0..{nseq - 1} of {w.batch}, channels "
                                           f"0..{nchan - 1} of {w.dim}, all {w.seqlen} tokens "
-                                          f"({dt:.1f} s wall)"}
+                                          f"({dt:.1f} s wall)",
+                                "cpu_model": cpu_model()}
+        st_val, st_chan = time_oracle_single(inp, w, 2.0)
+        line["cpu_baseline"]["single_thread"] = {
+            "value": st_val, "unit": UNIT, "cores": 1,
+            "sample": f"sequence 0, channels 0..{st_chan - 1}, all {w.seqlen} tokens"}
     elif rank == 0:
         line["cpu_baseline"] = None
     line["source_hash"] = kernel_source_hash()
