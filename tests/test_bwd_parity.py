@@ -171,17 +171,27 @@ def test_bwd_full_channel_sums_medium(cuda):
     check_bwd(synth.ScanWorkload("bwd-medium", 2, 1024, 512, 16, "bf16", 13, init_state=True), cuda)
 
 
-def test_bwd_full_size_sampled_channels(cuda):
-    """The Mamba-1.4B layer (4 x 8192 x 4096 x 16, bf16): the per-channel
-    gradients (dx, ddelta, dz over all tokens; dA, dD, ddelta_bias) of sampled
-    channels against the oracle run on those channels alone (a channel's own
-    gradients depend only on its own inputs and the shared B, C rows)."""
+@pytest.mark.parametrize("mode", ["recompute", "checkpoints"])
+def test_bwd_full_size_sampled_channels(cuda, mode):
+    """The Mamba-1.4B layer (4 x 8192 x 4096 x 16, bf16), as the bench times it
+    (7 warps per CTA; with the states recomputed, or read from the training
+    forward's checkpoints): the per-channel gradients (dx, ddelta, dz over all
+    tokens; dA, dD, ddelta_bias) of sampled channels against the oracle run on
+    those channels alone (a channel's own gradients depend only on its own
+    inputs and the shared B, C rows).  Channel 4095 lies in the partial last
+    block of 56 channels."""
     w = synth.MAMBA_1P4B
     inp = synth.make_scan_inputs(w, device=str(cuda))
     g = torch.Generator(device=cuda).manual_seed(99)
     dout = torch.randn(inp["x"].shape, generator=g, device=cuda).to(inp["x"].dtype)
+    ck = None
+    if mode == "checkpoints":
+        ck = ops.checkpoint_buffer(inp["x"], inp["A"])
+        ops.scan_fwd(**inp, checkpoints=ck)
+    d = binding.make_desc(w.batch, w.seqlen, w.dim, w.dstate, inp["x"].dtype)
+    assert binding.ssm_scan_bwd_plan(d, ck is not None).warps == 7
     got = ops.scan_bwd(inp["x"], inp["delta"], inp["A"], inp["B"], inp["C"], dout, D=inp["D"],
-                       z=inp["z"], delta_bias=inp["delta_bias"])
+                       z=inp["z"], delta_bias=inp["delta_bias"], checkpoints=ck)
     torch.cuda.synchronize()
     ds = [0, 1, 2047, 4095]
     idx = torch.tensor(ds, device=cuda)
