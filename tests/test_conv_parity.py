@@ -293,3 +293,76 @@ def test_conv_decode_continues_prefill(cuda):
     assert rel_err(f64(y), f64(full[:, 64])) <= tol
     assert rel_err(f64(last), f64(full_last)) <= tol
     assert torch.equal(cst, full_cst)
+
+
+# ------------------------------------------------------------ full size, sampled
+
+def test_conv_full_size_sampled(cuda):
+    """The Mamba-1.4B layer (4 x 8192 x 4096, bf16) with the width-4 conv and
+    the inputs the benchmark draws: the standalone conv (TMA-streamed) and the
+    fused conv + scan, on sampled channels of sampled sequences (all 8192
+    tokens), against the oracle conv and scan run on those channels alone."""
+    from parity import sample_channels
+    w = synth.MAMBA_1P4B
+    inp = synth.make_scan_inputs(w, device=str(cuda))
+    conv = synth.make_conv_inputs(w.batch, w.dim, 4, seed=w.seed + 500, device=str(cuda))
+    xc, cst = ops.conv1d_fwd(inp["x"], conv["conv_w"], conv["conv_bias"], None)
+    out, last, cst2 = ops.conv_scan_fwd(inp["x"], conv["conv_w"], inp["delta"], inp["A"], inp["B"],
+                                        inp["C"], D=inp["D"], z=inp["z"],
+                                        delta_bias=inp["delta_bias"], conv_bias=conv["conv_bias"])
+    torch.cuda.synchronize()
+    tol = TOL[inp["x"].dtype]
+    for b, ds in sample_channels(w.batch, w.dim):
+        idx = torch.tensor(ds, device=cuda)
+        tok = lambda t: f64(t[b].index_select(-1, idx))[None]       # (1, L, nd)
+        par = lambda t: f64(t.index_select(0, idx))
+        ref_xc, ref_cst = oracle.conv1d_fwd(tok(inp["x"]), par(conv["conv_w"]),
+                                            par(conv["conv_bias"]), None, True)
+        assert rel_err(tok(xc), ref_xc) <= tol, (b, ds)
+        assert np.array_equal(f64(cst[b].index_select(0, idx))[None], ref_cst), (b, ds)
+        ref_out, ref_last = oracle.scan_fwd(ref_xc, tok(inp["delta"]), par(inp["A"]),
+                                            f64(inp["B"][b])[None], f64(inp["C"][b])[None],
+                                            D=par(inp["D"]), z=tok(inp["z"]),
+                                            delta_bias=par(inp["delta_bias"]))
+        assert rel_err(tok(out), ref_out) <= tol, (b, ds, rel_err(tok(out), ref_out))
+        assert rel_err(f64(last[b].index_select(0, idx))[None], ref_last) <= tol, (b, ds)
+        assert np.array_equal(f64(cst2[b].index_select(0, idx))[None], ref_cst), (b, ds)
+
+
+def test_conv_decode_full_size_sampled(cuda):
+    """The decode shape (256 sequences x 5120 channels, dstate 16, bf16) with
+    the width-4 conv in front, as the benchmark times it (the compile-time
+    width kernel): 4 chained steps, sampled channels against the oracle's conv
+    step and decode step run on those channels alone."""
+    from parity import sample_channels
+    w = synth.DECODE
+    inp = synth.make_decode_inputs(w, device=str(cuda))
+    conv = synth.make_conv_inputs(w.batch, w.dim, 4, seed=w.seed + 3, device=str(cuda),
+                                  with_state=True)
+    state, cstate = inp["state"].clone(), conv["conv_state"].clone()
+    samples = sample_channels(w.batch, w.dim)
+    refs = {}
+    for b, ds in samples:
+        idx = torch.tensor(ds, device=cuda)
+        refs[b] = (f64(inp["state"][b].index_select(0, idx))[None],
+                   f64(conv["conv_state"][b].index_select(0, idx))[None])
+    tol = TOL[inp["x"].dtype]
+    for s in range(4):
+        out = ops.conv_state_update(cstate, conv["conv_w"], state, inp["x"][s], inp["delta"][s],
+                                    inp["A"], inp["B"][s], inp["C"][s], D=inp["D"], z=inp["z"][s],
+                                    delta_bias=inp["delta_bias"], conv_bias=conv["conv_bias"])
+        torch.cuda.synchronize()
+        for b, ds in samples:
+            idx = torch.tensor(ds, device=cuda)
+            par = lambda t: f64(t.index_select(0, idx))
+            row = lambda t: f64(t[s][b].index_select(0, idx))[None]    # (1, nd)
+            ref_h, ref_c = refs[b]
+            xc, ref_c = oracle.conv1d_fwd(row(inp["x"])[:, None, :], par(conv["conv_w"]),
+                                          par(conv["conv_bias"]), ref_c, True)
+            ref_out, ref_h = oracle.state_update(ref_h, xc[:, 0, :], row(inp["delta"]), par(inp["A"]),
+                                                 f64(inp["B"][s][b])[None], f64(inp["C"][s][b])[None],
+                                                 par(inp["D"]), row(inp["z"]), par(inp["delta_bias"]))
+            refs[b] = (ref_h, ref_c)
+            assert rel_err(f64(out[b].index_select(0, idx))[None], ref_out) <= tol, (s, b, ds)
+            assert rel_err(f64(state[b].index_select(0, idx))[None], ref_h) <= tol, (s, b, ds)
+            assert np.array_equal(f64(cstate[b].index_select(0, idx))[None], ref_c), (s, b, ds)

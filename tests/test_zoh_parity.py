@@ -115,3 +115,25 @@ def test_euler_option_equals_plain_call(cuda):
                                  last, inp["initial_state"], ws, ws.numel())
     torch.cuda.synchronize()
     assert st == binding.SSM_OK and torch.equal(out, a) and torch.equal(last, la)
+
+
+def test_zoh_full_size_sampled(cuda):
+    """The Mamba-1.4B layer (4 x 8192 x 4096 x 16, bf16) with exact ZOH, as the
+    benchmark times it: every output of sampled channels and their final
+    states against the oracle's ZOH scan on those channels alone."""
+    from parity import sample_channels
+    w = synth.MAMBA_1P4B
+    inp = synth.make_scan_inputs(w, device=str(cuda))
+    out, last = ops.scan_fwd(**inp, discretization="zoh")
+    torch.cuda.synchronize()
+    tol = TOL[inp["x"].dtype]
+    for b, ds in sample_channels(w.batch, w.dim):
+        idx = torch.tensor(ds, device=cuda)
+        tok = lambda t: f64(t[b].index_select(-1, idx))[None]
+        par = lambda t: f64(t.index_select(0, idx))
+        ref, ref_last = oracle.scan_fwd(tok(inp["x"]), tok(inp["delta"]), par(inp["A"]),
+                                        f64(inp["B"][b])[None], f64(inp["C"][b])[None],
+                                        D=par(inp["D"]), z=tok(inp["z"]),
+                                        delta_bias=par(inp["delta_bias"]), zoh=True)
+        assert rel_err(tok(out), ref) <= tol, (b, ds, rel_err(tok(out), ref))
+        assert rel_err(f64(last[b].index_select(0, idx))[None], ref_last) <= tol, (b, ds)
