@@ -53,3 +53,20 @@ def test_host_pipeline_long_sequences_chunked(cuda):
     ref, ref_last = oracle_full(inp)
     assert rel_err(f64(out), ref) <= TOL[torch.bfloat16]
     assert rel_err(f64(last), ref_last) <= TOL[torch.bfloat16]
+
+
+def test_host_pipeline_full_size_sampled(cuda):
+    """The Mamba-1.4B layer (4 x 8192 x 4096 x 16, bf16) from pinned host
+    memory, as the benchmark's end-to-end figure runs it (slices of one
+    sequence): sampled channels of every sampled sequence (all 8192 tokens)
+    and their final states against the oracle."""
+    from parity import oracle_sampled, sample_channels
+    w = synth.MAMBA_1P4B
+    inp = synth.make_scan_inputs(w, device=str(cuda))
+    host = {k: (None if v is None else v.cpu()) for k, v in inp.items()}
+    out, last = run_host(host, cuda, 0)
+    tol = TOL[inp["x"].dtype]
+    for b, (ds, ref, ref_last) in oracle_sampled(inp, sample_channels(w.batch, w.dim)).items():
+        idx = torch.tensor(ds)
+        assert rel_err(f64(out[b].index_select(-1, idx)), ref) <= tol, (b, ds)
+        assert rel_err(f64(last[b].index_select(0, idx)), ref_last) <= tol, (b, ds)

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from parity import TOL, f64, rel_err
-from selective_state_space_137_b300 import ops
+from selective_state_space_137_b300 import ops, synth
 
 pytestmark = pytest.mark.gpu
 
@@ -74,3 +74,30 @@ def test_lti_conv_mode_equals_recurrence(cuda):
     y_rec, _ = ops.scan_fwd(x, dl, t(A), Bs, Cs, delta_softplus=False)
     torch.cuda.synchronize()
     assert rel_err(f64(y_conv), f64(y_rec)) <= 1e-4
+
+
+def test_lti_full_size_sampled(cuda):
+    """The Mamba-130M layer (8 x 2048 x 1536, N = 16) in convolution mode with
+    the inputs the benchmark draws: the kernel K of sampled channels against
+    the oracle's closed form, and y = K * x on those channels against the
+    oracle's convolution with the same fp32 K."""
+    from parity import sample_channels
+    w = synth.MAMBA_130M
+    g = torch.Generator(device=cuda).manual_seed(5)
+    N = w.dstate
+    delta = 0.001 + 0.1 * torch.rand(w.dim, generator=g, device=cuda)
+    A = -torch.arange(1, N + 1, device=cuda, dtype=torch.float32).repeat(w.dim, 1).contiguous()
+    Bv = torch.randn(N, generator=g, device=cuda)
+    Cv = torch.randn(N, generator=g, device=cuda)
+    Bp, Cp = Bv.repeat(w.dim, 1).contiguous(), Cv.repeat(w.dim, 1).contiguous()
+    x = torch.randn((w.batch, w.seqlen, w.dim), generator=g, device=cuda).to(torch.bfloat16)
+    K = ops.lti_kernel(delta, A, Bp, Cp, w.seqlen)
+    y = ops.lti_conv_fwd(K, x)
+    torch.cuda.synchronize()
+    for b, ds in sample_channels(w.batch, w.dim):
+        idx = torch.tensor(ds, device=cuda)
+        sel = lambda t: f64(t.index_select(0, idx))
+        Kref = oracle.lti_kernel(sel(delta), sel(A), sel(Bp), sel(Cp), w.seqlen)
+        assert rel_err(sel(K), Kref) <= 1e-4, (b, ds)
+        ref = oracle.lti_conv(sel(K), f64(x[b:b + 1].index_select(-1, idx)))
+        assert rel_err(f64(y[b:b + 1].index_select(-1, idx)), ref) <= TOL[torch.bfloat16], (b, ds)
