@@ -1,8 +1,8 @@
 // scan_ws.cuh -- warp-specialised selective scan (path 2; bf16 or fp32 I/O,
-// dstate 16).
+// dstate 8, 16 or 32).
 //
 // A CTA owns 16 channels of one sequence and three warps:
-//   warp 0, scan: lane (c, s) = (lane % 16, lane / 16) keeps states [8s, 8s+8)
+//   warp 0, scan: lane (c, s) = (lane % 16, lane / 16) keeps states [N/2 s, N/2 (s+1))
 //     of channel c in registers and runs, step after step,
 //       dA = 2^(Delta * A[n] log2 e)   h = dA h + (Delta x) B[n]   y_s = sum C[n] h
 //     with f32x2 arithmetic.  It never meets a block-wide barrier: per tile
@@ -41,12 +41,20 @@
 #ifndef SSM_WS_MINBLOCKS
 #define SSM_WS_MINBLOCKS 7   // resident CTAs per SM the register budget must allow
 #endif
+#ifndef SSM_WS_MINBLOCKS32
+#define SSM_WS_MINBLOCKS32 6
+#endif
 
 namespace ssm {
 
-template <typename IO, int T_, int S_, int R_, int CK_ = 0>
+// N_: dstate (8, 16 or 32); a lane keeps N/2 states of one channel.
+template <typename IO, int T_, int S_, int R_, int CK_ = 0, int N_ = 16>
 struct WsCfg {
-    static constexpr int N = 16, DC = 16, KS = 2, NS = 8, T = T_, S = S_, R = R_;
+    static constexpr int N = N_, DC = 16, KS = 2, NS = N / KS, T = T_, S = S_, R = R_;
+    static_assert(N == 8 || N == 16 || N == 32, "dstate 8, 16 or 32");
+    // resident CTAs per SM the register budget must allow (16 states per lane
+    // at dstate 32 need more registers)
+    static constexpr int MINB = N == 32 ? SSM_WS_MINBLOCKS32 : SSM_WS_MINBLOCKS;
     static constexpr int CK = CK_;               // causal conv width in front (0: none)
     static constexpr bool CONV = CK > 0;
     static constexpr int HALO = CONV ? CK - 1 : 0;   // raw x rows before the tile
@@ -78,7 +86,7 @@ struct WsCfg {
 // ZOH: the exact zero-order-hold input term ((exp(Delta A) - 1) / A) B x; the
 // pre-pass then hands over (Delta, x) instead of (Delta, Delta x).
 template <typename IO, typename Cfg, int MODE, bool ZOH = false>
-__global__ void __launch_bounds__(96, SSM_WS_MINBLOCKS)
+__global__ void __launch_bounds__(96, Cfg::MINB)
     scan_ws_kernel(const __grid_constant__ TiledMaps maps, const ScanParams p) {
     constexpr int N = Cfg::N, NS = Cfg::NS, DC = Cfg::DC, T = Cfg::T, S = Cfg::S, R = Cfg::R;
     constexpr bool FULL = (MODE == MODE_FULL);

@@ -199,20 +199,28 @@ TiledShape tiled_shape_io(int64_t n) {
 #ifndef SSM_WS_SLOTS
 #define SSM_WS_SLOTS 2       // helper <-> scan hand-over slots
 #endif
-template <typename IO, int CK = 0>
-using WsConfig = ssm::WsCfg<IO, SSM_WS_T, SSM_WS_STAGES, SSM_WS_SLOTS, CK>;
+template <typename IO, int CK = 0, int N = 16>
+using WsConfig = ssm::WsCfg<IO, SSM_WS_T, SSM_WS_STAGES, SSM_WS_SLOTS, CK, N>;
 // Conv widths fused into the warp-specialised kernel (compile-time width);
 // wider convs take the generic kernel.
 constexpr int kWsMaxConvWidth = 4;
 
-bool ws_path(const ssm_scan_desc* d) { return SSM_USE_WS && d->dstate == 16; }
+bool ws_path(const ssm_scan_desc* d) {
+    return SSM_USE_WS && (d->dstate == 8 || d->dstate == 16 || d->dstate == 32);
+}
+
+template <typename IO>
+TiledShape ws_shape(int64_t n) {
+    switch (n) {
+        case 8: return TiledShape{WsConfig<IO, 0, 8>::DC, WsConfig<IO, 0, 8>::THREADS, WsConfig<IO, 0, 8>::SMEM};
+        case 32: return TiledShape{WsConfig<IO, 0, 32>::DC, WsConfig<IO, 0, 32>::THREADS, WsConfig<IO, 0, 32>::SMEM};
+    }
+    return TiledShape{WsConfig<IO>::DC, WsConfig<IO>::THREADS, WsConfig<IO>::SMEM};
+}
 
 TiledShape tiled_shape(const ssm_scan_desc* d) {
     if (ws_path(d))
-        return d->io_dtype == SSM_DTYPE_F32
-                   ? TiledShape{WsConfig<float>::DC, WsConfig<float>::THREADS, WsConfig<float>::SMEM}
-                   : TiledShape{WsConfig<__nv_bfloat16>::DC, WsConfig<__nv_bfloat16>::THREADS,
-                                WsConfig<__nv_bfloat16>::SMEM};
+        return d->io_dtype == SSM_DTYPE_F32 ? ws_shape<float>(d->dstate) : ws_shape<__nv_bfloat16>(d->dstate);
     return d->io_dtype == SSM_DTYPE_F32 ? tiled_shape_io<float>(d->dstate)
                                         : tiled_shape_io<__nv_bfloat16>(d->dstate);
 }
@@ -314,9 +322,9 @@ cudaError_t launch_tiled(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
 
 // agg_only: the chunk aggregates and carries alone (the chunk start states
 // that the backward's recompute needs); out and z are not read.
-template <typename IO, int CK = 0, bool ZOH = false>
-cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s, bool agg_only = false) {
-    using Cfg = WsConfig<IO, CK>;
+template <typename IO, int CK, bool ZOH, int N>
+cudaError_t launch_ws_n(const ssm_scan_desc* d, ScanParams p, cudaStream_t s, bool agg_only) {
+    using Cfg = WsConfig<IO, CK, N>;
     const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int e = (int)sizeof(IO);
@@ -349,6 +357,17 @@ cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s, bool
     if (agg_only) return cudaGetLastError();
     kfull<<<dim3(gx, (unsigned)d->batch, (unsigned)p.nchunk), Cfg::THREADS, Cfg::SMEM, s>>>(maps, p);
     return cudaGetLastError();
+}
+
+// The warp-specialised scan for dstate 8, 16 or 32.
+template <typename IO, int CK = 0, bool ZOH = false>
+cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s, bool agg_only = false) {
+    switch (d->dstate) {
+        case 8: return launch_ws_n<IO, CK, ZOH, 8>(d, p, s, agg_only);
+        case 16: return launch_ws_n<IO, CK, ZOH, 16>(d, p, s, agg_only);
+        case 32: return launch_ws_n<IO, CK, ZOH, 32>(d, p, s, agg_only);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <typename IO>
@@ -1337,7 +1356,7 @@ cudaError_t launch_bwd(const ssm_scan_desc* desc, const BwdPlan& pl, ssm::BwdPar
             // rows and bases, which the TMA-staged sweep needs too; chunk lengths
             // are multiples of its 16-step tile), else the general kernel's
             bool done = false;
-            if constexpr (N == 16) {
+            if constexpr (N == 8 || N == 16 || N == 32) {
                 if (tma && ws_path(desc) && tiled_shape_ok(desc)) {
                     const cudaError_t e = launch_ws<IO>(desc, fp, s, true);
                     if (e != cudaSuccess) return e;
