@@ -387,7 +387,7 @@ SSM_API ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc *desc,
 
 /* How ssm_scan_fwd will execute `desc` (host-side query, no GPU work).
  *   path        : 0 = general kernel (one thread per channel), 1 = tiled B300 kernel,
- *                 2 = warp-specialised tiled kernel (dstate 8, 16 or 32)
+ *                 2 = warp-specialised tiled kernel (dstate 8, 16, 32 or 64)
  *                 (the tiled kernel is used when the io tensors are 16-byte
  *                 aligned; the plan reported assumes they are)
  *   nchunk      : pieces the time axis is cut into (1 = not cut)

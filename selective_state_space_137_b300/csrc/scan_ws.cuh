@@ -1,5 +1,5 @@
 // scan_ws.cuh -- warp-specialised selective scan (path 2; bf16 or fp32 I/O,
-// dstate 8, 16 or 32).
+// dstate 8, 16, 32 or 64).
 //
 // A CTA owns 16 channels of one sequence and three warps:
 //   warp 0, scan: lane (c, s) = (lane % 16, lane / 16) keeps states [N/2 s, N/2 (s+1))
@@ -44,17 +44,20 @@
 #ifndef SSM_WS_MINBLOCKS32
 #define SSM_WS_MINBLOCKS32 6
 #endif
+#ifndef SSM_WS_MINBLOCKS64
+#define SSM_WS_MINBLOCKS64 4
+#endif
 
 namespace ssm {
 
-// N_: dstate (8, 16 or 32); a lane keeps N/2 states of one channel.
+// N_: dstate (8, 16, 32 or 64); a lane keeps N/2 states of one channel.
 template <typename IO, int T_, int S_, int R_, int CK_ = 0, int N_ = 16>
 struct WsCfg {
     static constexpr int N = N_, DC = 16, KS = 2, NS = N / KS, T = T_, S = S_, R = R_;
-    static_assert(N == 8 || N == 16 || N == 32, "dstate 8, 16 or 32");
-    // resident CTAs per SM the register budget must allow (16 states per lane
-    // at dstate 32 need more registers)
-    static constexpr int MINB = N == 32 ? SSM_WS_MINBLOCKS32 : SSM_WS_MINBLOCKS;
+    static_assert(N == 8 || N == 16 || N == 32 || N == 64, "dstate 8, 16, 32 or 64");
+    // resident CTAs per SM the register budget must allow (16 or 32 states per
+    // lane at dstate 32 or 64 need more registers)
+    static constexpr int MINB = N == 64 ? SSM_WS_MINBLOCKS64 : N == 32 ? SSM_WS_MINBLOCKS32 : SSM_WS_MINBLOCKS;
     static constexpr int CK = CK_;               // causal conv width in front (0: none)
     static constexpr bool CONV = CK > 0;
     static constexpr int HALO = CONV ? CK - 1 : 0;   // raw x rows before the tile

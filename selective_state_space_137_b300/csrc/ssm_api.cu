@@ -206,7 +206,7 @@ using WsConfig = ssm::WsCfg<IO, SSM_WS_T, SSM_WS_STAGES, SSM_WS_SLOTS, CK, N>;
 constexpr int kWsMaxConvWidth = 4;
 
 bool ws_path(const ssm_scan_desc* d) {
-    return SSM_USE_WS && (d->dstate == 8 || d->dstate == 16 || d->dstate == 32);
+    return SSM_USE_WS && (d->dstate == 8 || d->dstate == 16 || d->dstate == 32 || d->dstate == 64);
 }
 
 template <typename IO>
@@ -214,6 +214,7 @@ TiledShape ws_shape(int64_t n) {
     switch (n) {
         case 8: return TiledShape{WsConfig<IO, 0, 8>::DC, WsConfig<IO, 0, 8>::THREADS, WsConfig<IO, 0, 8>::SMEM};
         case 32: return TiledShape{WsConfig<IO, 0, 32>::DC, WsConfig<IO, 0, 32>::THREADS, WsConfig<IO, 0, 32>::SMEM};
+        case 64: return TiledShape{WsConfig<IO, 0, 64>::DC, WsConfig<IO, 0, 64>::THREADS, WsConfig<IO, 0, 64>::SMEM};
     }
     return TiledShape{WsConfig<IO>::DC, WsConfig<IO>::THREADS, WsConfig<IO>::SMEM};
 }
@@ -359,13 +360,14 @@ cudaError_t launch_ws_n(const ssm_scan_desc* d, ScanParams p, cudaStream_t s, bo
     return cudaGetLastError();
 }
 
-// The warp-specialised scan for dstate 8, 16 or 32.
+// The warp-specialised scan for dstate 8, 16, 32 or 64.
 template <typename IO, int CK = 0, bool ZOH = false>
 cudaError_t launch_ws(const ssm_scan_desc* d, ScanParams p, cudaStream_t s, bool agg_only = false) {
     switch (d->dstate) {
         case 8: return launch_ws_n<IO, CK, ZOH, 8>(d, p, s, agg_only);
         case 16: return launch_ws_n<IO, CK, ZOH, 16>(d, p, s, agg_only);
         case 32: return launch_ws_n<IO, CK, ZOH, 32>(d, p, s, agg_only);
+        case 64: return launch_ws_n<IO, CK, ZOH, 64>(d, p, s, agg_only);
     }
     return cudaErrorInvalidValue;
 }
@@ -1356,7 +1358,7 @@ cudaError_t launch_bwd(const ssm_scan_desc* desc, const BwdPlan& pl, ssm::BwdPar
             // rows and bases, which the TMA-staged sweep needs too; chunk lengths
             // are multiples of its 16-step tile), else the general kernel's
             bool done = false;
-            if constexpr (N == 8 || N == 16 || N == 32) {
+            if constexpr (N == 8 || N == 16 || N == 32 || N == 64) {
                 if (tma && ws_path(desc) && tiled_shape_ok(desc)) {
                     const cudaError_t e = launch_ws<IO>(desc, fp, s, true);
                     if (e != cudaSuccess) return e;

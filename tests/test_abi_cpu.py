@@ -112,7 +112,7 @@ def test_plan_picks_the_tiled_path(ssm_lib):
     long = L.ssm_scan_plan(L.make_desc(1, 262144, 2048, 16, L.SSM_DTYPE_BF16))
     assert long.path == 2 and long.nchunk > 1 and long.launches == 3 and long.workspace > 0
     assert L.ssm_scan_workspace_size(L.make_desc(1, 262144, 2048, 16, L.SSM_DTYPE_BF16)) >= long.workspace
-    for n, path in ((1, 0), (2, 0), (4, 0), (8, 2), (16, 2), (32, 2), (64, 0)):
+    for n, path in ((1, 0), (2, 0), (4, 0), (8, 2), (16, 2), (32, 2), (64, 2)):
         assert L.ssm_scan_plan(L.make_desc(2, 300, 72, n, L.SSM_DTYPE_BF16)).path == path
     assert L.ssm_scan_plan(L.make_desc(2, 300, 72, 16, L.SSM_DTYPE_F32)).path == 2
     assert L.ssm_scan_plan(L.make_desc(2, 300, 12, 16, L.SSM_DTYPE_BF16)).path == 0   # 24-byte rows
