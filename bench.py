@@ -109,15 +109,16 @@ def peaks():
 # these files when it was captured; its traffic figure is used only while they
 # are unchanged.
 _KERNEL_SOURCES = {
-    "scan_fwd": ("common.cuh", "tma.cuh", "scan_generic.cuh", "scan_tiled.cuh", "scan_ws.cuh",
+    "scan_fwd": ("common.cuh", "tma.cuh", "scan_generic.cuh", "tile_io.cuh", "scan_warp.cuh",
                  "ssm_api.cu"),
-    "conv_scan_fwd": ("common.cuh", "tma.cuh", "scan_generic.cuh", "scan_tiled.cuh",
+    "conv_scan_fwd": ("common.cuh", "tma.cuh", "scan_generic.cuh", "tile_io.cuh",
                       "scan_ws.cuh", "ssm_api.cu"),
-    "state_update": ("common.cuh", "scan_tiled.cuh", "decode.cuh", "ssm_api.cu"),
-    "conv1d_fwd": ("common.cuh", "scan_generic.cuh", "scan_tiled.cuh", "conv.cuh", "ssm_api.cu"),
-    "scan_bwd": ("common.cuh", "tma.cuh", "scan_tiled.cuh", "scan_bwd.cuh", "ssm_api.cu"),
-    "x_proj": ("common.cuh", "tma.cuh", "scan_tiled.cuh", "gemm.cuh", "ssm_api.cu"),
-    "dt_proj": ("common.cuh", "tma.cuh", "scan_tiled.cuh", "gemm.cuh", "ssm_api.cu"),
+    "state_update": ("common.cuh", "tile_io.cuh", "decode.cuh", "ssm_api.cu"),
+    "conv1d_fwd": ("common.cuh", "scan_generic.cuh", "tile_io.cuh", "conv.cuh", "ssm_api.cu"),
+    "scan_bwd": ("common.cuh", "tma.cuh", "tile_io.cuh", "scan_warp.cuh", "scan_bwd.cuh",
+                 "ssm_api.cu"),
+    "x_proj": ("common.cuh", "tma.cuh", "tile_io.cuh", "gemm.cuh", "ssm_api.cu"),
+    "dt_proj": ("common.cuh", "tma.cuh", "tile_io.cuh", "gemm.cuh", "ssm_api.cu"),
 }
 
 
@@ -427,6 +428,9 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(dev)
         time.sleep(0.15)
     barrier(world)
+    # a bounded device wait that gave up leaves its launch incomplete: such a
+    # run is not a measurement (read outside the timed region)
+    require_device_ok(binding, "after the timed scan steps")
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     total_ms = ev[0].elapsed_time(ev[-1])
     total_ms = max_over_ranks(total_ms, world, dev)
@@ -486,9 +490,20 @@ def run_ours(args, world, rank, local):
             "sample": f"sequence 0, channels 0..{st_chan - 1}, all {w.seqlen} tokens"}
     elif rank == 0:
         line["cpu_baseline"] = None
+    require_device_ok(binding, "after the other sections")
+    line["device_status"] = "SSM_OK"
     line["source_hash"] = kernel_source_hash()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def require_device_ok(binding, where):
+    """Refuse to report when any kernel's bounded wait timed out: its outputs
+    are incomplete and its time is not the path's."""
+    st = binding.ssm_get_device_status()
+    if st != binding.SSM_OK:
+        raise SystemExit(f"bench: device error word {binding.ssm_status_string(st)} {where}; "
+                         "no result is printed")
 
 
 def run_e2e(args, w, inp, desc, plan, dev, world, binding):
@@ -736,6 +751,21 @@ def run_proj(args, w, dev, scan_inp=None):
                            "proj_with_softplus_epilogue_ms": _time_calls(proj_sp, dev, steps),
                            "scan_with_softplus_ms": _time_calls(scan_sp, dev, steps),
                            "scan_without_softplus_ms": _time_calls(scan_nosp, dev, steps)}
+        if R in (64, 128) and N == 16:
+            # dt_proj fused into the scan's prologue (ssm_proj_scan_fwd): x_proj,
+            # then the scan forms the raw step itself on the tensor cores
+            dt3 = dt_low.view(w.batch, w.seqlen, R)
+
+            def proj_scan():
+                assert binding.ssm_proj_scan_fwd(sdesc, pd, x3, dt3, inp["W_dt"], scan_inp["A"], B3,
+                                                 C3, scan_inp["D"], scan_inp["z"], bias, out, last,
+                                                 None, ws, ws.numel(), stream) == binding.SSM_OK
+
+            def xproj_then_proj_scan():
+                xonly()
+                proj_scan()
+            res["pipeline"]["dt_proj_fused_in_scan_ms"] = _time_calls(xproj_then_proj_scan, dev, steps)
+            res["pipeline"]["proj_scan_kernel_ms"] = _time_calls(proj_scan, dev, steps)
     return res
 
 

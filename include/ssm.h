@@ -224,6 +224,31 @@ SSM_API ssm_status ssm_selection_proj_fwd(const ssm_scan_desc *desc, const ssm_p
                                           const float *delta_bias, void *dt_low, void *B, void *C,
                                           void *delta, void *stream);
 
+/* The scan with the second selection projection fused in front: for every
+ * token and channel the raw step delta_raw = dt_low W_dt^T (the selection
+ * mechanism of "Mamba的三大创新": Delta computed from the input) is formed
+ * inside the scan, a tile of 16 steps x 16 channels at a time, on the tensor
+ * cores with fp32 accumulation, and never stored; the scan then proceeds as
+ * ssm_scan_fwd with that raw step, softplus and delta_bias.  The pipeline
+ * x_proj -> scan needs no dt_proj launch and no (batch, seqlen, dim) delta
+ * tensor in memory.
+ *   dt_low       (batch, seqlen, R) bf16: the dt_low output of
+ *                ssm_selection_proj_fwd (called with delta = NULL)
+ *   W_dt         (dim, R) bf16
+ *   everything else as ssm_scan_fwd (delta is not an argument).
+ * Supported: bf16 I/O, dstate 16, desc->delta_softplus = 1, R = proj->dt_rank
+ * of 64 or 128, dim a multiple of 8, every tensor 16-byte aligned; otherwise
+ * SSM_ERR_UNSUPPORTED (shape) or SSM_ERR_INVALID_ARG (alignment, NULL).  The
+ * raw step is exact fp32 of the bf16 operands (ssm_selection_proj_fwd rounds
+ * it to bf16), so results differ from the unfused pipeline by that rounding.
+ * Workspace: ssm_scan_workspace_size(desc) bytes. */
+SSM_API ssm_status ssm_proj_scan_fwd(const ssm_scan_desc *desc, const ssm_proj_desc *proj,
+                                     const void *x, const void *dt_low, const void *W_dt,
+                                     const float *A, const void *B, const void *C,
+                                     const float *D, const void *z, const float *delta_bias,
+                                     void *out, float *last_state, const float *initial_state,
+                                     void *workspace, size_t workspace_bytes, void *stream);
+
 /* Gradients of ssm_scan_fwd (the backward half of training; "Mamba的三大创新",
  * stage 2, parallel training of the recurrence).  The states are recomputed
  * from the inputs (stored every 16 steps in the workspace), never kept from
@@ -386,10 +411,12 @@ SSM_API ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc *desc,
                                         const float *initial_state, void *stream);
 
 /* How ssm_scan_fwd will execute `desc` (host-side query, no GPU work).
- *   path        : 0 = general kernel (one thread per channel), 1 = tiled B300 kernel,
- *                 2 = warp-specialised tiled kernel (dstate 8, 16, 32 or 64)
+ *   path        : 0 = general kernel (one thread per channel),
+ *                 3 = tiled kernel of one-warp CTAs (dstate 8, 16, 32 or 64)
  *                 (the tiled kernel is used when the io tensors are 16-byte
- *                 aligned; the plan reported assumes they are)
+ *                 aligned; the plan reported assumes they are).  Value 2 (the
+ *                 warp-specialised kernel) is what the exact-ZOH scan and the
+ *                 fused conv take; value 1 is no longer used.
  *   nchunk      : pieces the time axis is cut into (1 = not cut)
  *   launches    : kernels one ssm_scan_fwd call enqueues
  *   workspace   : bytes of workspace the call needs (= ssm_scan_workspace_size) */
@@ -408,6 +435,17 @@ SSM_API ssm_status ssm_scan_plan(const ssm_scan_desc *desc, ssm_scan_plan_info *
  * outputs are then incomplete), SSM_OK otherwise.  Reading it clears it.
  * Synchronises with the device (it waits for all prior work). */
 SSM_API ssm_status ssm_get_device_status(void);
+
+/* The same status, scoped to one stream: waits only for the work already
+ * enqueued on `stream` (NULL = the legacy default stream, which itself waits
+ * for the device's other blocking streams), then reads and clears the error
+ * word.  SSM_ERR_TIMEOUT if a bounded wait gave up, SSM_OK otherwise,
+ * SSM_ERR_CUDA if the read failed.  The error word is one per device (a
+ * device variable of the library), not one per call: a timeout in one
+ * caller's stream is seen, and cleared, by whichever query reads it first.
+ * `workspace` is accepted for the form of the boundary's plan (the word in a
+ * call's workspace) and is not used; pass NULL or any workspace. */
+SSM_API ssm_status ssm_get_async_status(void *workspace, void *stream);
 
 /* Test hook for the timeout path: launches one warp that waits, for at most
  * `limit_ns` nanoseconds (1e3 .. 5e9), on a shared-memory barrier that nothing

@@ -263,10 +263,20 @@ def selection_proj(x, W_x, W_dt, dt_rank):
     N = N2 // 2
     Bm = xdbl[:, R:R + N]
     Cm = xdbl[:, R + N:]
-    delta = dt_low @ W_dt.T
     shp = (bsz, seqlen)
-    return (dt_low.reshape(*shp, R), Bm.reshape(*shp, N), Cm.reshape(*shp, N),
-            delta.reshape(*shp, dim))
+    dt_low = dt_low.reshape(*shp, R)
+    return dt_low, Bm.reshape(*shp, N), Cm.reshape(*shp, N), dt_proj(dt_low, W_dt)
+
+
+def dt_proj(dt_low, W_dt):
+    """The second selection projection alone: delta_raw = dt_low W_dt^T, the
+    raw step of every token and channel.  dt_low: (batch, seqlen, R); W_dt:
+    (dim, R).  fp64 numpy matmul.  Returns (batch, seqlen, dim)."""
+    dt_low = _f64(dt_low)
+    W_dt = _f64(W_dt)
+    if dt_low.ndim != 3 or W_dt.ndim != 2 or W_dt.shape[1] != dt_low.shape[2]:
+        raise ValueError("dt_low must be (batch, seqlen, R) and W_dt (dim, R)")
+    return dt_low @ W_dt.T
 
 
 def conv1d_fwd(x, w, bias=None, conv_state=None, activation=True, lib=None):

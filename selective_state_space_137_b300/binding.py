@@ -20,10 +20,11 @@ SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 # Every symbol include/ssm.h declares; the CPU tests check the library exports them.
 EXPORTED = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update",
             "ssm_scan_plan", "ssm_status_string", "ssm_version", "ssm_scan_fwd_noalloc",
-            "ssm_get_device_status", "ssm_selftest_wait_timeout", "ssm_conv1d_fwd",
+            "ssm_get_device_status", "ssm_get_async_status", "ssm_selftest_wait_timeout", "ssm_conv1d_fwd",
             "ssm_conv_scan_fwd", "ssm_conv_state_update", "ssm_scan_bwd_workspace_size",
             "ssm_scan_bwd", "ssm_scan_fwd_ex", "ssm_state_update_ex", "ssm_lti_kernel",
-            "ssm_lti_conv_fwd", "ssm_selection_proj_fwd", "ssm_scan_fwd_host_workspace_size",
+            "ssm_lti_conv_fwd", "ssm_selection_proj_fwd", "ssm_proj_scan_fwd",
+            "ssm_scan_fwd_host_workspace_size",
             "ssm_scan_fwd_host", "ssm_scan_checkpoint_size", "ssm_scan_fwd_train",
             "ssm_scan_bwd_ex_workspace_size", "ssm_scan_bwd_ex", "ssm_scan_bwd_plan")
 SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
@@ -88,6 +89,9 @@ def _load():
     lib.ssm_lti_kernel.argtypes = [dp, op, fp, fp, fp, fp, fp, vp]
     lib.ssm_lti_conv_fwd.restype = ctypes.c_int
     lib.ssm_lti_conv_fwd.argtypes = [dp, fp, vp, fp, vp, vp, vp]
+    lib.ssm_proj_scan_fwd.restype = ctypes.c_int
+    lib.ssm_proj_scan_fwd.argtypes = [dp, ctypes.POINTER(ssm_proj_desc), vp, vp, vp, fp, vp, vp, fp,
+                                      vp, fp, vp, fp, fp, vp, sz, vp]
     lib.ssm_selection_proj_fwd.restype = ctypes.c_int
     lib.ssm_selection_proj_fwd.argtypes = [dp, ctypes.POINTER(ssm_proj_desc), vp, vp, vp, fp, vp, vp,
                                            vp, vp, vp]
@@ -127,6 +131,8 @@ def _load():
     lib.ssm_selftest_wait_timeout.argtypes = [ctypes.c_int64, vp]
     lib.ssm_get_device_status.restype = ctypes.c_int
     lib.ssm_get_device_status.argtypes = []
+    lib.ssm_get_async_status.restype = ctypes.c_int
+    lib.ssm_get_async_status.argtypes = [vp, vp]
     lib.ssm_status_string.restype = ctypes.c_char_p
     lib.ssm_status_string.argtypes = [ctypes.c_int]
     lib.ssm_version.restype = ctypes.c_int
@@ -143,6 +149,10 @@ def ssm_status_string(status: int) -> str:
 
 def ssm_get_device_status() -> int:
     return lib.ssm_get_device_status()
+
+
+def ssm_get_async_status(workspace=None, stream=None) -> int:
+    return lib.ssm_get_async_status(_ptr(workspace), _stream(stream))
 
 
 def ssm_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
@@ -309,6 +319,14 @@ def ssm_lti_conv_fwd(desc, K, x, D, z, out, stream=None) -> int:
     """y = K * x + D x (gated by silu(z)), the convolution mode."""
     return lib.ssm_lti_conv_fwd(ctypes.byref(desc), _ptr(K), _ptr(x), _ptr(D), _ptr(z), _ptr(out),
                                 _stream(stream))
+
+
+def ssm_proj_scan_fwd(desc, proj, x, dt_low, W_dt, A, B, C, D, z, delta_bias, out, last_state,
+                      initial_state, workspace, workspace_bytes, stream=None):
+    return lib.ssm_proj_scan_fwd(ctypes.byref(desc), ctypes.byref(proj), _ptr(x), _ptr(dt_low),
+                                 _ptr(W_dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                 _ptr(delta_bias), _ptr(out), _ptr(last_state), _ptr(initial_state),
+                                 _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
 def ssm_selection_proj_fwd(desc, proj, x, W_x, W_dt, delta_bias, dt_low, B, C, delta,

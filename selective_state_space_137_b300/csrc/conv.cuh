@@ -11,7 +11,7 @@
 #pragma once
 #include "common.cuh"
 #include "scan_generic.cuh"   // kMaxConvWidth
-#include "scan_tiled.cuh"     // silu_tiled, unpack / pack
+#include "tile_io.cuh"     // silu_tiled, unpack / pack
 #include "tma.cuh"
 
 #ifndef SSM_CONV_UNROLL

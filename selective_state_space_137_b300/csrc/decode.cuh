@@ -10,7 +10,7 @@
 #pragma once
 #include "common.cuh"
 #include "scan_generic.cuh"   // kMaxConvWidth
-#include "scan_tiled.cuh"     // softplus_tiled / silu_tiled
+#include "tile_io.cuh"     // softplus_tiled / silu_tiled
 
 namespace ssm {
 

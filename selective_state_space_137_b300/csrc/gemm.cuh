@@ -23,7 +23,7 @@
 // and exits.
 #pragma once
 #include "common.cuh"
-#include "scan_tiled.cuh"   // softplus_tiled
+#include "tile_io.cuh"   // softplus_tiled
 #include "tma.cuh"
 
 namespace ssm {

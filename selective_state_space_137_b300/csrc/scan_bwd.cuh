@@ -35,7 +35,7 @@
 // end of each tile.
 #pragma once
 #include "common.cuh"
-#include "scan_tiled.cuh"   // softplus_tiled, silu_tiled, round_up, load1
+#include "tile_io.cuh"   // softplus_tiled, silu_tiled, round_up, load1
 #include "tma.cuh"
 
 namespace ssm {

@@ -41,6 +41,10 @@ struct ScanParams {
     // training forward: the state before every 16th token, (batch, ceil(L/16), dim, N)
     float* ckpt = nullptr;
     int64_t ckpt_tiles = 0;
+    // dt_proj fused in front (read only by kernels instantiated with it):
+    // delta_raw = dt_low W_dt^T, dt_low (batch, seqlen, R) and W_dt (dim, R) bf16
+    const void* dt_low = nullptr;
+    const void* W_dt = nullptr;
 };
 
 constexpr int kCkptSteps = 16;
@@ -195,7 +199,9 @@ __global__ void carry_kernel(const float* __restrict__ A, const float* __restric
     float s = initial_state ? initial_state[i] : 0.f;
     for (int k = 0; k < nchunk; ++k) {
         float* slot = carry + ((b * nchunk + k) * dim + d) * N + n;
-        const float e = *slot;                     // end state of chunk k from zero
+        // end state of chunk k from zero; the last chunk has none (its slot
+        // only receives the start state)
+        const float e = k + 1 < nchunk ? *slot : 0.f;
         *slot = s;                                 // start state of chunk k
         if (k + 1 < nchunk) {
             const float decay = exp2f(a2 * dsum[(b * nchunk + k) * dim + d]);

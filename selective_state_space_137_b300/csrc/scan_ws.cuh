@@ -32,7 +32,7 @@
 #pragma once
 #include "common.cuh"
 #include "scan_generic.cuh"
-#include "scan_tiled.cuh"
+#include "tile_io.cuh"
 #include "tma.cuh"
 
 #ifndef SSM_HELPER_WAIT

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "common.cuh"
 #include "conv.cuh"
@@ -19,11 +20,22 @@
 #include "lti.cuh"
 #include "scan_bwd.cuh"
 #include "scan_generic.cuh"
-#include "scan_tiled.cuh"
+#include "tile_io.cuh"
+#include "scan_warp.cuh"
 #include "scan_ws.cuh"
 #include "selftest.cuh"
 
 namespace {
+
+// An NVTX range around each entry point that enqueues GPU work, named after
+// it: a profiler that records NVTX shows which library call issued which
+// kernels.  With no tool attached a push or pop is one call through a
+// pointer that is checked and skipped.
+struct TraceRange {
+    explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+};
+#define SSM_TRACE(name) TraceRange ssm_trace_range_(name)
 
 using ssm::DecodeParams;
 using ssm::ScanParams;
@@ -143,53 +155,19 @@ cudaError_t dispatch_decode(int64_t n, const DecodeParams& p, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------
-// Tiled path (path 1): TMA-staged tiles, per-token work hoisted out of the
-// state loop.  Chosen for bf16/fp32 I/O with dstate 8, 16 or 32, rows that
-// are 16-byte multiples and 16-byte aligned tensors.
+// Tiled paths: TMA-staged 16-step tiles of 16 channels, taken for bf16/fp32
+// I/O with dstate 8, 16, 32 or 64, rows that are 16-byte multiples and
+// 16-byte aligned tensors.
+//   path 3 (scan_warp.cuh): one-warp CTAs, the first-order scan (and the
+//          aggregate pass the backward's recompute uses);
+//   path 2 (scan_ws.cuh): warp-specialised CTAs, for the exact zero-order
+//          hold and the causal conv fused in front of the scan.
 
 constexpr int kPlanSMs = 148;        // the plan is fixed for a 148-SM B300
-// Tile shape (compile-time; the defaults are the tuned ones).
-#ifndef SSM_TILE_T
-#define SSM_TILE_T 32        // time steps per tile
-#endif
-#ifndef SSM_TILE_STAGES
-#define SSM_TILE_STAGES 3    // TMA ring depth
-#endif
-#ifndef SSM_STAGES16
-#define SSM_STAGES16 2       // TMA ring depth for dstate 16 (keeps 7 CTAs per SM)
-#endif
-#ifndef SSM_KS16
-#define SSM_KS16 4           // state slices per channel for dstate 16
-#endif
-#ifndef SSM_DC16
-#define SSM_DC16 16          // channels per CTA for dstate 16
-#endif
-constexpr int kTileT = SSM_TILE_T;
-constexpr int kStages = SSM_TILE_STAGES;
+constexpr int kChunkRound = 32;      // chunk lengths are multiples of this (and of both tiles)
 
-template <typename IO, int N>
-struct TiledFor;   // (KS, DC) per dstate
-template <typename IO> struct TiledFor<IO, 8>  { using Cfg = ssm::TiledCfg<IO, 8, 1, 32, kTileT, kStages>; };
-template <typename IO> struct TiledFor<IO, 16> { using Cfg = ssm::TiledCfg<IO, 16, SSM_KS16, SSM_DC16, kTileT, SSM_STAGES16>; };
-template <typename IO> struct TiledFor<IO, 32> { using Cfg = ssm::TiledCfg<IO, 32, 4, 16, kTileT, kStages>; };
-
-struct TiledShape { int dc, threads, smem; };
-
-template <typename IO>
-TiledShape tiled_shape_io(int64_t n) {
-    switch (n) {
-        case 8: { using C = typename TiledFor<IO, 8>::Cfg; return {C::DC, C::THREADS, C::SMEM}; }
-        case 16: { using C = typename TiledFor<IO, 16>::Cfg; return {C::DC, C::THREADS, C::SMEM}; }
-        case 32: { using C = typename TiledFor<IO, 32>::Cfg; return {C::DC, C::THREADS, C::SMEM}; }
-    }
-    return {0, 0, 0};
-}
-
-// Path 2 (warp-specialised: helper warp for loads and per-token work, scan
-// warp for the recurrence): dstate 16, bf16 or fp32 I/O.
-#ifndef SSM_USE_WS
-#define SSM_USE_WS 1
-#endif
+// Path 2 (warp-specialised: helper warps for loads and per-token work, a scan
+// warp for the recurrence).
 #ifndef SSM_WS_T
 #define SSM_WS_T 16          // time steps per tile
 #endif
@@ -205,30 +183,61 @@ using WsConfig = ssm::WsCfg<IO, SSM_WS_T, SSM_WS_STAGES, SSM_WS_SLOTS, CK, N>;
 // wider convs take the generic kernel.
 constexpr int kWsMaxConvWidth = 4;
 
-bool ws_path(const ssm_scan_desc* d) {
-    return SSM_USE_WS && (d->dstate == 8 || d->dstate == 16 || d->dstate == 32 || d->dstate == 64);
-}
+// Path 3 (one warp per CTA).  Two ring depths at dstate <= 16: 8 stages when
+// the time axis is not cut (7 CTAs of 30 KB per SM), 6 for chunked long
+// sequences, whose 25 KB CTAs let 8 chunks per SM run at once (measured on
+// the long-sequence workload: 8 stages 4.75 ms, 6 stages 4.39 ms, 4 stages
+// with 12 chunks 4.51 ms).
+template <typename IO, int N>
+using WarpConfig = ssm::WarpCfg<IO, N>;
+template <typename IO, int N>
+using WarpConfigChunked = ssm::WarpCfg<IO, N, (N <= 16 ? 6 : N == 32 ? 4 : 3)>;
+
+bool tiled_dstate(int64_t n) { return n == 8 || n == 16 || n == 32 || n == 64; }
+
+// Which tiled kernel a plan is for.
+enum TiledKind { kKindWarp = 3, kKindWs = 2 };
+
+// dc: channels per CTA; threads; smem: shared bytes per CTA; slots: resident
+// CTAs per SM the register budget allows.  `chunked` picks the configuration a
+// chunked launch uses.
+struct TiledShape { int dc, threads, smem, slots; };
 
 template <typename IO>
-TiledShape ws_shape(int64_t n) {
+TiledShape tiled_shape_io(int64_t n, TiledKind kind, bool chunked) {
     switch (n) {
-        case 8: return TiledShape{WsConfig<IO, 0, 8>::DC, WsConfig<IO, 0, 8>::THREADS, WsConfig<IO, 0, 8>::SMEM};
-        case 32: return TiledShape{WsConfig<IO, 0, 32>::DC, WsConfig<IO, 0, 32>::THREADS, WsConfig<IO, 0, 32>::SMEM};
-        case 64: return TiledShape{WsConfig<IO, 0, 64>::DC, WsConfig<IO, 0, 64>::THREADS, WsConfig<IO, 0, 64>::SMEM};
+#define SSM_SHAPE_CASE(NN)                                                                         \
+        case NN:                                                                                   \
+            if (kind == kKindWarp && chunked)                                                      \
+                return TiledShape{16, 32, WarpConfigChunked<IO, NN>::SMEM,                         \
+                                  WarpConfigChunked<IO, NN>::MINB};                                \
+            if (kind == kKindWarp)                                                                 \
+                return TiledShape{16, 32, WarpConfig<IO, NN>::SMEM, WarpConfig<IO, NN>::MINB};     \
+            return TiledShape{WsConfig<IO, 0, NN>::DC, WsConfig<IO, 0, NN>::THREADS,               \
+                              WsConfig<IO, 0, NN>::SMEM, WsConfig<IO, 0, NN>::MINB};
+        SSM_SHAPE_CASE(8) SSM_SHAPE_CASE(16) SSM_SHAPE_CASE(32) SSM_SHAPE_CASE(64)
+#undef SSM_SHAPE_CASE
     }
-    return TiledShape{WsConfig<IO>::DC, WsConfig<IO>::THREADS, WsConfig<IO>::SMEM};
+    return {0, 0, 0, 0};
 }
 
-TiledShape tiled_shape(const ssm_scan_desc* d) {
-    if (ws_path(d))
-        return d->io_dtype == SSM_DTYPE_F32 ? ws_shape<float>(d->dstate) : ws_shape<__nv_bfloat16>(d->dstate);
-    return d->io_dtype == SSM_DTYPE_F32 ? tiled_shape_io<float>(d->dstate)
-                                        : tiled_shape_io<__nv_bfloat16>(d->dstate);
+TiledShape tiled_shape(const ssm_scan_desc* d, TiledKind kind, bool chunked = false) {
+    return d->io_dtype == SSM_DTYPE_F32 ? tiled_shape_io<float>(d->dstate, kind, chunked)
+                                        : tiled_shape_io<__nv_bfloat16>(d->dstate, kind, chunked);
 }
 
-// Shape-only eligibility for the tiled path (pointer alignment is checked at call time).
+// Resident CTAs per SM of a tiled configuration (shared memory, threads, registers).
+int resident_per_sm(const TiledShape& sh) {
+    int per_sm = (228 * 1024) / (sh.smem + 1024);
+    if (per_sm > 2048 / sh.threads) per_sm = 2048 / sh.threads;
+    if (per_sm > sh.slots) per_sm = sh.slots;
+    if (per_sm > 32) per_sm = 32;
+    return per_sm;
+}
+
+// Shape-only eligibility for the tiled paths (pointer alignment is checked at call time).
 bool tiled_shape_ok(const ssm_scan_desc* d) {
-    if (tiled_shape(d).dc == 0) return false;
+    if (!tiled_dstate(d->dstate)) return false;
     const int64_t e = d->io_dtype == SSM_DTYPE_F32 ? 4 : 2;
     if ((d->dim * e) % 16 != 0 || (d->dstate * e) % 16 != 0) return false;
     // TMA coordinates are 32-bit and the batch is a grid dimension
@@ -236,28 +245,54 @@ bool tiled_shape_ok(const ssm_scan_desc* d) {
     return true;
 }
 
-// Chunks of the time axis for the tiled path: cut only when the (batch,
-// channel-block) CTAs cannot fill the GPU; chunk lengths are tile multiples.
-void tiled_chunks(const ssm_scan_desc* d, int* nchunk, int64_t* chunk_len) {
-    const TiledShape sh = tiled_shape(d);
+// Chunks of the time axis for a tiled path: cut only when the (batch,
+// channel-block) CTAs cannot fill the GPU; chunk lengths are multiples of
+// kChunkRound, so every chunk but the last is whole tiles.
+void tiled_chunks(const ssm_scan_desc* d, TiledKind kind, int* nchunk, int64_t* chunk_len) {
+    const TiledShape sh = tiled_shape(d, kind);
     const int64_t groups = d->batch * ((d->dim + sh.dc - 1) / sh.dc);
-    int per_sm = (228 * 1024) / (sh.smem + 1024);
-    if (per_sm > 2048 / sh.threads) per_sm = 2048 / sh.threads;
-    if (per_sm > 32) per_sm = 32;
-    const int64_t target = (int64_t)kPlanSMs * per_sm;
+    const int64_t target = (int64_t)kPlanSMs * resident_per_sm(sh);
     int64_t k = 1;
     if (groups > 0 && groups * 2 < target) {
-        k = target / groups;   // rounded down: every CTA of the pass in one wave
-        const int64_t kmax = d->seqlen / (4 * kTileT);
+        // as many chunks as the chunked configuration keeps resident, rounded
+        // down: every CTA of the pass in one wave
+        k = (int64_t)kPlanSMs * resident_per_sm(tiled_shape(d, kind, true)) / groups;
+        const int64_t kmax = d->seqlen / (4 * kChunkRound);
         if (k > kmax) k = kmax;
         if (k > 4096) k = 4096;
         if (k < 1) k = 1;
     }
     int64_t len = (d->seqlen + k - 1) / k;
-    len = (len + kTileT - 1) / kTileT * kTileT;
-    if (len < kTileT) len = kTileT;
+    len = (len + kChunkRound - 1) / kChunkRound * kChunkRound;
+    if (len < kChunkRound) len = kChunkRound;
     *chunk_len = len;
     *nchunk = d->seqlen > 0 ? (int)((d->seqlen + len - 1) / len) : 1;
+}
+
+// Identifier of the calling thread's current CUDA context (0 when there is
+// none).  Resources cached per device (copy streams, events, the address of
+// the no-allocation scratch array) are keyed on it, so they are made again
+// when the context changes (e.g. after cudaDeviceReset and a new primary
+// context) instead of being used with the old context's handles.
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -286,39 +321,6 @@ bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz
     return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <typename IO, int N>
-cudaError_t launch_tiled(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
-    using Cfg = typename TiledFor<IO, N>::Cfg;
-    const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    ssm::TiledMaps maps;
-    memset(&maps, 0, sizeof(maps));
-    const int e = (int)sizeof(IO);
-    bool ok = encode_3d(&maps.x, p.x, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
-              encode_3d(&maps.delta, p.delta, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
-              encode_3d(&maps.B, p.B, dt, e, N, d->seqlen, d->batch, N, Cfg::T) &&
-              encode_3d(&maps.C, p.C, dt, e, N, d->seqlen, d->batch, N, Cfg::T) &&
-              encode_3d(&maps.out, p.out, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
-    if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
-    if (!ok) return cudaErrorInvalidValue;
-
-    auto kfull = ssm::scan_tiled_kernel<IO, Cfg, ssm::MODE_FULL>;
-    auto kagg = ssm::scan_tiled_kernel<IO, Cfg, ssm::MODE_AGG>;
-    cudaError_t err = cudaFuncSetAttribute(kfull, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(kagg, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-    if (err != cudaSuccess) return err;
-    const unsigned gx = (unsigned)((d->dim + Cfg::DC - 1) / Cfg::DC);
-    if (p.nchunk > 1) {
-        kagg<<<dim3(gx, (unsigned)d->batch, (unsigned)(p.nchunk - 1)), Cfg::THREADS, Cfg::SMEM, s>>>(maps, p);
-        const int64_t total = p.batch * p.dim * N;
-        ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
-            p.A, p.initial_state, p.carry, p.dsum, p.batch, p.dim, N, p.nchunk);
-    }
-    kfull<<<dim3(gx, (unsigned)d->batch, (unsigned)p.nchunk), Cfg::THREADS, Cfg::SMEM, s>>>(maps, p);
-    return cudaGetLastError();
 }
 
 // agg_only: the chunk aggregates and carries alone (the chunk start states
@@ -384,12 +386,96 @@ cudaError_t launch_ws_conv(const ssm_scan_desc* d, const ScanParams& p, cudaStre
     return cudaErrorInvalidValue;
 }
 
+// Path 3: the one-warp-CTA scan for dstate 8, 16, 32 or 64 (first-order
+// input term).  agg_only: the chunk aggregates and carries alone (the chunk
+// start states the backward's recompute needs); out, z and C are not read.
+template <typename IO, int N, typename Cfg>
+cudaError_t launch_warp_cfg(const ssm_scan_desc* d, ScanParams p, cudaStream_t s, bool agg_only) {
+    const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int e = (int)sizeof(IO);
+    ssm::TiledMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    bool ok = encode_3d(&maps.x, p.x, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+              encode_3d(&maps.delta, p.delta, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+              encode_3d(&maps.B, p.B, dt, e, N, d->seqlen, d->batch, N, Cfg::T);
+    if (ok && !agg_only)
+        ok = encode_3d(&maps.C, p.C, dt, e, N, d->seqlen, d->batch, N, Cfg::T) &&
+             encode_3d(&maps.out, p.out, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+    if (ok && p.z && !agg_only)
+        ok = encode_3d(&maps.z, p.z, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+    if (!ok) return cudaErrorInvalidValue;
+    // softplus and the gate are compile-time flags of the kernel
+    const bool sp = p.softplus != 0, zg = p.z != nullptr;
+    auto kfull = sp ? (zg ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, true, true>
+                          : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, true, false>)
+                    : (zg ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, false, true>
+                          : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, false, false>);
+    auto kagg = sp ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_AGG, true, false>
+                   : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_AGG, false, false>;
+    cudaError_t err = cudaFuncSetAttribute(kfull, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(kagg, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (err != cudaSuccess) return err;
+    const unsigned gx = (unsigned)((d->dim + Cfg::DC - 1) / Cfg::DC);
+    if (p.nchunk > 1) {
+        kagg<<<dim3(gx, (unsigned)d->batch, (unsigned)(p.nchunk - 1)), 32, Cfg::SMEM, s>>>(maps, p);
+        const int64_t total = p.batch * p.dim * N;
+        ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+            p.A, p.initial_state, p.carry, p.dsum, p.batch, p.dim, N, p.nchunk);
+    }
+    if (agg_only) return cudaGetLastError();
+    kfull<<<dim3(gx, (unsigned)d->batch, (unsigned)p.nchunk), 32, Cfg::SMEM, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+template <typename IO, int N>
+cudaError_t launch_warp_n(const ssm_scan_desc* d, const ScanParams& p, cudaStream_t s, bool agg_only) {
+    return p.nchunk > 1 ? launch_warp_cfg<IO, N, WarpConfigChunked<IO, N>>(d, p, s, agg_only)
+                        : launch_warp_cfg<IO, N, WarpConfig<IO, N>>(d, p, s, agg_only);
+}
+
+// The one-warp scan with dt_proj fused in front (bf16 I/O, dstate 16, softplus):
+// the chunked configuration's 6-stage ring plus the two fp32 raw-step tiles.
+template <int R>
+cudaError_t launch_warp_proj(const ssm_scan_desc* d, ScanParams p, cudaStream_t s) {
+    using IO = __nv_bfloat16;
+    using Cfg = WarpConfigChunked<IO, 16>;
+    constexpr int SMEM = Cfg::SMEM + 2 * Cfg::T * Cfg::DC * 4;
+    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    ssm::TiledMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    bool ok = encode_3d(&maps.x, p.x, dt, 2, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+              encode_3d(&maps.B, p.B, dt, 2, 16, d->seqlen, d->batch, 16, Cfg::T) &&
+              encode_3d(&maps.C, p.C, dt, 2, 16, d->seqlen, d->batch, 16, Cfg::T) &&
+              encode_3d(&maps.out, p.out, dt, 2, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+    if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, 2, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T);
+    if (!ok) return cudaErrorInvalidValue;
+    auto kfull = p.z ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, true, true, R>
+                     : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, true, false, R>;
+    auto kagg = ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_AGG, true, false, R>;
+    cudaError_t err = cudaFuncSetAttribute(kfull, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(kagg, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (err != cudaSuccess) return err;
+    const unsigned gx = (unsigned)((d->dim + Cfg::DC - 1) / Cfg::DC);
+    if (p.nchunk > 1) {
+        kagg<<<dim3(gx, (unsigned)d->batch, (unsigned)(p.nchunk - 1)), 32, SMEM, s>>>(maps, p);
+        const int64_t total = p.batch * p.dim * 16;
+        ssm::carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+            p.A, p.initial_state, p.carry, p.dsum, p.batch, p.dim, 16, p.nchunk);
+    }
+    kfull<<<dim3(gx, (unsigned)d->batch, (unsigned)p.nchunk), 32, SMEM, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
 template <typename IO>
-cudaError_t dispatch_tiled(const ssm_scan_desc* d, const ScanParams& p, cudaStream_t s) {
+cudaError_t launch_warp(const ssm_scan_desc* d, const ScanParams& p, cudaStream_t s,
+                        bool agg_only = false) {
     switch (d->dstate) {
-        case 8: return launch_tiled<IO, 8>(d, p, s);
-        case 16: return launch_tiled<IO, 16>(d, p, s);
-        case 32: return launch_tiled<IO, 32>(d, p, s);
+        case 8: return launch_warp_n<IO, 8>(d, p, s, agg_only);
+        case 16: return launch_warp_n<IO, 16>(d, p, s, agg_only);
+        case 32: return launch_warp_n<IO, 32>(d, p, s, agg_only);
+        case 64: return launch_warp_n<IO, 64>(d, p, s, agg_only);
     }
     return cudaErrorInvalidValue;
 }
@@ -419,11 +505,11 @@ ssm_status ssm_scan_plan(const ssm_scan_desc* desc, ssm_scan_plan_info* info) {
     int64_t chunk_len;
     const bool tiled = tiled_shape_ok(desc);
     if (tiled) {
-        tiled_chunks(desc, &nchunk, &chunk_len);
+        tiled_chunks(desc, kKindWarp, &nchunk, &chunk_len);
     } else {
         nchunk = generic_nchunk(desc);
     }
-    info->path = tiled ? (ws_path(desc) ? 2 : 1) : 0;
+    info->path = tiled ? kKindWarp : 0;
     info->nchunk = nchunk;
     info->launches = (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) ? 0
                      : (nchunk > 1 ? 3 : 1);
@@ -434,15 +520,18 @@ ssm_status ssm_scan_plan(const ssm_scan_desc* desc, ssm_scan_plan_info* info) {
 
 size_t ssm_scan_workspace_size(const ssm_scan_desc* desc) {
     if (check_desc(desc) != SSM_OK) return 0;
-    // Enough for either path: the tiled one is taken only with 16-byte
-    // aligned tensors, which is known at call time.
+    // Enough for any path: the tiled ones are taken only with 16-byte
+    // aligned tensors, which is known at call time, and the exact-ZOH scan
+    // and the fused conv take the warp-specialised kernel's plan.
     size_t need = workspace_for(desc, generic_nchunk(desc));
     if (tiled_shape_ok(desc)) {
-        int nchunk;
-        int64_t chunk_len;
-        tiled_chunks(desc, &nchunk, &chunk_len);
-        const size_t t = workspace_for(desc, nchunk);
-        if (t > need) need = t;
+        for (TiledKind kind : {kKindWarp, kKindWs}) {
+            int nchunk;
+            int64_t chunk_len;
+            tiled_chunks(desc, kind, &nchunk, &chunk_len);
+            const size_t t = workspace_for(desc, nchunk);
+            if (t > need) need = t;
+        }
     }
     return need;
 }
@@ -486,13 +575,14 @@ ssm_status scan_fwd_impl(const ssm_scan_desc* desc, bool zoh, const void* x, con
     bool tiled = tiled_shape_ok(desc) && aligned16(x) && aligned16(delta) &&
                  aligned16(B) && aligned16(C) && aligned16(out) && opt_aligned(z, 16) &&
                  opt_aligned(last_state, 16);
-    // checkpoints every 16 tokens: the warp-specialised kernel (16-step tiles)
-    // or the general one
-    if (ckpt && !(ws_path(desc) && SSM_WS_T == ssm::kCkptSteps)) tiled = false;
+    // checkpoints every 16 tokens: the one-warp kernel (16-step tiles) or the
+    // general one; the exact-ZOH scan takes the warp-specialised kernel
+    if (ckpt && (zoh || WarpConfig<float, 16>::T != ssm::kCkptSteps)) tiled = false;
+    const TiledKind kind = zoh ? kKindWs : kKindWarp;
     int nchunk;
     int64_t chunk_len;
     if (tiled) {
-        tiled_chunks(desc, &nchunk, &chunk_len);
+        tiled_chunks(desc, kind, &nchunk, &chunk_len);
     } else {
         nchunk = generic_nchunk(desc);
         chunk_len = (desc->seqlen + nchunk - 1) / nchunk;
@@ -527,17 +617,15 @@ ssm_status scan_fwd_impl(const ssm_scan_desc* desc, bool zoh, const void* x, con
     cudaError_t e;
     const bool f32 = desc->io_dtype == SSM_DTYPE_F32;
     if (zoh) {
-        // exact zero-order hold: the warp-specialised kernel for dstate 16,
+        // exact zero-order hold: the warp-specialised kernel for dstate 8 to 64,
         // the generic kernel (with the same chunk plan's workspace) otherwise
-        if (tiled && ws_path(desc))
+        if (tiled)
             e = f32 ? launch_ws<float, 0, true>(desc, p, s) : launch_ws<__nv_bfloat16, 0, true>(desc, p, s);
         else
             e = f32 ? dispatch_generic<float, false, true>(N, p, s)
                     : dispatch_generic<__nv_bfloat16, false, true>(N, p, s);
-    } else if (tiled && ws_path(desc)) {
-        e = f32 ? launch_ws<float>(desc, p, s) : launch_ws<__nv_bfloat16>(desc, p, s);
     } else if (tiled) {
-        e = f32 ? dispatch_tiled<float>(desc, p, s) : dispatch_tiled<__nv_bfloat16>(desc, p, s);
+        e = f32 ? launch_warp<float>(desc, p, s) : launch_warp<__nv_bfloat16>(desc, p, s);
     } else {
         e = f32 ? dispatch_generic<float>(N, p, s) : dispatch_generic<__nv_bfloat16>(N, p, s);
     }
@@ -562,6 +650,7 @@ ssm_status ssm_scan_fwd(const ssm_scan_desc* desc, const void* x, const void* de
                         const void* z, const float* delta_bias, void* out, float* last_state,
                         const float* initial_state, void* workspace, size_t workspace_bytes,
                         void* stream) {
+    SSM_TRACE("ssm_scan_fwd");
     return scan_fwd_impl(desc, false, x, delta, A, B, C, D, z, delta_bias, out, last_state,
                          initial_state, workspace, workspace_bytes, stream);
 }
@@ -577,6 +666,7 @@ ssm_status ssm_scan_fwd_train(const ssm_scan_desc* desc, const void* x, const vo
                               const void* z, const float* delta_bias, void* out, float* last_state,
                               const float* initial_state, float* checkpoints, void* workspace,
                               size_t workspace_bytes, void* stream) {
+    SSM_TRACE("ssm_scan_fwd_train");
     if (!checkpoints || !aligned16(checkpoints)) return SSM_ERR_INVALID_ARG;
     return scan_fwd_impl(desc, false, x, delta, A, B, C, D, z, delta_bias, out, last_state,
                          initial_state, workspace, workspace_bytes, stream, checkpoints);
@@ -587,11 +677,71 @@ ssm_status ssm_scan_fwd_ex(const ssm_scan_desc* desc, const ssm_scan_opts* opts,
                            const float* D, const void* z, const float* delta_bias, void* out,
                            float* last_state, const float* initial_state, void* workspace,
                            size_t workspace_bytes, void* stream) {
+    SSM_TRACE("ssm_scan_fwd_ex");
     const ssm_status so = check_opts(opts);
     if (so != SSM_OK) return so;
     return scan_fwd_impl(desc, opts->discretization == SSM_DISC_ZOH, x, delta, A, B, C, D, z,
                          delta_bias, out, last_state, initial_state, workspace, workspace_bytes,
                          stream);
+}
+
+ssm_status ssm_proj_scan_fwd(const ssm_scan_desc* desc, const ssm_proj_desc* proj, const void* x,
+                             const void* dt_low, const void* W_dt, const float* A, const void* B,
+                             const void* C, const float* D, const void* z,
+                             const float* delta_bias, void* out, float* last_state,
+                             const float* initial_state, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+    SSM_TRACE("ssm_proj_scan_fwd");
+    const ssm_status st = check_desc(desc);
+    if (st != SSM_OK) return st;
+    if (!proj || proj->dt_rank <= 0 || proj->reserved != 0) return SSM_ERR_INVALID_ARG;
+    if (desc->io_dtype != SSM_DTYPE_BF16 || desc->dstate != 16 || !desc->delta_softplus ||
+        (proj->dt_rank != 64 && proj->dt_rank != 128) || !tiled_shape_ok(desc))
+        return SSM_ERR_UNSUPPORTED;
+    for (const void* q : std::initializer_list<const void*>{x, dt_low, W_dt, B, C, z, out, last_state})
+        if (!opt_aligned(q, 16)) return SSM_ERR_INVALID_ARG;
+    if (!opt_aligned(A, 4) || !opt_aligned(D, 4) || !opt_aligned(delta_bias, 4) ||
+        !opt_aligned(initial_state, 4))
+        return SSM_ERR_INVALID_ARG;
+    if (desc->batch == 0 || desc->dim == 0) return SSM_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (desc->seqlen == 0) {
+        const size_t state_bytes = (size_t)desc->batch * (size_t)desc->dim * 16 * sizeof(float);
+        if (last_state && last_state != initial_state) {
+            cudaError_t e = initial_state
+                ? cudaMemcpyAsync(last_state, initial_state, state_bytes, cudaMemcpyDeviceToDevice, s)
+                : cudaMemsetAsync(last_state, 0, state_bytes, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    if (!x || !dt_low || !W_dt || !A || !B || !C || !out) return SSM_ERR_INVALID_ARG;
+    int nchunk;
+    int64_t chunk_len;
+    tiled_chunks(desc, kKindWarp, &nchunk, &chunk_len);
+    const size_t need = workspace_for(desc, nchunk);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return SSM_ERR_INVALID_ARG;
+    ScanParams p;
+    p.x = x; p.delta = nullptr; p.A = A; p.B = B; p.C = C; p.D = D; p.z = z;
+    p.delta_bias = delta_bias; p.out = out; p.last_state = last_state;
+    p.initial_state = initial_state;
+    p.batch = desc->batch; p.seqlen = desc->seqlen; p.dim = desc->dim;
+    p.nchunk = nchunk;
+    p.chunk_len = chunk_len;
+    p.softplus = 1;
+    p.carry = nullptr; p.dsum = nullptr;
+    if (nchunk > 1) {
+        char* w = static_cast<char*>(workspace);
+        const size_t per = (size_t)desc->batch * (size_t)nchunk * (size_t)desc->dim;
+        p.carry = reinterpret_cast<float*>(w);
+        p.dsum = reinterpret_cast<float*>(w + ((per * 16 * sizeof(float) + 255) & ~(size_t)255));
+    }
+    p.dt_low = dt_low;
+    p.W_dt = W_dt;
+    const cudaError_t e = proj->dt_rank == 128 ? launch_warp_proj<128>(desc, p, s)
+                                               : launch_warp_proj<64>(desc, p, s);
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
 
 ssm_status ssm_selftest_wait_timeout(int64_t limit_ns, void* stream) {
@@ -607,6 +757,24 @@ ssm_status ssm_get_device_status(void) {
     if (word == 0) return SSM_OK;
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(ssm::g_ssm_device_error, &zero, sizeof(zero)) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    return SSM_ERR_TIMEOUT;
+}
+
+ssm_status ssm_get_async_status(void* workspace, void* stream) {
+    (void)workspace;   // the error word is the device's, not the call's
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned word = 0;
+    // read after the stream's earlier work, wait for this stream only
+    if (cudaMemcpyFromSymbolAsync(&word, ssm::g_ssm_device_error, sizeof(word), 0,
+                                  cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (word == 0) return SSM_OK;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbolAsync(ssm::g_ssm_device_error, &zero, sizeof(zero), 0,
+                                cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
         return SSM_ERR_CUDA;
     return SSM_ERR_TIMEOUT;
 }
@@ -659,6 +827,7 @@ ssm_status ssm_state_update(const ssm_scan_desc* desc, float* state, const void*
                             const void* delta, const float* A, const void* B, const void* C,
                             const float* D, const void* z, const float* delta_bias, void* out,
                             void* stream) {
+    SSM_TRACE("ssm_state_update");
     return state_update_impl(desc, false, state, x, delta, A, B, C, D, z, delta_bias, out, stream);
 }
 
@@ -666,6 +835,7 @@ ssm_status ssm_state_update_ex(const ssm_scan_desc* desc, const ssm_scan_opts* o
                                const void* x, const void* delta, const float* A, const void* B,
                                const void* C, const float* D, const void* z,
                                const float* delta_bias, void* out, void* stream) {
+    SSM_TRACE("ssm_state_update_ex");
     const ssm_status so = check_opts(opts);
     if (so != SSM_OK) return so;
     return state_update_impl(desc, opts->discretization == SSM_DISC_ZOH, state, x, delta, A, B, C,
@@ -793,6 +963,7 @@ extern "C" {
 ssm_status ssm_conv1d_fwd(const ssm_scan_desc* desc, const ssm_conv_desc* conv, const void* x,
                           const float* w, const float* bias, const float* conv_state_in,
                           void* out, float* conv_state_out, void* stream) {
+    SSM_TRACE("ssm_conv1d_fwd");
     if (!desc) return SSM_ERR_INVALID_ARG;
     if (desc->batch < 0 || desc->seqlen < 0 || desc->dim < 0) return SSM_ERR_INVALID_ARG;
     if (desc->io_dtype != SSM_DTYPE_F32 && desc->io_dtype != SSM_DTYPE_BF16)
@@ -852,6 +1023,7 @@ ssm_status ssm_conv_scan_fwd(const ssm_scan_desc* desc, const ssm_conv_desc* con
                              const float* D, const void* z, const float* delta_bias, void* out,
                              float* last_state, const float* initial_state, void* workspace,
                              size_t workspace_bytes, void* stream) {
+    SSM_TRACE("ssm_conv_scan_fwd");
     ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     st = check_conv(conv);
@@ -887,11 +1059,11 @@ ssm_status ssm_conv_scan_fwd(const ssm_scan_desc* desc, const ssm_conv_desc* con
                        opt_aligned(last_state, 16);
     // The conv is fused into the warp-specialised kernel (dstate 16, width up
     // to kWsMaxConvWidth) and into the generic one, which takes the rest.
-    const bool ws = tiled && ws_path(desc) && conv->width <= kWsMaxConvWidth;
+    const bool ws = tiled && conv->width <= kWsMaxConvWidth;
     int nchunk;
     int64_t chunk_len;
     if (ws) {
-        tiled_chunks(desc, &nchunk, &chunk_len);
+        tiled_chunks(desc, kKindWs, &nchunk, &chunk_len);
     } else {
         nchunk = generic_nchunk(desc);
         chunk_len = (desc->seqlen + nchunk - 1) / nchunk;
@@ -936,6 +1108,7 @@ ssm_status ssm_conv_state_update(const ssm_scan_desc* desc, const ssm_conv_desc*
                                  float* state, const void* x, const void* delta, const float* A,
                                  const void* B, const void* C, const float* D, const void* z,
                                  const float* delta_bias, void* out, void* stream) {
+    SSM_TRACE("ssm_conv_state_update");
     ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     st = check_conv(conv);
@@ -1064,6 +1237,7 @@ extern "C" ssm_status ssm_selection_proj_fwd(const ssm_scan_desc* desc, const ss
                                              const void* x, const void* W_x, const void* W_dt,
                                              const float* delta_bias, void* dt_low, void* B,
                                              void* C, void* delta_raw, void* stream) {
+    SSM_TRACE("ssm_selection_proj_fwd");
     if (!desc || !proj) return SSM_ERR_INVALID_ARG;
     if (desc->batch < 0 || desc->seqlen < 0 || desc->dim < 0 || desc->dstate <= 0 ||
         proj->dt_rank <= 0 || proj->reserved != 0)
@@ -1113,6 +1287,7 @@ extern "C" {
 ssm_status ssm_lti_kernel(const ssm_scan_desc* desc, const ssm_scan_opts* opts,
                           const float* delta, const float* A, const float* B, const float* C,
                           float* K, void* stream) {
+    SSM_TRACE("ssm_lti_kernel");
     if (!desc || desc->dim < 0 || desc->seqlen < 0 || desc->dstate <= 0) return SSM_ERR_INVALID_ARG;
     if (!dstate_supported(desc->dstate)) return SSM_ERR_UNSUPPORTED;
     if (opts && check_opts(opts) != SSM_OK) return SSM_ERR_INVALID_ARG;
@@ -1133,6 +1308,7 @@ ssm_status ssm_lti_kernel(const ssm_scan_desc* desc, const ssm_scan_opts* opts,
 
 ssm_status ssm_lti_conv_fwd(const ssm_scan_desc* desc, const float* K, const void* x,
                             const float* D, const void* z, void* out, void* stream) {
+    SSM_TRACE("ssm_lti_conv_fwd");
     if (!desc || desc->batch < 0 || desc->dim < 0 || desc->seqlen < 0) return SSM_ERR_INVALID_ARG;
     if (desc->io_dtype != SSM_DTYPE_F32 && desc->io_dtype != SSM_DTYPE_BF16)
         return SSM_ERR_UNSUPPORTED;
@@ -1354,13 +1530,13 @@ cudaError_t launch_bwd(const ssm_scan_desc* desc, const BwdPlan& pl, ssm::BwdPar
         const int64_t total = p.batch * p.dim * N;
         if (!p.ckpt_given) {
             // chunk start states, as the forward's chunked path computes them: the
-            // warp-specialised kernel's aggregate pass where it applies (16-byte
-            // rows and bases, which the TMA-staged sweep needs too; chunk lengths
-            // are multiples of its 16-step tile), else the general kernel's
+            // one-warp kernel's aggregate pass where it applies (16-byte rows and
+            // bases, which the TMA-staged sweep needs too; chunk lengths are
+            // multiples of its 16-step tile), else the general kernel's
             bool done = false;
             if constexpr (N == 8 || N == 16 || N == 32 || N == 64) {
-                if (tma && ws_path(desc) && tiled_shape_ok(desc)) {
-                    const cudaError_t e = launch_ws<IO>(desc, fp, s, true);
+                if (tma && tiled_shape_ok(desc)) {
+                    const cudaError_t e = launch_warp<IO>(desc, fp, s, true);
                     if (e != cudaSuccess) return e;
                     done = true;
                 }
@@ -1460,6 +1636,7 @@ ssm_status ssm_scan_bwd(const ssm_scan_desc* desc, const void* x, const void* de
                         float* dA, float* dB, float* dC, float* dD, void* dz,
                         float* ddelta_bias, float* dinitial_state, void* workspace,
                         size_t workspace_bytes, void* stream) {
+    SSM_TRACE("ssm_scan_bwd");
     return ssm_scan_bwd_ex(desc, x, delta, A, B, C, D, z, delta_bias, initial_state, dout,
                            dlast_state, nullptr, dx, ddelta, dA, dB, dC, dD, dz, ddelta_bias,
                            dinitial_state, workspace, workspace_bytes, stream);
@@ -1472,6 +1649,7 @@ ssm_status ssm_scan_bwd_ex(const ssm_scan_desc* desc, const void* x, const void*
                            void* dx, void* ddelta, float* dA, float* dB, float* dC, float* dD,
                            void* dz, float* ddelta_bias, float* dinitial_state, void* workspace,
                            size_t workspace_bytes, void* stream) {
+    SSM_TRACE("ssm_scan_bwd_ex");
     const ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     const size_t esz = io_size(desc);
@@ -1609,26 +1787,40 @@ HostLayout host_layout(const ssm_scan_desc* d, int64_t slice_batch) {
     return h;
 }
 
-// Two copy streams of this device, made once and kept.
+// The copy streams and events of the host pipeline, made once per device and
+// context and kept.  g_copy_mutex is held while a call enqueues its work, so
+// two host threads never interleave their records and waits on the events.
 struct CopyStreams {
+    unsigned long long ctx = 0;
     cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, ev_in[kHostBufs] = {}, ev_done[kHostBufs] = {}, ev_out[kHostBufs] = {};
 };
 std::mutex g_copy_mutex;
 CopyStreams g_copy_streams[kMaxDevices];
 
-cudaError_t copy_streams(CopyStreams* cs) {
+// Needs g_copy_mutex held.
+cudaError_t copy_streams(CopyStreams** cs) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_copy_mutex);
     CopyStreams& c = g_copy_streams[dev];
-    if (!c.in) {
-        e = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking);
+    const unsigned long long ctx = current_context_id();
+    if (!c.in || ctx == 0 || c.ctx != ctx) {
+        CopyStreams n;
+        e = cudaStreamCreateWithFlags(&n.in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&n.out, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.start, cudaEventDisableTiming);
+        for (int i = 0; i < kHostBufs && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&n.ev_in[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.ev_done[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.ev_out[i], cudaEventDisableTiming);
+        }
         if (e != cudaSuccess) return e;
+        n.ctx = current_context_id();
+        c = n;
     }
-    *cs = c;
+    *cs = &c;
     return cudaSuccess;
 }
 
@@ -1645,6 +1837,7 @@ extern "C" ssm_status ssm_scan_fwd_host(const ssm_scan_desc* desc, int64_t slice
                                         const float* delta_bias, void* out, float* last_state,
                                         const float* initial_state, void* workspace,
                                         size_t workspace_bytes, void* stream) {
+    SSM_TRACE("ssm_scan_fwd_host");
     const ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     if (desc->batch == 0 || desc->dim == 0) return SSM_OK;
@@ -1660,21 +1853,20 @@ extern "C" ssm_status ssm_scan_fwd_host(const ssm_scan_desc* desc, int64_t slice
     const HostLayout h = host_layout(desc, slice_batch);
     if (!workspace || workspace_bytes < h.total || (reinterpret_cast<uintptr_t>(workspace) & 255))
         return SSM_ERR_INVALID_ARG;
-    CopyStreams cs;
-    if (copy_streams(&cs) != cudaSuccess) return SSM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_copy_mutex);
+    CopyStreams* csp = nullptr;
+    if (copy_streams(&csp) != cudaSuccess) return SSM_ERR_CUDA;
+    const CopyStreams& cs = *csp;
     cudaStream_t comp = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
     const size_t e = io_size(desc);
     const int64_t nsl = (desc->batch + h.bs - 1) / h.bs;
 
     // events: start; per buffer "inputs in", "scanned", "outputs out"
-    cudaEvent_t ev_start, ev_in[kHostBufs], ev_done[kHostBufs], ev_out[kHostBufs];
-    bool made = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; i < kHostBufs && made; ++i)
-        made = cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
-               cudaEventCreateWithFlags(&ev_done[i], cudaEventDisableTiming) == cudaSuccess &&
-               cudaEventCreateWithFlags(&ev_out[i], cudaEventDisableTiming) == cudaSuccess;
-    if (!made) return SSM_ERR_CUDA;
+    cudaEvent_t ev_start = cs.start;
+    const cudaEvent_t* ev_in = cs.ev_in;
+    const cudaEvent_t* ev_done = cs.ev_done;
+    const cudaEvent_t* ev_out = cs.ev_out;
 
     cudaError_t err = cudaEventRecord(ev_start, comp);
     if (err == cudaSuccess) err = cudaStreamWaitEvent(cs.in, ev_start, 0);
@@ -1734,12 +1926,6 @@ extern "C" ssm_status ssm_scan_fwd_host(const ssm_scan_desc* desc, int64_t slice
         if (err == cudaSuccess && nsl > 1)
             err = cudaStreamWaitEvent(comp, ev_out[(last + 1) % kHostBufs], 0);
     }
-    cudaEventDestroy(ev_start);
-    for (int i = 0; i < kHostBufs; ++i) {
-        cudaEventDestroy(ev_in[i]);
-        cudaEventDestroy(ev_done[i]);
-        cudaEventDestroy(ev_out[i]);
-    }
     if (res != SSM_OK) return res;
     return err == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
 }
@@ -1754,24 +1940,33 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_NOALLOC_SCRATCH_BY
 
 constexpr int kNoAllocMaxDevices = 256;
 std::mutex g_noalloc_mutex;
-void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+struct NoAllocSlot {
+    unsigned long long ctx = 0;
+    void* addr = nullptr;
+};
+NoAllocSlot g_noalloc_addr[kNoAllocMaxDevices];
 
 // Device address of g_noalloc_scratch on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device with cudaGetSymbolAddress (that device current) and cached.
+// with cudaGetSymbolAddress (that device current) once per device and
+// context, and cached; a new context (e.g. after cudaDeviceReset) looks it
+// up again.
 cudaError_t noalloc_scratch_address(void** addr) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_addr[dev] == nullptr) {
+    NoAllocSlot& slot = g_noalloc_addr[dev];
+    const unsigned long long ctx = current_context_id();
+    if (slot.addr == nullptr || ctx == 0 || slot.ctx != ctx) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);   // makes the context current if needed
         if (e != cudaSuccess) return e;
-        g_noalloc_addr[dev] = p;
+        slot.addr = p;
+        slot.ctx = current_context_id();
     }
-    *addr = g_noalloc_addr[dev];
+    *addr = slot.addr;
     return cudaSuccess;
 }
 
@@ -1783,6 +1978,7 @@ extern "C" ssm_status ssm_scan_fwd_noalloc(const ssm_scan_desc* desc, const void
                                            const float* delta_bias, void* out,
                                            float* last_state, const float* initial_state,
                                            void* stream) {
+    SSM_TRACE("ssm_scan_fwd_noalloc");
     const ssm_status st = check_desc(desc);
     if (st != SSM_OK) return st;
     const size_t need = ssm_scan_workspace_size(desc);

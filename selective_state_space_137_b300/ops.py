@@ -328,6 +328,45 @@ def selection_proj(x, W_x, W_dt, dt_rank, dstate, delta_bias=None, delta_softplu
     return dt_low, Bm, Cm, delta
 
 
+def proj_scan_fwd(x, dt_low, W_dt, A, B, C, D=None, z=None, delta_bias=None, initial_state=None,
+                  out=None, last_state=None, workspace=None, stream=None):
+    """The scan with dt_proj fused in front (ssm_proj_scan_fwd): the raw step
+    is dt_low W_dt^T, formed inside the scan, then softplus(. + delta_bias).
+    x, z: (batch, seqlen, dim) bf16; dt_low (batch, seqlen, R) bf16; W_dt (dim,
+    R) bf16; B, C (batch, seqlen, 16) bf16; the rest as scan_fwd.  Returns
+    ``(out, last_state)``."""
+    if not x.is_cuda:
+        raise ValueError("proj_scan_fwd runs on a CUDA device only")
+    bsz, seqlen, dim = x.shape
+    R = dt_low.shape[-1]
+    dstate = A.shape[1]
+    dev = x.device
+    _check(x, "x", (bsz, seqlen, dim), torch.bfloat16, dev)
+    _check(dt_low, "dt_low", (bsz, seqlen, R), torch.bfloat16, dev)
+    _check(W_dt, "W_dt", (dim, R), torch.bfloat16, dev)
+    _check(A, "A", (dim, dstate), torch.float32, dev)
+    _check(B, "B", (bsz, seqlen, dstate), torch.bfloat16, dev)
+    _check(C, "C", (bsz, seqlen, dstate), torch.bfloat16, dev)
+    _check(z, "z", (bsz, seqlen, dim), torch.bfloat16, dev)
+    _check(D, "D", (dim,), torch.float32, dev)
+    _check(delta_bias, "delta_bias", (dim,), torch.float32, dev)
+    _check(initial_state, "initial_state", (bsz, dim, dstate), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(x)
+    if last_state is None:
+        last_state = torch.empty((bsz, dim, dstate), dtype=torch.float32, device=dev)
+    desc = _b.make_desc(bsz, seqlen, dim, dstate, torch.bfloat16, True)
+    need = _b.ssm_scan_workspace_size(desc)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = _b.ssm_proj_scan_fwd(desc, _b.ssm_proj_desc(int(R), 0), x, dt_low, W_dt, A, B, C, D, z,
+                              delta_bias, out, last_state, initial_state, workspace,
+                              workspace.numel(), stream)
+    if st != _b.SSM_OK:
+        raise _b.SSMError(st, "ssm_proj_scan_fwd")
+    return out, last_state
+
+
 def scan_fwd_host(x, delta, A, B, C, D=None, z=None, delta_bias=None, initial_state=None,
                   delta_softplus=True, slice_batch=0, out=None, last_state=None, workspace=None,
                   stream=None):

@@ -108,13 +108,15 @@ def test_synthetic_inputs_are_seeded():
 def test_plan_picks_the_tiled_path(ssm_lib):
     L = ssm_lib
     big = L.ssm_scan_plan(L.make_desc(4, 8192, 4096, 16, L.SSM_DTYPE_BF16))
-    assert (big.path, big.nchunk, big.launches, big.workspace) == (2, 1, 1, 0)
+    assert (big.path, big.nchunk, big.launches, big.workspace) == (3, 1, 1, 0)
     long = L.ssm_scan_plan(L.make_desc(1, 262144, 2048, 16, L.SSM_DTYPE_BF16))
-    assert long.path == 2 and long.nchunk > 1 and long.launches == 3 and long.workspace > 0
+    assert long.path == 3 and long.nchunk > 1 and long.launches == 3 and long.workspace > 0
+    # one wave of one-warp CTAs: 128 channel groups x chunks <= 148 SMs x 8
+    assert 8 <= long.nchunk and long.nchunk * 128 <= 148 * 8
     assert L.ssm_scan_workspace_size(L.make_desc(1, 262144, 2048, 16, L.SSM_DTYPE_BF16)) >= long.workspace
-    for n, path in ((1, 0), (2, 0), (4, 0), (8, 2), (16, 2), (32, 2), (64, 2)):
+    for n, path in ((1, 0), (2, 0), (4, 0), (8, 3), (16, 3), (32, 3), (64, 3)):
         assert L.ssm_scan_plan(L.make_desc(2, 300, 72, n, L.SSM_DTYPE_BF16)).path == path
-    assert L.ssm_scan_plan(L.make_desc(2, 300, 72, 16, L.SSM_DTYPE_F32)).path == 2
+    assert L.ssm_scan_plan(L.make_desc(2, 300, 72, 16, L.SSM_DTYPE_F32)).path == 3
     assert L.ssm_scan_plan(L.make_desc(2, 300, 12, 16, L.SSM_DTYPE_BF16)).path == 0   # 24-byte rows
 
 

@@ -30,6 +30,17 @@ def test_wait_timeout_is_reported_and_cleared(cuda):
     assert binding.ssm_get_device_status() == binding.SSM_OK
 
 
+def test_stream_scoped_status(cuda):
+    """ssm_get_async_status waits for one stream, then reads and clears the
+    same device-wide word."""
+    s = torch.cuda.Stream()
+    assert binding.ssm_get_async_status(None, s) == binding.SSM_OK
+    assert binding.ssm_selftest_wait_timeout(2_000_000, s) == binding.SSM_OK
+    assert binding.ssm_get_async_status(None, s) == binding.SSM_ERR_TIMEOUT
+    assert binding.ssm_get_async_status(None, s) == binding.SSM_OK     # cleared
+    assert binding.ssm_get_device_status() == binding.SSM_OK
+
+
 def test_selftest_rejects_bad_limits(cuda):
     assert binding.ssm_selftest_wait_timeout(10) == binding.SSM_ERR_INVALID_ARG
     assert binding.ssm_selftest_wait_timeout(10**12) == binding.SSM_ERR_INVALID_ARG

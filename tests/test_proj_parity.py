@@ -59,8 +59,12 @@ def test_proj_mamba_1p4b_rows_sampled(cuda):
 
 
 def test_proj_feeds_the_scan(cuda):
-    """delta_raw, B, C from the projections go straight into ssm_scan_fwd;
-    against the oracle's projections followed by the oracle's scan."""
+    """delta_raw, B, C from the projections go straight into ssm_scan_fwd.
+    Each stage is held to the bf16 bound against the oracle on that stage's
+    own inputs: the projections against the oracle's projections, and the
+    scan against the oracle's scan fed the very bf16 values the GPU scan
+    consumed (the bf16 rounding of the projection outputs is an input to the
+    scan, not an error of it)."""
     bsz, L, dim, R, N = 2, 256, 256, 32, 16
     p = synth.make_proj_inputs(bsz, L, dim, R, N, 11)
     s = synth.make_scan_inputs(synth.ScanWorkload("proj-scan", bsz, L, dim, N, "bf16", 12))
@@ -70,10 +74,12 @@ def test_proj_feeds_the_scan(cuda):
                              z=s["z"].to(cuda), delta_bias=s["delta_bias"].to(cuda))
     torch.cuda.synchronize()
     _, rB, rC, rdelta = oracle.selection_proj(f64(p["x"]), f64(p["W_x"]), f64(p["W_dt"]), R)
-    ref, ref_last = oracle.scan_fwd(f64(p["x"]), rdelta, f64(s["A"]), rB, rC, D=f64(s["D"]),
-                                    z=f64(s["z"]), delta_bias=f64(s["delta_bias"]))
-    assert rel_err(f64(out), ref) <= 2e-2
-    assert rel_err(f64(last), ref_last) <= 2e-2
+    for name, g, r in (("B", Bm, rB), ("C", Cm, rC), ("delta", delta, rdelta)):
+        assert rel_err(f64(g), r) <= TOL, name
+    ref, ref_last = oracle.scan_fwd(f64(p["x"]), f64(delta), f64(s["A"]), f64(Bm), f64(Cm),
+                                    D=f64(s["D"]), z=f64(s["z"]), delta_bias=f64(s["delta_bias"]))
+    assert rel_err(f64(out), ref) <= TOL
+    assert rel_err(f64(last), ref_last) <= TOL
 
 
 def test_proj_rejections(cuda):
@@ -106,7 +112,8 @@ def test_proj_epilogue_finishes_delta(cuda):
     _, rB, rC, rdelta = oracle.selection_proj(f64(p["x"]), f64(p["W_x"]), f64(p["W_dt"]), R)
     sp = np.logaddexp(0.0, rdelta + f64(s["delta_bias"]))
     assert rel_err(f64(dt), sp) <= TOL
-    ref, ref_last = oracle.scan_fwd(f64(p["x"]), rdelta, f64(s["A"]), rB, rC, D=f64(s["D"]),
-                                    z=f64(s["z"]), delta_bias=f64(s["delta_bias"]))
-    assert rel_err(f64(out), ref) <= 2e-2
-    assert rel_err(f64(last), ref_last) <= 2e-2
+    # the scan against the oracle's scan of the step the epilogue produced
+    ref, ref_last = oracle.scan_fwd(f64(p["x"]), f64(dt), f64(s["A"]), f64(Bm), f64(Cm),
+                                    D=f64(s["D"]), z=f64(s["z"]), delta_softplus=False)
+    assert rel_err(f64(out), ref) <= TOL
+    assert rel_err(f64(last), ref_last) <= TOL

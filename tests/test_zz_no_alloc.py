@@ -1,8 +1,10 @@
 """ssm_scan_fwd_noalloc, the scan entry point for callers that cannot
 allocate device memory (an operator plug-in handed only its input and output
-buffers, or a latency-bound loop that must not call cudaMalloc).  It must
-give the same results as ssm_scan_fwd with a caller workspace, call after
-call, although every call reuses one fixed device scratch array.
+buffers, or a latency-bound loop that must not call cudaMalloc).  It runs the
+same kernels as ssm_scan_fwd with a caller workspace, so its results must be
+bit-identical to that entry point's, call after call, although every call
+reuses one fixed device scratch array; one case is also held against the
+oracle.
 
 This file is collected last on purpose, and passes both alone in a fresh
 process and after the other tests.
@@ -12,7 +14,7 @@ import dataclasses
 import pytest
 import torch
 
-from parity import TOL, f64, rel_err, to_device
+from parity import TOL, f64, oracle_full, rel_err, to_device
 from selective_state_space_137_b300 import binding, ops, synth
 
 pytestmark = pytest.mark.gpu
@@ -41,17 +43,24 @@ def test_noalloc_matches_workspace_entry_point(cuda):
     cases = [CHUNKED,
              dataclasses.replace(CHUNKED, seed=72),                      # same shape, new data
              dataclasses.replace(CHUNKED, io="f32", dim=24, seqlen=5000, seed=73)]  # new layout
-    for w in cases:
+    for i, w in enumerate(cases):
         d = binding.make_desc(w.batch, w.seqlen, w.dim, w.dstate, synth.io_dtype(w.io))
         need = binding.ssm_scan_workspace_size(d)
         assert 0 < need <= binding.SSM_NOALLOC_SCRATCH_BYTES
-        inp = to_device(synth.make_scan_inputs(w), cuda)
+        inp_cpu = synth.make_scan_inputs(w)
+        inp = to_device(inp_cpu, cuda)
         ref_out, ref_last = ops.scan_fwd(**inp)          # caller-provided workspace
         out, last = noalloc_scan(inp)                     # fixed scratch, consecutive calls
-        torch.cuda.synchronize()
-        tol = TOL[synth.io_dtype(w.io)]
-        assert rel_err(f64(out), f64(ref_out)) <= tol
-        assert rel_err(f64(last), f64(ref_last)) <= tol
+        out2, last2 = noalloc_scan(inp)                   # the same call again: the scratch
+        torch.cuda.synchronize()                          # holds the last call's carries
+        # the same kernels on the same inputs: bit-identical results
+        assert torch.equal(out, ref_out) and torch.equal(last, ref_last), w.name
+        assert torch.equal(out2, out) and torch.equal(last2, last), w.name
+        if i == 0:
+            tol = TOL[synth.io_dtype(w.io)]
+            ref, ref_state = oracle_full(inp_cpu)
+            assert rel_err(f64(out), ref) <= tol
+            assert rel_err(f64(last), ref_state) <= tol
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(cuda):
