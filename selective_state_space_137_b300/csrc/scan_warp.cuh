@@ -460,8 +460,16 @@ __global__ void __launch_bounds__(32, Cfg::MINB)
         for (int c = 0; c < 2; ++c) {
             if (!(c ? v1 : v0)) continue;
             float* ck = p.ckpt + ((((int64_t)b * p.ckpt_tiles + tile) * p.dim + d0 + c0 + c) * N) + K * s;
+            if constexpr (K % 4 == 0) {   // 16-byte stores (K s floats from a 16-byte aligned row)
 #pragma unroll
-            for (int q = 0; q < K; ++q) ck[q] = c ? h[q].y : h[q].x;
+                for (int q = 0; q < K; q += 4)
+                    *reinterpret_cast<float4*>(ck + q) =
+                        c ? make_float4(h[q].y, h[q + 1].y, h[q + 2].y, h[q + 3].y)
+                          : make_float4(h[q].x, h[q + 1].x, h[q + 2].x, h[q + 3].x);
+            } else {
+#pragma unroll
+                for (int q = 0; q < K; ++q) ck[q] = c ? h[q].y : h[q].x;
+            }
         }
     };
     // output tile jp leaves by TMA store from ob[jp & 1]
