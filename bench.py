@@ -115,7 +115,7 @@ _KERNEL_SOURCES = {
                       "scan_ws.cuh", "ssm_api.cu"),
     "state_update": ("common.cuh", "tile_io.cuh", "decode.cuh", "ssm_api.cu"),
     "conv1d_fwd": ("common.cuh", "scan_generic.cuh", "tile_io.cuh", "conv.cuh", "ssm_api.cu"),
-    "scan_bwd": ("common.cuh", "tma.cuh", "tile_io.cuh", "scan_warp.cuh", "scan_bwd.cuh",
+    "scan_bwd": ("common.cuh", "tma.cuh", "tile_io.cuh", "scan_warp.cuh", "scan_bwd.cuh", "scan_bwd_warp.cuh",
                  "ssm_api.cu"),
     "x_proj": ("common.cuh", "tma.cuh", "tile_io.cuh", "gemm.cuh", "ssm_api.cu"),
     "dt_proj": ("common.cuh", "tma.cuh", "tile_io.cuh", "gemm.cuh", "ssm_api.cu"),

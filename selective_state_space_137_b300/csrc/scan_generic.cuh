@@ -51,9 +51,12 @@ constexpr int kCkptSteps = 16;
 
 constexpr int kMaxConvWidth = 8;
 
-// MODE_FULL: outputs for tokens of one chunk, from its start state.
-// MODE_AGG : chunk end-state from a zero start, plus the chunk's sum of Delta.
-enum { MODE_FULL = 0, MODE_AGG = 1 };
+// MODE_FULL  : outputs for tokens of one chunk, from its start state.
+// MODE_AGG   : chunk end-state from a zero start, plus the chunk's sum of Delta.
+// MODE_STATES: the state before every 16th token of one chunk, from its start
+//              state, and nothing else (the backward's recompute; the one-warp
+//              scan only).
+enum { MODE_FULL = 0, MODE_AGG = 1, MODE_STATES = 2 };
 
 // ZOH: the exact zero-order-hold input term ((exp(Delta A) - 1) / A) B x in
 // place of Delta B x (expm1f keeps it accurate for small Delta A).

@@ -27,7 +27,9 @@
 // independent CTAs.
 //
 // MODE_AGG gives a chunk's end state from a zero start and its sum of Delta
-// (no z, C, readout or output), for the cross-chunk carry.
+// (no z, C, readout or output), for the cross-chunk carry.  MODE_STATES runs
+// a chunk from its start state and writes the state before every tile (the
+// checkpoints the backward reads), with no readout or output either.
 //
 // This is the recurrent mode of the selective SSM (stage 2 in
 // "Mamba的三大创新") with the Mamba block's gate and skip fused in; the
@@ -163,7 +165,7 @@ struct WarpScan {
         // Delta x = (Delta' ln 2) x: the input term of the scan
         const float2 dx = __fmul2_rn(__fmul2_rn(dl, make_float2(kLn2, kLn2)), xv);
         r.dd[i] = make_float4(dl.x, dl.y, dx.x, dx.y);
-        if (!FULL && t < steps) dsum2 = __fadd2_rn(dsum2, dl);
+        if (MODE == MODE_AGG && t < steps) dsum2 = __fadd2_rn(dsum2, dl);
     }
     // 16-byte chunks of fp32 B | C per row (the aggregate pass widens B only)
     static constexpr int CHN = FULL ? 2 * N / 4 : N / 4;
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(32, Cfg::MINB)
     {
         const int64_t ch0 = (int64_t)b * p.dim + d0 + c0;
         const float* src = nullptr;
-        if (FULL) {
+        if (MODE != MODE_AGG) {
             if (p.nchunk > 1) src = p.carry + (((int64_t)b * p.nchunk + k) * p.dim + d0 + c0) * N;
             else if (p.initial_state) src = p.initial_state + ch0 * N;
         }
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(32, Cfg::MINB)
         }
     };
     auto ckpt_store = [&](int j) {   // training forward: the state before tile j (T = 16 steps)
-        if (!(FULL && p.ckpt)) return;
+        if (MODE == MODE_AGG || !p.ckpt) return;
         const int64_t tile = t_begin / T + j;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -565,6 +567,7 @@ __global__ void __launch_bounds__(32, Cfg::MINB)
     }
     if (!ok) return;
 
+    if (MODE == MODE_STATES) return;
     if (!FULL) {
         // the chunk's sum of Delta: lanes s = 0..3 of a channel pair hold partial sums
         dsum2.x += __shfl_xor_sync(0xffffffffu, dsum2.x, 8);

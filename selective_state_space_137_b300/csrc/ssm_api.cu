@@ -19,6 +19,7 @@
 #include "gemm.cuh"
 #include "lti.cuh"
 #include "scan_bwd.cuh"
+#include "scan_bwd_warp.cuh"
 #include "scan_generic.cuh"
 #include "tile_io.cuh"
 #include "scan_warp.cuh"
@@ -433,6 +434,34 @@ template <typename IO, int N>
 cudaError_t launch_warp_n(const ssm_scan_desc* d, const ScanParams& p, cudaStream_t s, bool agg_only) {
     return p.nchunk > 1 ? launch_warp_cfg<IO, N, WarpConfigChunked<IO, N>>(d, p, s, agg_only)
                         : launch_warp_cfg<IO, N, WarpConfig<IO, N>>(d, p, s, agg_only);
+}
+
+// The one-warp scan in MODE_STATES (dstate 16): the state before every tile of
+// every chunk into p.ckpt, each chunk from p.carry (nchunk > 1, filled by an
+// aggregate pass and the carry) or the initial state.
+template <typename IO, typename Cfg>
+cudaError_t launch_warp_states_cfg(const ssm_scan_desc* d, const ScanParams& p, cudaStream_t s) {
+    const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int e = (int)sizeof(IO);
+    ssm::TiledMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    const bool ok = encode_3d(&maps.x, p.x, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+                    encode_3d(&maps.delta, p.delta, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
+                    encode_3d(&maps.B, p.B, dt, e, 16, d->seqlen, d->batch, 16, Cfg::T);
+    if (!ok || !p.ckpt) return cudaErrorInvalidValue;
+    auto kern = p.softplus ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_STATES, true, false>
+                           : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_STATES, false, false>;
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (err != cudaSuccess) return err;
+    const unsigned gx = (unsigned)((d->dim + Cfg::DC - 1) / Cfg::DC);
+    kern<<<dim3(gx, (unsigned)d->batch, (unsigned)p.nchunk), 32, Cfg::SMEM, s>>>(maps, p);
+    return cudaGetLastError();
+}
+template <typename IO>
+cudaError_t launch_warp_states(const ssm_scan_desc* d, const ScanParams& p, cudaStream_t s) {
+    return p.nchunk > 1 ? launch_warp_states_cfg<IO, WarpConfigChunked<IO, 16>>(d, p, s)
+                        : launch_warp_states_cfg<IO, WarpConfig<IO, 16>>(d, p, s);
 }
 
 // The one-warp scan with dt_proj fused in front (bf16 I/O, dstate 16, softplus):
@@ -1343,6 +1372,11 @@ struct BwdPlan {
     int nchunk = 1;
     int warps = ssm::kBwdWarps;   // warps per CTA of the sweep
     int64_t chunk_len = 0, ntiles = 0, nblk = 0;
+    // the one-warp-layout sweep (dstate 16, 16-byte rows): warps per CTA (0:
+    // not used) and channel blocks; the sweeps above are its fallback when a
+    // call's pointers are not 16-byte aligned
+    int ww = 0;
+    int64_t nblk_w = 0;
     size_t off_fstart = 0, off_fdsum = 0, off_ebuf = 0, off_bdsum = 0, off_ckpt = 0, off_pbc = 0,
            off_pa = 0, off_pd = 0, off_pbias = 0, bytes = 0;
 };
@@ -1426,6 +1460,63 @@ int bwd_pick_warps(int64_t batch, int64_t dim, int64_t n, bool f32) {
     return best;
 }
 
+// Shared memory of a CTA of the one-warp-layout sweep with w warps.
+int bwd_warp_smem(int w, bool f32) {
+    return f32 ? ssm::BwdWarpCfg<float>::smem(w) : ssm::BwdWarpCfg<__nv_bfloat16>::smem(w);
+}
+
+// The one-warp-layout sweep applies to dstate 16 with 16-byte rows.
+bool bwd_warp_shape_ok(const ssm_scan_desc* d) {
+    const int64_t e = (int64_t)io_size(d);
+    return d->dstate == 16 && (d->dim * e) % 16 == 0 && d->seqlen < ((int64_t)1 << 31) &&
+           d->dim < ((int64_t)1 << 31);
+}
+
+// Chunks and warps per CTA of the one-warp-layout sweep.  A warp-unit is one
+// warp's 16 channels of one sequence over one chunk.  Chunks: one while there
+// are at least 4 warp-units per SM, else enough to give each SM about 7.
+// Warps per CTA: the fewest warp-steps on the busiest SM (CTAs land
+// round-robin; a grid beyond the resident CTAs runs in waves), plus the
+// traffic of the per-CTA dB | dC partial sums (fewer, wider CTAs write less);
+// ties go to wider CTAs.
+void bwd_warp_plan(const ssm_scan_desc* d, int64_t& k, int& ww, int64_t& nblk) {
+    const bool f32 = d->io_dtype == SSM_DTYPE_F32;
+    const int wmax = f32 ? ssm::BwdWarpCfg<float>::WMAX : ssm::BwdWarpCfg<__nv_bfloat16>::WMAX;
+    const int64_t units = d->batch * ((d->dim + 15) / 16);
+    const int64_t L = d->seqlen;
+    k = 1;
+    if (units < (int64_t)kPlanSMs * 4) {
+        k = (int64_t)kPlanSMs * 7 / (units > 0 ? units : 1);
+        const int64_t kmax = L / 512;
+        if (k > kmax) k = kmax;
+        if (k > 4096) k = 4096;
+        if (k < 1) k = 1;
+    }
+    const double step_s = 26e-9;                        // one warp-step of a loaded SM (measured scale)
+    const double steps = (double)((L + k - 1) / k);
+    double best = 1e300;
+    ww = wmax;
+    nblk = (d->dim + 16 * wmax - 1) / (16 * wmax);
+    for (int w = wmax; w >= 1; --w) {
+        const int64_t blk = (d->dim + 16 * w - 1) / (16 * w);
+        const int64_t ctas = d->batch * k * blk;
+        int64_t per_sm = 233472 / (bwd_warp_smem(w, f32) + 1024);
+        const int64_t by_regs = 65536 / (w * 32 * 224);
+        if (by_regs < per_sm) per_sm = by_regs;
+        if (per_sm < 1) per_sm = 1;
+        const int64_t slots = (int64_t)kPlanSMs * per_sm;
+        const int64_t busiest = ctas <= slots ? (ctas + kPlanSMs - 1) / kPlanSMs * w
+                                              : (ctas + slots - 1) / slots * per_sm * w;
+        const double t = (double)busiest * steps * step_s +
+                         (double)blk * d->batch * L * 2 * 16 * 4 * 2 / 6e12;
+        if (t < best * 0.999) {
+            best = t;
+            ww = w;
+            nblk = blk;
+        }
+    }
+}
+
 // Chunks of the time axis: one chunk unless the (sequence, channel-block)
 // CTAs fill less than half of the GPU's 2 x 148 slots (each chunk beyond the
 // first costs an aggregate pass forward and one backward).
@@ -1455,6 +1546,14 @@ BwdPlan bwd_plan(const ssm_scan_desc* d, bool with_ckpt = false) {
     pl.chunk_len = len;
     pl.nchunk = L > 0 ? (int)((L + len - 1) / len) : 1;
     pl.ntiles = (L + T - 1) / T;
+    if (bwd_warp_shape_ok(d) && L > 0 && d->batch > 0 && d->dim > 0) {
+        int64_t kw = 1;
+        bwd_warp_plan(d, kw, pl.ww, pl.nblk_w);
+        int64_t lw = (L + kw - 1) / kw;
+        lw = (lw + T - 1) / T * T;
+        pl.chunk_len = lw;
+        pl.nchunk = (int)((L + lw - 1) / lw);
+    }
     const size_t B = (size_t)d->batch, D = (size_t)d->dim, K = (size_t)pl.nchunk;
     size_t o = 0;
     if (pl.nchunk > 1) {
@@ -1467,7 +1566,8 @@ BwdPlan bwd_plan(const ssm_scan_desc* d, bool with_ckpt = false) {
     }
     pl.off_ckpt = o;
     if (!with_ckpt) o = align256(o + B * (size_t)pl.ntiles * D * N * 4);
-    pl.off_pbc = o;   o = align256(o + (size_t)pl.nblk * B * (size_t)L * 2 * N * 4);
+    const size_t nblk_max = (size_t)(pl.nblk > pl.nblk_w ? pl.nblk : pl.nblk_w);
+    pl.off_pbc = o;   o = align256(o + nblk_max * B * (size_t)L * 2 * N * 4);
     pl.off_pa = o;    o = align256(o + B * K * D * N * 4);
     pl.off_pd = o;    o = align256(o + B * K * D * 4);
     pl.off_pbias = o; o = align256(o + B * K * D * 4);
@@ -1521,6 +1621,45 @@ cudaError_t launch_sweep(const BwdPlan& pl, const ssm::BwdParams& p, bool tma, c
     }
 }
 
+// States recomputed per block of the one-warp-layout sweep (the tile's 16, or
+// 8 at a time with the first half recomputed twice).
+constexpr int kBwdWarpHist = 16;
+
+// The one-warp-layout reverse sweep (dstate 16): pl.ww warps per CTA, TMA
+// boxes of 16 channels x 16 steps.
+template <typename IO>
+cudaError_t launch_bwd_warp(const BwdPlan& pl, const ssm::BwdParams& p, cudaStream_t s) {
+    using Cfg = ssm::BwdWarpCfg<IO>;
+    const CUtensorMapDataType dt = sizeof(IO) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int e = (int)sizeof(IO);
+    ssm::BwdMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    const int64_t Dm = p.dim, L = p.seqlen, Bz = p.batch;
+    const int C = Cfg::DC, T = Cfg::T;
+    bool ok = encode_3d(&maps.x, p.x, dt, e, Dm, L, Bz, C, T) &&
+              encode_3d(&maps.delta, p.delta, dt, e, Dm, L, Bz, C, T) &&
+              encode_3d(&maps.dout, p.dout, dt, e, Dm, L, Bz, C, T) &&
+              encode_3d(&maps.B, p.B, dt, e, 16, L, Bz, 16, T) &&
+              encode_3d(&maps.C, p.C, dt, e, 16, L, Bz, 16, T) &&
+              encode_3d(&maps.dx, p.dx, dt, e, Dm, L, Bz, C, T) &&
+              encode_3d(&maps.ddelta, p.ddelta, dt, e, Dm, L, Bz, C, T);
+    if (ok && p.z) ok = encode_3d(&maps.z, p.z, dt, e, Dm, L, Bz, C, T);
+    if (ok && p.dz) ok = encode_3d(&maps.dz, p.dz, dt, e, Dm, L, Bz, C, T);
+    if (!ok || pl.ww < 1 || pl.ww > Cfg::WMAX) return cudaErrorInvalidValue;
+    constexpr int H = kBwdWarpHist;
+    const bool sp = p.softplus != 0, zg = p.z != nullptr;
+    auto kern = sp ? (zg ? ssm::scan_bwd_warp_kernel<IO, H, true, true>
+                         : ssm::scan_bwd_warp_kernel<IO, H, true, false>)
+                   : (zg ? ssm::scan_bwd_warp_kernel<IO, H, false, true>
+                         : ssm::scan_bwd_warp_kernel<IO, H, false, false>);
+    const int smem = Cfg::smem(pl.ww);
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kern<<<dim3((unsigned)pl.nblk_w, (unsigned)p.batch, (unsigned)p.nchunk), 32 * pl.ww, smem, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
 template <typename IO, int N>
 cudaError_t launch_bwd(const ssm_scan_desc* desc, const BwdPlan& pl, ssm::BwdParams p,
                        const ScanParams& fp, float* dB, float* dC, float* dA, float* dD,
@@ -1554,19 +1693,40 @@ cudaError_t launch_bwd(const ssm_scan_desc* desc, const BwdPlan& pl, ssm::BwdPar
         ssm::scan_bwd_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
             p.A, p.dlast, p.ebuf, p.bdsum, p.batch, p.dim, N, p.nchunk);
     }
-    cudaError_t err;
-    switch (pl.warps) {
-        case 4: err = launch_sweep<IO, N, 4>(pl, p, tma, s); break;
-        case 5: err = launch_sweep<IO, N, 5>(pl, p, tma, s); break;
-        case 6: err = launch_sweep<IO, N, 6>(pl, p, tma, s); break;
-        case 7: err = launch_sweep<IO, N, 7>(pl, p, tma, s); break;
-        case 8: err = launch_sweep<IO, N, 8>(pl, p, tma, s); break;
-        default: err = cudaErrorInvalidValue;
+    cudaError_t err = cudaErrorInvalidValue;
+    int64_t nblk = pl.nblk;
+    bool swept = false;
+    if constexpr (N == 16) {
+        if (tma && pl.ww > 0) {
+            // this sweep reads the state before every tile: without the training
+            // forward's checkpoints, the one-warp scan writes them first
+            err = cudaSuccess;
+            if (!p.ckpt_given) {
+                ScanParams sp = fp;
+                sp.ckpt = p.ckpt;
+                sp.ckpt_tiles = p.ntiles;
+                err = launch_warp_states<IO>(desc, sp, s);
+                p.ckpt_given = 1;
+            }
+            if (err == cudaSuccess) err = launch_bwd_warp<IO>(pl, p, s);
+            nblk = pl.nblk_w;
+            swept = true;
+        }
+    }
+    if (!swept) {
+        switch (pl.warps) {
+            case 4: err = launch_sweep<IO, N, 4>(pl, p, tma, s); break;
+            case 5: err = launch_sweep<IO, N, 5>(pl, p, tma, s); break;
+            case 6: err = launch_sweep<IO, N, 6>(pl, p, tma, s); break;
+            case 7: err = launch_sweep<IO, N, 7>(pl, p, tma, s); break;
+            case 8: err = launch_sweep<IO, N, 8>(pl, p, tma, s); break;
+            default: err = cudaErrorInvalidValue;
+        }
     }
     if (err != cudaSuccess) return err;
     const int64_t nout = p.batch * p.seqlen * 2 * N + p.dim * N + 2 * p.dim;
     ssm::scan_bwd_reduce_kernel<N><<<(unsigned)((nout + 255) / 256), 256, 0, s>>>(
-        p, (int)pl.nblk, dB, dC, dA, dD, dbias);
+        p, (int)nblk, dB, dC, dA, dD, dbias);
     return cudaGetLastError();
 }
 
@@ -1622,9 +1782,9 @@ ssm_status ssm_scan_bwd_plan(const ssm_scan_desc* desc, int with_checkpoints,
     if (desc->batch == 0 || desc->dim == 0 || desc->seqlen == 0) return SSM_OK;
     const BwdPlan pl = bwd_plan(desc, with_checkpoints != 0);
     info->nchunk = pl.nchunk;
-    info->warps = pl.warps;
-    info->channels = bwd_channels_per_cta(desc->dstate, pl.warps);
-    info->ctas = pl.nblk * desc->batch * pl.nchunk;
+    info->warps = pl.ww ? pl.ww : pl.warps;
+    info->channels = pl.ww ? 16 * pl.ww : bwd_channels_per_cta(desc->dstate, pl.warps);
+    info->ctas = (pl.ww ? pl.nblk_w : pl.nblk) * desc->batch * pl.nchunk;
     info->workspace = (int64_t)pl.bytes;
     return SSM_OK;
 }

@@ -190,22 +190,31 @@ def test_lti_rejections_before_launch(ssm_lib):
 def test_bwd_plan_query(ssm_lib):
     """ssm_scan_bwd_plan: warps per CTA chosen so the CTAs spread evenly over
     the 148 SMs (one wave), its workspace equals the size query's, and it
-    rejects what the size query rejects."""
+    rejects what the size query rejects.  dstate 16 with 16-byte rows takes
+    the one-warp-layout sweep (16 channels a warp, up to 7 warps a CTA in
+    bf16 and 6 in fp32); other dstates the sweep of 32 / (dstate / 4) channels a warp."""
     bf = torch.bfloat16
     big = ssm_lib.make_desc(4, 8192, 4096, 16, bf)         # Mamba-1.4B layer
     pl = ssm_lib.ssm_scan_bwd_plan(big)
-    assert (pl.nchunk, pl.warps, pl.channels, pl.ctas) == (1, 7, 56, 296)
+    assert (pl.nchunk, pl.warps, pl.channels, pl.ctas) == (1, 7, 112, 148)
     pl = ssm_lib.ssm_scan_bwd_plan(ssm_lib.make_desc(8, 2048, 1536, 16, bf))   # Mamba-130M layer
-    assert (pl.nchunk, pl.warps, pl.channels, pl.ctas) == (1, 6, 48, 256)
+    assert (pl.nchunk, pl.warps, pl.channels, pl.ctas) == (1, 6, 96, 128)
     pl = ssm_lib.ssm_scan_bwd_plan(ssm_lib.make_desc(1, 262144, 2048, 16, bf))  # few channels, long
-    assert pl.nchunk > 1 and pl.warps == 8
+    assert pl.nchunk > 1 and pl.ctas <= 2 * 148
+    pl = ssm_lib.ssm_scan_bwd_plan(ssm_lib.make_desc(4, 8192, 4096, 64, bf))
+    assert pl.channels == 2 * pl.warps                 # 16 lanes a channel at dstate 64
     for d in (big, ssm_lib.make_desc(2, 300, 72, 16, torch.float32),
+              ssm_lib.make_desc(4, 8192, 4096, 16, torch.float32),
               ssm_lib.make_desc(4, 8192, 4096, 64, bf), ssm_lib.make_desc(1, 40, 5000, 8, bf)):
         for ck in (False, True):
             pl = ssm_lib.ssm_scan_bwd_plan(d, ck)
             assert pl.workspace == ssm_lib.ssm_scan_bwd_ex_workspace_size(d, ck)
             assert pl.ctas == pl.nchunk * d.batch * -(-d.dim // pl.channels)
-            assert pl.ctas <= 148 * (65536 // (pl.warps * 32 * 128)) or pl.warps == 8
+            if d.dstate == 16:
+                assert pl.channels == 16 * pl.warps
+                assert pl.warps <= (7 if d.io_dtype == ssm_lib.SSM_DTYPE_BF16 else 6)
+            else:
+                assert pl.ctas <= 148 * (65536 // (pl.warps * 32 * 128)) or pl.warps == 8
     empty = ssm_lib.ssm_scan_bwd_plan(ssm_lib.make_desc(0, 10, 16, 16, bf))
     assert empty.ctas == 0 and empty.workspace == 0
     bad = ssm_lib.make_desc(1, 10, 16, 3, bf)

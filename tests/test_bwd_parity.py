@@ -174,12 +174,12 @@ def test_bwd_full_channel_sums_medium(cuda):
 @pytest.mark.parametrize("mode", ["recompute", "checkpoints"])
 def test_bwd_full_size_sampled_channels(cuda, mode):
     """The Mamba-1.4B layer (4 x 8192 x 4096 x 16, bf16), as the bench times it
-    (7 warps per CTA; with the states recomputed, or read from the training
-    forward's checkpoints): the per-channel gradients (dx, ddelta, dz over all
-    tokens; dA, dD, ddelta_bias) of sampled channels against the oracle run on
-    those channels alone (a channel's own gradients depend only on its own
-    inputs and the shared B, C rows).  Channel 4095 lies in the partial last
-    block of 56 channels."""
+    (7 warps of 16 channels per CTA; with the states recomputed, or read from
+    the training forward's checkpoints): the per-channel gradients (dx, ddelta,
+    dz over all tokens; dA, dD, ddelta_bias) of sampled channels against the
+    oracle run on those channels alone (a channel's own gradients depend only
+    on its own inputs and the shared B, C rows).  Channel 4095 lies in the
+    partial last block (64 of 112 channels)."""
     w = synth.MAMBA_1P4B
     inp = synth.make_scan_inputs(w, device=str(cuda))
     g = torch.Generator(device=cuda).manual_seed(99)
@@ -272,12 +272,43 @@ def test_bwd_with_training_checkpoints(cuda, case):
         assert norm_err(f64(got[k]), ref[k]) <= SUM_TOL[inp["x"].dtype], k
 
 
+def test_bwd_unaligned_tensors(cuda):
+    """Token tensors whose base addresses are not 16-byte aligned (a storage
+    offset of one element): the dstate-16 backward falls back from the TMA
+    sweeps to the register sweep, in the same workspace, with the same
+    gradients."""
+    w = dataclasses.replace(SMALL, name="bwd-unaligned", seed=17)
+    inp, dout, dl = make_case(w)
+    dev = to_device(inp, cuda)
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=cuda)
+        v = buf[1:1 + t.numel()].view(t.shape)
+        v.copy_(t.to(cuda))
+        assert v.data_ptr() % 16 != 0
+        return v
+    for k in ("x", "delta", "z"):
+        dev[k] = shifted(dev[k])
+    got = ops.scan_bwd(dev["x"], dev["delta"], dev["A"], dev["B"], dev["C"], shifted(dout),
+                       D=dev["D"], z=dev["z"], delta_bias=dev["delta_bias"],
+                       initial_state=dev["initial_state"], dlast_state=dl.to(cuda))
+    torch.cuda.synchronize()
+    ref = oracle.scan_bwd(f64(inp["x"]), f64(inp["delta"]), f64(inp["A"]), f64(inp["B"]),
+                          f64(inp["C"]), f64(dout), D=f64(inp["D"]), z=f64(inp["z"]),
+                          delta_bias=f64(inp["delta_bias"]), initial_state=f64(inp["initial_state"]),
+                          dlast_state=f64(dl))
+    for k in PER_TOKEN:
+        assert rel_err(f64(got[k]), ref[k]) <= TOL[torch.bfloat16], k
+    for k in SUMMED:
+        assert norm_err(f64(got[k]), ref[k]) <= SUM_TOL[torch.bfloat16], k
+
+
 def shape_for_warps(warps, n, io, L=40):
     """The smallest (batch, dim) whose backward plan sweeps in one chunk with
     `warps` warps per CTA and, where the channel block allows it, a partial
     last block of channels (found through the plan query)."""
     dt = synth.io_dtype(io)
-    for total in range(148 * 8, 60000, 8):
+    for total in range(8, 60000, 8):
         for b in (1, 2, 4):
             if total % b or (total // b) % 8:
                 continue
@@ -288,12 +319,17 @@ def shape_for_warps(warps, n, io, L=40):
     raise AssertionError(f"no shape selects {warps} warps at dstate {n}")
 
 
-@pytest.mark.parametrize("n,warps,io", [(16, 5, "bf16"), (16, 6, "bf16"), (16, 6, "f32"),
-                                        (16, 7, "bf16"), (8, 5, "bf16"), (8, 7, "f32"),
-                                        (32, 6, "bf16"), (64, 4, "bf16")])
+@pytest.mark.parametrize("n,warps,io", [(16, 1, "bf16"), (16, 2, "bf16"), (16, 3, "f32"),
+                                        (16, 4, "bf16"), (16, 5, "bf16"), (16, 6, "bf16"),
+                                        (16, 6, "f32"), (16, 7, "bf16"), (8, 5, "bf16"),
+                                        (8, 7, "f32"), (32, 6, "bf16"), (64, 4, "bf16")])
 def test_bwd_warps_per_cta(cuda, n, warps, io):
-    """Every compiled CTA width of the reverse sweep, on a shape that selects
-    it (one chunk; 40 steps = two full tiles and a ragged one)."""
+    """Every CTA width of the reverse sweeps, on a shape that selects it (one
+    chunk; 40 steps = two full tiles and a ragged one; a partial last block of
+    channels where the width allows one).  dstate 16 runs the one-warp-layout
+    sweep (CTAs of 1..7 warps, 16 channels each; the width of a single warp
+    with 8 channels is the smallest case), the other dstates the sweep of
+    8 channels a warp."""
     b, d = shape_for_warps(warps, n, io)
     w = synth.ScanWorkload(f"bwd-w{warps}-n{n}-{io}", b, 40, d, n, io, 30 + warps + n,
                            init_state=True)
