@@ -10,9 +10,11 @@
 // lane >> 3) owns the channel pair (2p, 2p + 1) and four states of both
 // channels, the pair in the two halves of an f32x2 register.  A CTA holds W
 // such warps side by side along the channels (W chosen by the host); the
-// warps share nothing but the per-step channel sums of dB and dC, added over
-// the CTA's warps once per tile through shared memory, in a fixed order (the
-// result does not depend on timing).
+// warps share nothing and never wait for one another: each writes the sums of
+// its dB and dC terms over its 16 channels (a [T][2N] tile in shared memory,
+// copied out after the tile's steps) to its own rows of the partial sums in
+// global memory, which the final reduce adds in a fixed order (the result
+// does not depend on timing).
 //
 // Per tile (reverse order):
 //   pre-pass  per token, once (lane p, steps s, s + 4, s + 8, s + 12): Delta,
@@ -24,7 +26,8 @@
 //             dA += Delta q, and three sums over the lane's states -- g B, A q
 //             and C h (the per-token gradients) -- finished over the four
 //             state quarters by shuffles; the dB = g Delta x and dC = dyc h
-//             terms summed over the warp's 16 channels by shuffles;
+//             terms summed over the warp's 16 channels by shuffles and
+//             stored (one 128-byte row per step);
 //   post-pass per token: dx, ddelta, dz from the state sums, cast, TMA store.
 //
 // Shuffle reductions without selects.  Slot q of a lane holds state
@@ -65,12 +68,11 @@ struct BwdWarpCfg {
     static constexpr int OFF_BP = OFF_XS + T * NP * 8;        // float4 [T][N / 2] (B_n, B_n, B_n+1, B_n+1)
     static constexpr int OFF_CP = OFF_BP + T * N * 8;         // the same for C
     static constexpr int OFF_SV = OFF_CP + T * N * 8;         // float2 [T][32] state sums
-    static constexpr int OFF_OB = OFF_SV + T * 32 * 8;        // IO [3][T][DC] dx, ddelta, dz
+    static constexpr int OFF_RD = OFF_SV + T * 32 * 8;        // float [T][2N] dB | dC sums of the tile
+    static constexpr int OFF_OB = OFF_RD + T * 2 * N * 4;     // IO [3][T][DC] dx, ddelta, dz
     static constexpr int OFF_BAR = round_up(OFF_OB + 3 * TOK, 16);
     static constexpr int WARP = round_up(OFF_BAR + NST * 8, 128);   // one warp's shared memory
-    static constexpr int RED = T * 2 * N * 4;                 // one warp's [T][2N] dB | dC sums
-    // CTA of w warps: w x WARP, then [2][w][T][2N] sums, 4 barriers, the abort flag
-    static constexpr int smem(int w) { return w * WARP + 2 * w * RED + 4 * 8 + 16; }
+    static constexpr int smem(int w) { return w * WARP; }
     static_assert(TOK % 128 == 0 && ROW % 128 == 0 && OFF_OB % 128 == 0, "TMA buffers 128-byte aligned");
 };
 
@@ -89,25 +91,15 @@ __global__ void __launch_bounds__(256, 1)
     const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
     unsigned char* ws = smem + warp * Cfg::WARP;
     uint64_t* full = reinterpret_cast<uint64_t*>(ws + Cfg::OFF_BAR);
-    float* red = reinterpret_cast<float*>(smem + W * Cfg::WARP);
-    uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + W * Cfg::WARP + 2 * W * Cfg::RED);
-    uint64_t* rempty = rfull + 2;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(rfull + 4);
-
     const int b = blockIdx.y, k = blockIdx.z;
-    const int64_t cta_d0 = (int64_t)blockIdx.x * W * DC;
-    int wv = (int)((p.dim - cta_d0 + DC - 1) / DC);   // warps of the CTA that own channels
-    if (wv > W) wv = W;
-    const int d0 = (int)cta_d0 + warp * DC;
-    if (lane == 0)
+    const int64_t unit = (int64_t)blockIdx.x * W + warp;   // this warp's 16-channel block
+    const int d0 = (int)(unit * DC);
+    if (d0 >= p.dim) return;   // a warp of the last CTA past the channels
+    if (lane == 0) {
         for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&rfull[i], (uint32_t)wv * 32u);   // rfull[2], rempty[2]
-        *abort_flag = 0;
+        fence_barrier_init();
     }
-    fence_barrier_init();
-    __syncthreads();   // the only block-wide barrier; warps without channels leave here
-    if (warp >= wv) return;
+    __syncwarp();
 
     const int64_t t0 = (int64_t)k * p.chunk_len;
     int64_t t1 = t0 + p.chunk_len;
@@ -194,7 +186,6 @@ __global__ void __launch_bounds__(256, 1)
         const bool landed =
             __all_sync(FULL, mbar_wait_bounded(&full[v % NST], (uint32_t)((v / NST) & 1)));
         if (landed) waited = v + 1;
-        else *abort_flag = 1;
         return landed;
     };
     auto refill = [&]() {   // after the warp's last read of the stage just consumed
@@ -203,23 +194,6 @@ __global__ void __launch_bounds__(256, 1)
             ++issued;
         }
     };
-    // wait for a phase of a CTA barrier; gives up when another warp gave up
-    auto wait_cta = [&](uint64_t* bar, int par) -> bool {
-        bool got = mbar_try_wait(bar, (uint32_t)par);
-        if (!got) {
-            const uint64_t start = global_ns();
-            while (!(got = mbar_try_wait_sleep(bar, (uint32_t)par, 20000u))) {
-                if (*abort_flag) break;
-                if (global_ns() - start > 2000000000ull) {
-                    atomicExch(&g_ssm_device_error, kDevErrTimeout);
-                    *abort_flag = 1;
-                    break;
-                }
-            }
-        }
-        return __all_sync(FULL, got);
-    };
-
     // ---- B or C tile [T][N] io -> (v, v) pairs; lane l writes float4 l, l + 32, ...
     auto widen = [&](const IO* src, float4* dst) {
 #pragma unroll
@@ -290,7 +264,12 @@ __global__ void __launch_bounds__(256, 1)
     // The shared-memory inputs of a step are read by bwd_load ahead of the
     // previous step's stores (the compiler cannot prove that they do not
     // overlap, so a load written after a store waits for it).
-    float* redw = nullptr;   // this warp's [T][2N] dB | dC sums of the current tile
+    // the tile's dB | dC sums, row t at 32 t.  The address is hidden from the
+    // compiler: it then keeps a step's shared loads after the previous step's
+    // stores, which holds the register count below the spill point (with the
+    // buffers provably disjoint it hoists loads many steps ahead and spills)
+    float* redw = reinterpret_cast<float*>(ws + Cfg::OFF_RD);
+    asm("" : "+l"(redw));
     struct BwdIn {
         float4 dd, bl, bh, cl, ch;
         float2 dy;
@@ -390,23 +369,6 @@ __global__ void __launch_bounds__(256, 1)
         }
     };
 
-    // ---- the CTA's channel sums of tile jc: rows t = warp, warp + wv, ... of the tile
-    auto consume = [&](int jc) -> bool {
-        const int par = jc & 1;
-        if (!wait_cta(&rfull[par], (jc >> 1) & 1)) return false;
-        const int j = ntile - 1 - jc;
-        const int64_t ts = t0 + (int64_t)j * T;
-        const int steps = (int)((t1 - ts) < T ? (t1 - ts) : T);
-        const float* rb = red + (size_t)par * W * T * 32;
-        for (int t = warp; t < steps; t += wv) {
-            float acc = rb[t * 32 + lane];
-            for (int w = 1; w < wv; ++w) acc += rb[(w * T + t) * 32 + lane];
-            p.pBC[(((int64_t)blockIdx.x * p.batch + b) * p.seqlen + ts + t) * 32 + lane] = acc;
-        }
-        mbar_arrive(&rempty[par]);
-        return true;
-    };
-
     bool ok = true;
     // ---- reverse sweep
     for (int jj = 0; ok && jj < ntile; ++jj) {
@@ -429,12 +391,6 @@ __global__ void __launch_bounds__(256, 1)
         pre_bwd(ws + (v % NST) * Cfg::STAGE, steps);
         __syncwarp();
         refill();
-        const int par = jj & 1;
-        if (jj >= 2 && !wait_cta(&rempty[par], ((jj - 2) >> 1) & 1)) {   // all warps summed tile jj - 2
-            ok = false;
-            break;
-        }
-        redw = red + ((size_t)par * W + warp) * T * 32;
 #pragma unroll
         for (int blk = T / H - 1; blk >= 0; --blk) {   // all T steps (see pre_bwd)
             const int base = blk * H;
@@ -461,15 +417,15 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
         __syncwarp();
-        mbar_arrive(&rfull[par]);   // this warp's sums of the tile are in place
-        post(ts, steps);
-        if (jj >= 1 && !consume(jj - 1)) {
-            ok = false;
-            break;
+        {   // the tile's sums to this warp's rows of the partial sums
+            float* dst = p.pBC + ((unit * p.batch + b) * p.seqlen + ts) * 32 + lane;
+#pragma unroll
+            for (int t = 0; t < T; ++t)
+                if (t < steps) __stcg(dst + t * 32, redw[t * 32 + lane]);
         }
+        post(ts, steps);
         __syncwarp();   // the pre-pass of the next tile rewrites what the post-pass read
     }
-    if (ok && ntile > 0) ok = consume(ntile - 1);
 
     if (lane == 0) {
         bulk_wait<0>();

@@ -1373,10 +1373,11 @@ struct BwdPlan {
     int warps = ssm::kBwdWarps;   // warps per CTA of the sweep
     int64_t chunk_len = 0, ntiles = 0, nblk = 0;
     // the one-warp-layout sweep (dstate 16, 16-byte rows): warps per CTA (0:
-    // not used) and channel blocks; the sweeps above are its fallback when a
-    // call's pointers are not 16-byte aligned
+    // not used), channel blocks of the grid and dB | dC partial sums (one per
+    // 16-channel warp); the sweeps above are its fallback when a call's
+    // pointers are not 16-byte aligned
     int ww = 0;
-    int64_t nblk_w = 0;
+    int64_t nblk_w = 0, npart_w = 0;
     size_t off_fstart = 0, off_fdsum = 0, off_ebuf = 0, off_bdsum = 0, off_ckpt = 0, off_pbc = 0,
            off_pa = 0, off_pd = 0, off_pbias = 0, bytes = 0;
 };
@@ -1476,9 +1477,8 @@ bool bwd_warp_shape_ok(const ssm_scan_desc* d) {
 // warp's 16 channels of one sequence over one chunk.  Chunks: one while there
 // are at least 4 warp-units per SM, else enough to give each SM about 7.
 // Warps per CTA: the fewest warp-steps on the busiest SM (CTAs land
-// round-robin; a grid beyond the resident CTAs runs in waves), plus the
-// traffic of the per-CTA dB | dC partial sums (fewer, wider CTAs write less);
-// ties go to wider CTAs.
+// round-robin; a grid beyond the resident CTAs runs in waves); ties go to
+// wider CTAs.
 void bwd_warp_plan(const ssm_scan_desc* d, int64_t& k, int& ww, int64_t& nblk) {
     const bool f32 = d->io_dtype == SSM_DTYPE_F32;
     const int wmax = f32 ? ssm::BwdWarpCfg<float>::WMAX : ssm::BwdWarpCfg<__nv_bfloat16>::WMAX;
@@ -1507,8 +1507,7 @@ void bwd_warp_plan(const ssm_scan_desc* d, int64_t& k, int& ww, int64_t& nblk) {
         const int64_t slots = (int64_t)kPlanSMs * per_sm;
         const int64_t busiest = ctas <= slots ? (ctas + kPlanSMs - 1) / kPlanSMs * w
                                               : (ctas + slots - 1) / slots * per_sm * w;
-        const double t = (double)busiest * steps * step_s +
-                         (double)blk * d->batch * L * 2 * 16 * 4 * 2 / 6e12;
+        const double t = (double)busiest * steps * step_s;
         if (t < best * 0.999) {
             best = t;
             ww = w;
@@ -1549,6 +1548,7 @@ BwdPlan bwd_plan(const ssm_scan_desc* d, bool with_ckpt = false) {
     if (bwd_warp_shape_ok(d) && L > 0 && d->batch > 0 && d->dim > 0) {
         int64_t kw = 1;
         bwd_warp_plan(d, kw, pl.ww, pl.nblk_w);
+        pl.npart_w = (d->dim + 15) / 16;
         int64_t lw = (L + kw - 1) / kw;
         lw = (lw + T - 1) / T * T;
         pl.chunk_len = lw;
@@ -1566,7 +1566,7 @@ BwdPlan bwd_plan(const ssm_scan_desc* d, bool with_ckpt = false) {
     }
     pl.off_ckpt = o;
     if (!with_ckpt) o = align256(o + B * (size_t)pl.ntiles * D * N * 4);
-    const size_t nblk_max = (size_t)(pl.nblk > pl.nblk_w ? pl.nblk : pl.nblk_w);
+    const size_t nblk_max = (size_t)(pl.nblk > pl.npart_w ? pl.nblk : pl.npart_w);
     pl.off_pbc = o;   o = align256(o + nblk_max * B * (size_t)L * 2 * N * 4);
     pl.off_pa = o;    o = align256(o + B * K * D * N * 4);
     pl.off_pd = o;    o = align256(o + B * K * D * 4);
@@ -1623,7 +1623,10 @@ cudaError_t launch_sweep(const BwdPlan& pl, const ssm::BwdParams& p, bool tma, c
 
 // States recomputed per block of the one-warp-layout sweep (the tile's 16, or
 // 8 at a time with the first half recomputed twice).
-constexpr int kBwdWarpHist = 16;
+#ifndef SSM_BWD_HIST
+#define SSM_BWD_HIST 16
+#endif
+constexpr int kBwdWarpHist = SSM_BWD_HIST;
 
 // The one-warp-layout reverse sweep (dstate 16): pl.ww warps per CTA, TMA
 // boxes of 16 channels x 16 steps.
@@ -1709,7 +1712,7 @@ cudaError_t launch_bwd(const ssm_scan_desc* desc, const BwdPlan& pl, ssm::BwdPar
                 p.ckpt_given = 1;
             }
             if (err == cudaSuccess) err = launch_bwd_warp<IO>(pl, p, s);
-            nblk = pl.nblk_w;
+            nblk = pl.npart_w;
             swept = true;
         }
     }
