@@ -293,7 +293,11 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // dt_low is read by all its channel blocks) right before their product, two
 // tiles ahead of their use, and the product lands in a double-buffered fp32
 // tile that the pre-pass reads in place of the delta tile.
-template <typename IO, typename Cfg, int MODE, bool SP, bool ZG, int PJR = 0>
+// CK: the kernel writes checkpoints (p.ckpt) -- the training forward and
+// MODE_STATES; the plain forward is compiled without that code (its mere
+// presence costs the plain forward 5%: measured 0.751 against 0.711 ms on the
+// Mamba-1.4B layer).
+template <typename IO, typename Cfg, int MODE, bool SP, bool ZG, int PJR = 0, bool CK = false>
 __global__ void __launch_bounds__(32, Cfg::MINB)
     scan_warp_kernel(const __grid_constant__ TiledMaps maps, const ScanParams p) {
     using W = WarpScan<IO, Cfg, MODE, SP, ZG, PJR>;
@@ -456,21 +460,23 @@ __global__ void __launch_bounds__(32, Cfg::MINB)
         }
     };
     auto ckpt_store = [&](int j) {   // training forward: the state before tile j (T = 16 steps)
-        if (MODE == MODE_AGG || !p.ckpt) return;
-        const int64_t tile = t_begin / T + j;
+        if constexpr (CK && MODE != MODE_AGG) {
+            if (!p.ckpt) return;
+            const int64_t tile = t_begin / T + j;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            if (!(c ? v1 : v0)) continue;
-            float* ck = p.ckpt + ((((int64_t)b * p.ckpt_tiles + tile) * p.dim + d0 + c0 + c) * N) + K * s;
-            if constexpr (K % 4 == 0) {   // 16-byte stores (K s floats from a 16-byte aligned row)
+            for (int c = 0; c < 2; ++c) {
+                if (!(c ? v1 : v0)) continue;
+                float* ck = p.ckpt + ((((int64_t)b * p.ckpt_tiles + tile) * p.dim + d0 + c0 + c) * N) + K * s;
+                if constexpr (K % 4 == 0) {   // 16-byte stores (K s floats from a 16-byte aligned row)
 #pragma unroll
-                for (int q = 0; q < K; q += 4)
-                    *reinterpret_cast<float4*>(ck + q) =
-                        c ? make_float4(h[q].y, h[q + 1].y, h[q + 2].y, h[q + 3].y)
-                          : make_float4(h[q].x, h[q + 1].x, h[q + 2].x, h[q + 3].x);
-            } else {
+                    for (int q = 0; q < K; q += 4)
+                        *reinterpret_cast<float4*>(ck + q) =
+                            c ? make_float4(h[q].y, h[q + 1].y, h[q + 2].y, h[q + 3].y)
+                              : make_float4(h[q].x, h[q + 1].x, h[q + 2].x, h[q + 3].x);
+                } else {
 #pragma unroll
-                for (int q = 0; q < K; ++q) ck[q] = c ? h[q].y : h[q].x;
+                    for (int q = 0; q < K; ++q) ck[q] = c ? h[q].y : h[q].x;
+                }
             }
         }
     };

@@ -408,10 +408,19 @@ cudaError_t launch_warp_cfg(const ssm_scan_desc* d, ScanParams p, cudaStream_t s
     if (!ok) return cudaErrorInvalidValue;
     // softplus and the gate are compile-time flags of the kernel
     const bool sp = p.softplus != 0, zg = p.z != nullptr;
-    auto kfull = sp ? (zg ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, true, true>
-                          : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, true, false>)
-                    : (zg ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, false, true>
-                          : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_FULL, false, false>);
+    // the training forward (checkpoints) is a kernel of its own: the plain
+    // forward is compiled without the checkpoint code
+    const bool ck = p.ckpt != nullptr;
+    using ssm::scan_warp_kernel;
+    using ssm::MODE_FULL;
+    auto kfull = ck ? (sp ? (zg ? scan_warp_kernel<IO, Cfg, MODE_FULL, true, true, 0, true>
+                                : scan_warp_kernel<IO, Cfg, MODE_FULL, true, false, 0, true>)
+                          : (zg ? scan_warp_kernel<IO, Cfg, MODE_FULL, false, true, 0, true>
+                                : scan_warp_kernel<IO, Cfg, MODE_FULL, false, false, 0, true>))
+                    : (sp ? (zg ? scan_warp_kernel<IO, Cfg, MODE_FULL, true, true>
+                                : scan_warp_kernel<IO, Cfg, MODE_FULL, true, false>)
+                          : (zg ? scan_warp_kernel<IO, Cfg, MODE_FULL, false, true>
+                                : scan_warp_kernel<IO, Cfg, MODE_FULL, false, false>));
     auto kagg = sp ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_AGG, true, false>
                    : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_AGG, false, false>;
     cudaError_t err = cudaFuncSetAttribute(kfull, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
@@ -450,8 +459,8 @@ cudaError_t launch_warp_states_cfg(const ssm_scan_desc* d, const ScanParams& p, 
                     encode_3d(&maps.delta, p.delta, dt, e, d->dim, d->seqlen, d->batch, Cfg::DC, Cfg::T) &&
                     encode_3d(&maps.B, p.B, dt, e, 16, d->seqlen, d->batch, 16, Cfg::T);
     if (!ok || !p.ckpt) return cudaErrorInvalidValue;
-    auto kern = p.softplus ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_STATES, true, false>
-                           : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_STATES, false, false>;
+    auto kern = p.softplus ? ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_STATES, true, false, 0, true>
+                           : ssm::scan_warp_kernel<IO, Cfg, ssm::MODE_STATES, false, false, 0, true>;
     const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
     if (err != cudaSuccess) return err;
     const unsigned gx = (unsigned)((d->dim + Cfg::DC - 1) / Cfg::DC);
