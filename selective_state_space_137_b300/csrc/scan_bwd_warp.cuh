@@ -309,25 +309,27 @@ __global__ void __launch_bounds__(256, 1)
             vc[q] = pc.x + pc.y;   // dC term
             if (ZG) yp = q ? __ffma2_rn(Cq[q], hc[q], yp) : __fmul2_rn(Cq[q], hc[q]);
         }
-        // dB, dC over the 8 pairs of the warp: lane bits 2, 1, 0
-        vb[0] += __shfl_xor_sync(FULL, vb[2], 4);
-        vb[1] += __shfl_xor_sync(FULL, vb[3], 4);
-        vc[0] += __shfl_xor_sync(FULL, vc[2], 4);
-        vc[1] += __shfl_xor_sync(FULL, vc[3], 4);
-        const float kb = b1 ? vb[1] : vb[0], eb = b1 ? vb[0] : vb[1];
-        const float kc = b1 ? vc[1] : vc[0], ec = b1 ? vc[0] : vc[1];
-        const float rb = kb + __shfl_xor_sync(FULL, eb, 2);
-        const float rc = kc + __shfl_xor_sync(FULL, ec, 2);
-        const float keep = b0 ? rc : rb, send = b0 ? rb : rc;
+        // dB, dC over the 8 pairs of the warp: lane bits 2, 1, 0 (the adds of a
+        // round paired in f32x2: one instruction for two sums)
+        const float2 ra = __fadd2_rn(make_float2(vb[0], vb[1]),
+                                     make_float2(__shfl_xor_sync(FULL, vb[2], 4), __shfl_xor_sync(FULL, vb[3], 4)));
+        const float2 rc_ = __fadd2_rn(make_float2(vc[0], vc[1]),
+                                      make_float2(__shfl_xor_sync(FULL, vc[2], 4), __shfl_xor_sync(FULL, vc[3], 4)));
+        const float kb = b1 ? ra.y : ra.x, eb = b1 ? ra.x : ra.y;
+        const float kc = b1 ? rc_.y : rc_.x, ec = b1 ? rc_.x : rc_.y;
+        const float2 rbc = __fadd2_rn(make_float2(kb, kc),
+                                      make_float2(__shfl_xor_sync(FULL, eb, 2), __shfl_xor_sync(FULL, ec, 2)));
+        const float keep = b0 ? rbc.y : rbc.x, send = b0 ? rbc.x : rbc.y;
         redw[t * 32 + o_lane] = keep + __shfl_xor_sync(FULL, send, 1);
         // g B, A q, C h over the four state quarters: lane bits 4, 3
-        const float S1 = s1.x + __shfl_xor_sync(FULL, s1.y, 16);
-        const float S2 = s2.x + __shfl_xor_sync(FULL, s2.y, 16);
+        const float2 S12 = __fadd2_rn(make_float2(s1.x, s2.x),
+                                      make_float2(__shfl_xor_sync(FULL, s1.y, 16), __shfl_xor_sync(FULL, s2.y, 16)));
+        const float S1 = S12.x, S2 = S12.y;
         const float YP = ZG ? yp.x + __shfl_xor_sync(FULL, yp.y, 16) : 0.f;
         const float ka = m ? YP : S1, ea = m ? S1 : YP;
         const float kz = m ? 0.f : S2, ez = m ? S2 : 0.f;
-        SV[t * 32 + lane] =
-            make_float2(ka + __shfl_xor_sync(FULL, ea, 8), kz + __shfl_xor_sync(FULL, ez, 8));
+        SV[t * 32 + lane] = __fadd2_rn(make_float2(ka, kz),
+                                       make_float2(__shfl_xor_sync(FULL, ea, 8), __shfl_xor_sync(FULL, ez, 8)));
     };
 
     // ---- per-token gradients of a tile from the state sums; one TMA store per tensor
