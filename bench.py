@@ -119,6 +119,7 @@ _KERNEL_SOURCES = {
                  "ssm_api.cu"),
     "x_proj": ("common.cuh", "tma.cuh", "tile_io.cuh", "gemm.cuh", "ssm_api.cu"),
     "dt_proj": ("common.cuh", "tma.cuh", "tile_io.cuh", "gemm.cuh", "ssm_api.cu"),
+    "lti_conv": ("common.cuh", "tma.cuh", "tile_io.cuh", "lti.cuh", "ssm_api.cu"),
 }
 
 

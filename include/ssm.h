@@ -192,7 +192,11 @@ SSM_API ssm_status ssm_scan_bwd_ex(const ssm_scan_desc *desc, const void *x, con
  *                     gated by silu(z) when z is not NULL.  x, z, out (batch,
  *                     seqlen, dim) io; K (dim, seqlen) fp32; D (dim) fp32 or NULL.
  *                     O(seqlen^2) work per (sequence, channel); desc->dstate and
- *                     desc->delta_softplus are ignored.  out must not alias x. */
+ *                     desc->delta_softplus are ignored.  out must not alias x.
+ *                     bf16 I/O with dim a multiple of 8 and 16-byte aligned x, z,
+ *                     out runs on the tensor cores, each tap of K carried as two
+ *                     bf16 terms (about 2^-17 of its value); fp32 I/O and other
+ *                     shapes run on the CUDA cores in fp32. */
 SSM_API ssm_status ssm_lti_kernel(const ssm_scan_desc *desc, const ssm_scan_opts *opts,
                                   const float *delta, const float *A, const float *B,
                                   const float *C, float *K, void *stream);

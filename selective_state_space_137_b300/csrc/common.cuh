@@ -62,4 +62,17 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
     return r;
 }
 
+// bf16 tensor-core product of one m16n8k16 tile: d += a b (fp32 accumulate).
+// Fragments (lane = 4 g + q): a0 = A[g][2q, 2q+1], a1 = A[g+8][2q, 2q+1],
+// a2 = A[g][2q+8, 2q+9], a3 = A[g+8][2q+8, 2q+9]; b0 = B[2q, 2q+1][g],
+// b1 = B[2q+8, 2q+9][g]; d = D[g][2q, 2q+1], D[g+8][2q, 2q+1] (low element first).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 }  // namespace ssm

@@ -270,16 +270,6 @@ struct WarpScan {
     }
 };
 
-// bf16 tensor-core product of one m16n8k16 tile: d += a b (fp32 accumulate).
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // PJR > 0 (bf16 I/O): dt_proj fused in front.  The raw step of tile m,
 // delta_raw[t][c] = sum_r dt_low[t][r] W_dt[d0 + c][r] over the tile's 16 steps
 // and 16 channels, is a [16 x R] x [R x 16] product: R / 16 k-steps of two

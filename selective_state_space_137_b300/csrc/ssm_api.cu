@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -318,6 +319,20 @@ bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz
     const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
     const cuuint64_t strides[2] = {(cuuint64_t)(cols * esz), (cuuint64_t)(cols * rows * esz)};
     const cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same with a box of box_cols x box_rows x box_batch.
+bool encode_3d_box(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz, int64_t cols,
+                   int64_t rows, int64_t batch, int box_cols, int box_rows, int box_batch) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)(cols * esz), (cuuint64_t)(cols * rows * esz)};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, (cuuint32_t)box_batch};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1362,8 +1377,37 @@ ssm_status ssm_lti_conv_fwd(const ssm_scan_desc* desc, const float* K, const voi
     ssm::LtiConvParams p;
     p.K = K; p.x = x; p.D = D; p.z = z; p.out = out;
     p.batch = desc->batch; p.seqlen = desc->seqlen; p.dim = desc->dim;
-    const dim3 grid((unsigned)tx, (unsigned)ty, (unsigned)desc->batch);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // bf16 I/O with 16-byte rows and bases: the tensor-core form
+    if (desc->io_dtype == SSM_DTYPE_BF16 && desc->dim % 8 == 0 && desc->seqlen < ((int64_t)1 << 30) &&
+        opt_aligned(x, 16) && opt_aligned(z, 16) && opt_aligned(out, 16) && desc->dim < ((int64_t)1 << 31)) {
+        const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        ssm::LtiMmaMaps maps;
+        memset(&maps, 0, sizeof(maps));
+        const int C = ssm::kLtiMmaCh, T = ssm::kLtiMmaChunk, NB = ssm::kLtiMmaB;
+        bool ok = encode_3d_box(&maps.x, x, dt, 2, desc->dim, desc->seqlen, desc->batch, C, T, NB) &&
+                  encode_3d_box(&maps.out, out, dt, 2, desc->dim, desc->seqlen, desc->batch, C, T, NB);
+        if (ok && z) ok = encode_3d_box(&maps.z, z, dt, 2, desc->dim, desc->seqlen, desc->batch, C, T, NB);
+        if (!ok) return SSM_ERR_CUDA;
+        auto kern = z ? ssm::lti_conv_mma_kernel<true> : ssm::lti_conv_mma_kernel<false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ssm::LtiMmaCfg::SMEM) !=
+            cudaSuccess)
+            return SSM_ERR_CUDA;
+        // persistent: as many CTAs as fit the GPU at once, shared by the batch blocks
+        int dev = 0, sms = 0, per_sm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, ssm::LtiMmaCfg::SMEM) !=
+                cudaSuccess)
+            return SSM_ERR_CUDA;
+        const int64_t nby = (desc->batch + NB - 1) / NB;
+        const int64_t items = (desc->dim / C) * ((desc->seqlen + T - 1) / T);
+        const int64_t slots = std::max<int64_t>(1, (int64_t)sms * std::max(per_sm, 1) / nby);
+        const dim3 g((unsigned)std::min(items, slots), (unsigned)nby);
+        kern<<<g, 256, ssm::LtiMmaCfg::SMEM, s>>>(maps, p);
+        return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_CUDA;
+    }
+    const dim3 grid((unsigned)tx, (unsigned)ty, (unsigned)desc->batch);
     if (desc->io_dtype == SSM_DTYPE_F32)
         ssm::lti_conv_kernel<float><<<grid, 256, 0, s>>>(p);
     else

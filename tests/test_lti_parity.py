@@ -56,6 +56,24 @@ def test_lti_conv(cuda, io, shape):
     assert rel_err(f64(y0), ref0) <= TOL[dt]
 
 
+def test_lti_conv_many_items_per_cta(cuda):
+    """bf16 with 16-byte rows takes the tensor-core kernel, whose persistent
+    CTAs each take several (channel block, step group) items of different
+    weights: 2 sequences (a partial block of 8), 900 steps (8 groups of 128,
+    the last partial), 1024 channels, with D and the gate."""
+    bsz, L, dim = 2, 900, 1024
+    delta, A, B, C = lti_params(dim, 16, 91)
+    K32 = torch.from_numpy(oracle.lti_kernel(delta, A, B, C, L).astype(np.float32))
+    g = torch.Generator().manual_seed(19)
+    x = torch.randn((bsz, L, dim), generator=g).to(torch.bfloat16)
+    z = torch.randn((bsz, L, dim), generator=g).to(torch.bfloat16)
+    D = torch.randn(dim, generator=g)
+    y = ops.lti_conv_fwd(K32.to(cuda), x.to(cuda), D=D.to(cuda), z=z.to(cuda))
+    torch.cuda.synchronize()
+    ref = oracle.lti_conv(f64(K32), f64(x), D=f64(D), z=f64(z))
+    assert rel_err(f64(y), ref) <= TOL[torch.bfloat16]
+
+
 def test_lti_conv_mode_equals_recurrence(cuda):
     """Convolution mode (kernel + conv) and the recurrence (ssm_scan_fwd with
     the constant step, B and C shared by all channels) give the same output."""
