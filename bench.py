@@ -511,7 +511,7 @@ def run_e2e(args, w, inp, desc, plan, dev, world, binding):
     """Same metric through the public API for host-resident data
     (ssm_scan_fwd_host): every step copies the activations x, delta, z, B, C
     from pinned host memory to the GPU and the output and final state back,
-    pipelined over batch slices inside the call; A, D and the bias (the
+    pipelined over slices inside the call; A, D and the bias (the
     layer's parameters) stay on the GPU."""
     names = ["x", "delta", "z", "B", "C"]
     host = {k: inp[k].cpu().pin_memory() for k in names if inp[k] is not None}
@@ -554,7 +554,7 @@ def run_e2e(args, w, inp, desc, plan, dev, world, binding):
     h2d_ms = a.elapsed_time(b) / 3
     return {"value": whole_job_rate(world, w.tokens, steps, total), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": total / steps, "api": "ssm_scan_fwd_host (batch slices pipelined)",
+            "ms_per_step": total / steps, "api": "ssm_scan_fwd_host (16 MiB slices pipelined)",
             "pcie_gb_per_s": (h2d + d2h) / (total / steps * 1e-3) / 1e9,
             "h2d_copy_alone_ms": h2d_ms, "h2d_gb_per_s": h2d / (h2d_ms * 1e-3) / 1e9}
 

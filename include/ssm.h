@@ -359,12 +359,19 @@ SSM_API ssm_status ssm_conv_state_update(const ssm_scan_desc *desc, const ssm_co
                                          const void *C, const float *D, const void *z,
                                          const float *delta_bias, void *out, void *stream);
 
-/* The scan over tensors that live in host memory: the batch is cut into
- * slices of `slice_batch` sequences, and each slice's inputs are copied in,
- * scanned and its outputs copied back in a three-stage pipeline (copies in,
- * the scan, copies out on their own streams, double-buffered), so the
- * host-device transfers overlap one another and the kernels.  Sequences are
- * independent, so the result equals one ssm_scan_fwd over the whole batch.
+/* The scan over tensors that live in host memory: the work is cut into
+ * slices, and each slice's inputs are copied in, scanned and its outputs
+ * copied back in a three-stage pipeline (copies in, the scan, copies out on
+ * their own streams, double-buffered), so the host-device transfers overlap
+ * one another and the kernels.  A slice is contiguous in host memory:
+ *   slice_batch > 0: that many whole sequences;
+ *   slice_batch < 0: a run of -slice_batch steps of one sequence, each run
+ *     starting from the state the previous run of that sequence ended in
+ *     (kept on the device);
+ *   slice_batch = 0: whole sequences while one sequence's x is at most
+ *     16 MiB, else 16 MiB runs of steps (multiples of 64).
+ * Sequences are independent and the state carries across runs, so the
+ * result equals one ssm_scan_fwd over the whole batch.
  *   host (pinned for overlap; pageable memory works but serialises):
  *     x, delta, z, out (batch, seqlen, dim) io; B, C (batch, seqlen, dstate) io;
  *     initial_state, last_state (batch, dim, dstate) fp32 (NULL: zeros / not returned)
@@ -372,7 +379,7 @@ SSM_API ssm_status ssm_conv_state_update(const ssm_scan_desc *desc, const ssm_co
  *   workspace: device memory of ssm_scan_fwd_host_workspace_size(desc,
  *     slice_batch) bytes, 256-byte aligned.
  * Asynchronous on `stream`: when the stream reaches this call's end, every
- * output has landed in host memory.  slice_batch <= 0 picks one. */
+ * output has landed in host memory. */
 SSM_API size_t ssm_scan_fwd_host_workspace_size(const ssm_scan_desc *desc, int64_t slice_batch);
 SSM_API ssm_status ssm_scan_fwd_host(const ssm_scan_desc *desc, int64_t slice_batch,
                                      const void *x, const void *delta, const float *A,

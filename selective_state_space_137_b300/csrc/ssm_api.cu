@@ -1961,32 +1961,59 @@ constexpr int kMaxDevices = 256;
 
 struct HostLayout {
     int64_t bs = 0;                   // sequences per slice
-    size_t tok = 0, bc = 0, st = 0;   // bytes per slice: (bs, L, D) io, (bs, L, N) io, (bs, D, N) fp32
+    int64_t ts = 0;                   // steps per slice (< L only with bs == 1)
+    size_t tok = 0, bc = 0, st = 0;   // bytes per slice: (bs, ts, D) io, (bs, ts, N) io, (bs, D, N) fp32
     size_t scan_ws = 0;               // ssm_scan_fwd workspace of one slice
     size_t per_buf = 0, total = 0;
     // offsets inside one buffer
     size_t o_x = 0, o_dl = 0, o_z = 0, o_b = 0, o_c = 0, o_out = 0, o_h0 = 0, o_h1 = 0, o_ws = 0;
 };
 
-int64_t host_slice(const ssm_scan_desc* d, int64_t slice_batch) {
-    if (slice_batch > 0) return slice_batch < d->batch ? slice_batch : d->batch;
-    // about 64 MB of token data per slice, and at least 2 slices when there are 2 sequences
-    const int64_t per_seq = d->seqlen * d->dim * (int64_t)io_size(d);
-    int64_t bs = per_seq > 0 ? (int64_t)(64u << 20) / per_seq : d->batch;
-    if (bs < 1) bs = 1;
-    if (d->batch >= 2 && bs > d->batch / 2) bs = d->batch / 2;
-    return bs < 1 ? 1 : bs;
+// Slices: slice_batch > 0 takes that many whole sequences; slice_batch < 0
+// takes -slice_batch steps of one sequence (the state carried from slice to
+// slice on the device); 0 picks: whole sequences while one sequence's x is at
+// most 16 MB (at least 2 slices when there are 2 sequences), else 16 MB runs
+// of steps of one sequence (multiples of 64 steps).  Small slices keep the
+// pipeline's ends short: the first slice's copy in and the last one's scan
+// and copy out are not overlapped.
+constexpr int64_t kHostSliceBytes = 16ll << 20;
+
+void host_slice(const ssm_scan_desc* d, int64_t slice_batch, int64_t* bs, int64_t* ts) {
+    *ts = d->seqlen;
+    if (slice_batch > 0) {
+        *bs = slice_batch < d->batch ? slice_batch : d->batch;
+        return;
+    }
+    if (slice_batch < 0) {
+        *bs = 1;
+        *ts = -slice_batch < d->seqlen ? -slice_batch : d->seqlen;
+        return;
+    }
+    const int64_t step = d->dim * (int64_t)io_size(d);
+    const int64_t per_seq = d->seqlen * step;
+    if (per_seq > kHostSliceBytes && step > 0) {
+        *bs = 1;
+        int64_t t = (kHostSliceBytes / step) / 64 * 64;
+        if (t < 64) t = 64;
+        *ts = t < d->seqlen ? t : d->seqlen;
+        return;
+    }
+    int64_t b = per_seq > 0 ? kHostSliceBytes / per_seq : d->batch;
+    if (b < 1) b = 1;
+    if (d->batch >= 2 && b > d->batch / 2) b = d->batch / 2;
+    *bs = b < 1 ? 1 : b;
 }
 
 HostLayout host_layout(const ssm_scan_desc* d, int64_t slice_batch) {
     HostLayout h;
-    h.bs = host_slice(d, slice_batch);
+    host_slice(d, slice_batch, &h.bs, &h.ts);
     const size_t e = io_size(d);
-    h.tok = (size_t)h.bs * (size_t)d->seqlen * (size_t)d->dim * e;
-    h.bc = (size_t)h.bs * (size_t)d->seqlen * (size_t)d->dstate * e;
+    h.tok = (size_t)h.bs * (size_t)h.ts * (size_t)d->dim * e;
+    h.bc = (size_t)h.bs * (size_t)h.ts * (size_t)d->dstate * e;
     h.st = (size_t)h.bs * (size_t)d->dim * (size_t)d->dstate * sizeof(float);
     ssm_scan_desc sd = *d;
     sd.batch = h.bs;
+    sd.seqlen = h.ts;
     h.scan_ws = ssm_scan_workspace_size(&sd);
     size_t o = 0;
     h.o_x = o;   o = align256(o + h.tok);
@@ -2076,7 +2103,9 @@ extern "C" ssm_status ssm_scan_fwd_host(const ssm_scan_desc* desc, int64_t slice
     cudaStream_t comp = static_cast<cudaStream_t>(stream);
     char* ws = static_cast<char*>(workspace);
     const size_t e = io_size(desc);
-    const int64_t nsl = (desc->batch + h.bs - 1) / h.bs;
+    const int64_t ngroups = (desc->batch + h.bs - 1) / h.bs;
+    const int64_t ntime = (desc->seqlen + h.ts - 1) / h.ts;
+    const int64_t nsl = ngroups * ntime;
 
     // events: start; per buffer "inputs in", "scanned", "outputs out"
     cudaEvent_t ev_start = cs.start;
@@ -2091,12 +2120,16 @@ extern "C" ssm_status ssm_scan_fwd_host(const ssm_scan_desc* desc, int64_t slice
     for (int64_t i = 0; i < nsl && err == cudaSuccess && res == SSM_OK; ++i) {
         const int bi = (int)(i % kHostBufs);
         char* buf = ws + (size_t)bi * h.per_buf;
-        const int64_t b0 = i * h.bs;
+        const int64_t g = i / ntime, j = i % ntime;   // batch group, run of steps
+        const int64_t b0 = g * h.bs, t0 = j * h.ts;
         const int64_t nb = desc->batch - b0 < h.bs ? desc->batch - b0 : h.bs;
-        const size_t tok = (size_t)nb * (size_t)desc->seqlen * (size_t)desc->dim * e;
-        const size_t tok_off = (size_t)b0 * (size_t)desc->seqlen * (size_t)desc->dim * e;
-        const size_t bc = (size_t)nb * (size_t)desc->seqlen * (size_t)desc->dstate * e;
-        const size_t bc_off = (size_t)b0 * (size_t)desc->seqlen * (size_t)desc->dstate * e;
+        const int64_t nt = desc->seqlen - t0 < h.ts ? desc->seqlen - t0 : h.ts;
+        // a slice is contiguous in host memory: whole sequences, or (ntime > 1)
+        // a run of steps of one sequence
+        const size_t tok = (size_t)nb * (size_t)nt * (size_t)desc->dim * e;
+        const size_t tok_off = ((size_t)b0 * (size_t)desc->seqlen + (size_t)t0) * (size_t)desc->dim * e;
+        const size_t bc = (size_t)nb * (size_t)nt * (size_t)desc->dstate * e;
+        const size_t bc_off = ((size_t)b0 * (size_t)desc->seqlen + (size_t)t0) * (size_t)desc->dstate * e;
         const size_t sb = (size_t)nb * (size_t)desc->dim * (size_t)desc->dstate * 4;
         const size_t sb_off = (size_t)b0 * (size_t)desc->dim * (size_t)desc->dstate * 4;
         // copies in: the buffer's previous slice must have been scanned and copied out
@@ -2111,17 +2144,26 @@ extern "C" ssm_status ssm_scan_fwd_host(const ssm_scan_desc* desc, int64_t slice
         if (z) h2d(h.o_z, static_cast<const char*>(z) + tok_off, tok);
         h2d(h.o_b, static_cast<const char*>(B) + bc_off, bc);
         h2d(h.o_c, static_cast<const char*>(C) + bc_off, bc);
-        if (initial_state) h2d(h.o_h0, reinterpret_cast<const char*>(initial_state) + sb_off, sb);
+        if (initial_state && j == 0)
+            h2d(h.o_h0, reinterpret_cast<const char*>(initial_state) + sb_off, sb);
         if (err == cudaSuccess) err = cudaEventRecord(ev_in[bi], cs.in);
-        // the scan of the slice on the caller's stream
+        // the scan of the slice on the caller's stream; a later run of steps
+        // starts from the state the previous one (the other buffer) ended in,
+        // which the scans' order on the stream keeps valid
         if (err == cudaSuccess) err = cudaStreamWaitEvent(comp, ev_in[bi], 0);
         if (err != cudaSuccess) break;
+        const float* h_start = nullptr;
+        if (j > 0)
+            h_start = reinterpret_cast<const float*>(ws + (size_t)((i - 1) % kHostBufs) * h.per_buf + h.o_h1);
+        else if (initial_state)
+            h_start = reinterpret_cast<const float*>(buf + h.o_h0);
+        const bool keep_state = last_state || j + 1 < ntime;
         ssm_scan_desc sd = *desc;
         sd.batch = nb;
+        sd.seqlen = nt;
         res = ssm_scan_fwd(&sd, buf + h.o_x, buf + h.o_dl, A, buf + h.o_b, buf + h.o_c, D,
                            z ? buf + h.o_z : nullptr, delta_bias, buf + h.o_out,
-                           last_state ? reinterpret_cast<float*>(buf + h.o_h1) : nullptr,
-                           initial_state ? reinterpret_cast<const float*>(buf + h.o_h0) : nullptr,
+                           keep_state ? reinterpret_cast<float*>(buf + h.o_h1) : nullptr, h_start,
                            h.scan_ws ? buf + h.o_ws : nullptr, h.scan_ws, comp);
         if (res != SSM_OK) break;
         err = cudaEventRecord(ev_done[bi], comp);
@@ -2130,7 +2172,7 @@ extern "C" ssm_status ssm_scan_fwd_host(const ssm_scan_desc* desc, int64_t slice
         if (err == cudaSuccess)
             err = cudaMemcpyAsync(static_cast<char*>(out) + tok_off, buf + h.o_out, tok,
                                   cudaMemcpyDeviceToHost, cs.out);
-        if (err == cudaSuccess && last_state)
+        if (err == cudaSuccess && last_state && j + 1 == ntime)
             err = cudaMemcpyAsync(reinterpret_cast<char*>(last_state) + sb_off, buf + h.o_h1, sb,
                                   cudaMemcpyDeviceToHost, cs.out);
         if (err == cudaSuccess) err = cudaEventRecord(ev_out[bi], cs.out);

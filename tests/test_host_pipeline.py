@@ -1,5 +1,6 @@
 """GPU parity of ssm_scan_fwd_host (the scan of host-resident tensors,
-pipelined over batch slices) against the fp64 oracle, and against the
+pipelined over slices: whole sequences, or runs of steps of one sequence with
+the state carried on the device) against the fp64 oracle, and against the
 device-resident call; the forward's bounds (1e-4 fp32 I/O, 1e-2 bf16 I/O)."""
 import dataclasses
 
@@ -24,10 +25,10 @@ def run_host(inp, cuda, slice_batch):
     return out, last
 
 
-@pytest.mark.parametrize("slice_batch", [0, 1, 2, 5])
+@pytest.mark.parametrize("slice_batch", [0, 1, 2, 5, -64, -100, -299])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_host_pipeline(cuda, slice_batch, io):
-    w = dataclasses.replace(BASE, io=io, seed=17 + slice_batch)
+    w = dataclasses.replace(BASE, io=io, seed=17 + abs(slice_batch))
     inp = synth.make_scan_inputs(w)
     out, last = run_host(inp, cuda, slice_batch)
     ref, ref_last = oracle_full(inp)
@@ -35,21 +36,24 @@ def test_host_pipeline(cuda, slice_batch, io):
     assert rel_err(f64(out), ref) <= tol and rel_err(f64(last), ref_last) <= tol
 
 
-def test_host_pipeline_matches_device_call(cuda):
+@pytest.mark.parametrize("slice_batch", [2, -128])
+def test_host_pipeline_matches_device_call(cuda, slice_batch):
     inp = synth.make_scan_inputs(dataclasses.replace(BASE, with_z=False, init_state=False))
-    out, last = run_host(inp, cuda, 2)
+    out, last = run_host(inp, cuda, slice_batch)
     dev = {k: (None if v is None else v.to(cuda)) for k, v in inp.items()}
     dout, dlast = ops.scan_fwd(**dev)
     torch.cuda.synchronize()
     assert rel_err(f64(out), f64(dout)) <= 1e-2 and rel_err(f64(last), f64(dlast)) <= 1e-4
 
 
-def test_host_pipeline_long_sequences_chunked(cuda):
-    """Slices of one long sequence: each slice takes the chunked (carry) plan."""
+@pytest.mark.parametrize("slice_batch", [1, -1000, -2500])
+def test_host_pipeline_long_sequences_chunked(cuda, slice_batch):
+    """One sequence per slice, or runs of 1000 / 2500 steps of it: each slice
+    takes the chunked (carry) plan, and the runs carry the state across."""
     w = synth.ScanWorkload("host-long", 3, 6000, 48, 16, "bf16", 27, dt_lo=1e-4, dt_hi=1e-2,
                            init_state=True)
     inp = synth.make_scan_inputs(w)
-    out, last = run_host(inp, cuda, 1)
+    out, last = run_host(inp, cuda, slice_batch)
     ref, ref_last = oracle_full(inp)
     assert rel_err(f64(out), ref) <= TOL[torch.bfloat16]
     assert rel_err(f64(last), ref_last) <= TOL[torch.bfloat16]
@@ -57,8 +61,8 @@ def test_host_pipeline_long_sequences_chunked(cuda):
 
 def test_host_pipeline_full_size_sampled(cuda):
     """The Mamba-1.4B layer (4 x 8192 x 4096 x 16, bf16) from pinned host
-    memory, as the benchmark's end-to-end figure runs it (slices of one
-    sequence): sampled channels of every sampled sequence (all 8192 tokens)
+    memory, as the benchmark's end-to-end figure runs it (runs of 2048 steps
+    of one sequence, 16 slices): sampled channels of every sampled sequence (all 8192 tokens)
     and their final states against the oracle."""
     from parity import oracle_sampled, sample_channels
     w = synth.MAMBA_1P4B
