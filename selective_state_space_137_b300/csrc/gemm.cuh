@@ -287,12 +287,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ---------------------------------------------------------------------------
 // Persistent form for output-heavy products with a short K loop (dt_proj:
-// K = dt_rank, C = tokens x dim): each CTA walks tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ... (consecutive CTAs share an N tile, so the B
-// rows and the small A operand are re-read from L2).  Two TMEM accumulators:
-// while the epilogue warps drain tile j, the producer and the MMA thread are
-// already on tile j + 1.
-//   warp 0 lane 0: TMA producer (stage ring continues across tiles)
+// K = dt_rank, C = tokens x dim): a CTA keeps one N tile, whose B rows (all
+// of K) it loads into shared memory once, and walks M tiles, so only the A
+// tiles stream through the ring (half the operand bytes of re-reading both
+// per tile, and a ring twice as deep in tiles).  The grid is a multiple of
+// the N tiles: CTA c takes N tile c % ntn and M tiles c / ntn, c / ntn + g,
+// ... (g CTAs per N tile).  Two TMEM accumulators: while the epilogue warps
+// drain tile j, the producer and the MMA thread are already on tile j + 1.
+//   warp 0 lane 0: TMA producer (B once, then the A ring across tiles)
 //   warp 1 lane 0: MMA issuer; acc_full[a] <- commit, waits acc_empty[a]
 //   warps 2..9   : epilogue; warp w reads TMEM lanes 32 (w % 4) .. and half
 //                  of the tile's columns (two warps per lane quarter: the
@@ -312,14 +314,17 @@ struct GemmPCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 128, "two accumulators of BN columns in 256");
     static constexpr int S = STAGES;
     static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;
-    static constexpr int B_BYTES = BN * kGemmBK * 2;
-    static constexpr int STAGE = (A_BYTES + B_BYTES + 1023) / 1024 * 1024;
-    static constexpr int ROWB = BN * 2 + 16;                       // padded output row (bytes)
-    static constexpr int OFF_OUT = S * STAGE;
-    static constexpr int OFF_BAR = OFF_OUT + kGemmBM * ROWB;
-    // full[S], empty[S], acc_full[2], acc_empty[2]; the TMEM address word; the fail word
-    static constexpr int OFF_TMEM = OFF_BAR + (2 * S + 4) * 8;
-    static constexpr int SMEM = OFF_TMEM + 16 + 1024;
+    static constexpr int B_BYTES = BN * kGemmBK * 2;                // one K slab of the N tile
+    static constexpr int STAGE = (A_BYTES + 1023) / 1024 * 1024;    // the ring holds A slabs
+    static constexpr int B_SLAB = (B_BYTES + 1023) / 1024 * 1024;
+    static constexpr int ROWB = BN * 2 + 16;                        // padded output row (bytes)
+    static constexpr int OFF_B = S * STAGE;                         // nk resident B slabs
+    // after the B slabs (nk of them): the output rows, then full[S], empty[S],
+    // acc_full[2], acc_empty[2], bfull; the TMEM address word; the fail word
+    __host__ __device__ static constexpr int off_out(int nk) { return OFF_B + nk * B_SLAB; }
+    __host__ __device__ static constexpr int off_bar(int nk) { return off_out(nk) + kGemmBM * ROWB; }
+    __host__ __device__ static constexpr int off_tmem(int nk) { return off_bar(nk) + (2 * S + 5) * 8; }
+    __host__ __device__ static constexpr int smem(int nk) { return off_tmem(nk) + 16 + 1024; }
     static constexpr int ACC_COLS = BN <= 32 ? 32 : BN <= 64 ? 64 : 128;
     static constexpr int TMEM_COLS = 2 * ACC_COLS;
 };
@@ -331,17 +336,23 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
     constexpr int S = Cfg::S;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+    const int nk = (p.K + kGemmBK - 1) / kGemmBK;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::off_bar(nk));
     uint64_t* empty = full + S;
     uint64_t* acc_full = empty + S;
     uint64_t* acc_empty = acc_full + 2;
-    uint32_t* tmem_word = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_TMEM);
+    uint64_t* bfull = acc_empty + 2;
+    uint32_t* tmem_word = reinterpret_cast<uint32_t*>(smem + Cfg::off_tmem(nk));
     volatile uint32_t* fail = tmem_word + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mtiles = (int)((p.M + kGemmBM - 1) / kGemmBM);
-    const int ntiles = mtiles * ((p.N + BN - 1) / BN);
-    const int nk = (p.K + kGemmBK - 1) / kGemmBK;
+    const int ntn = (p.N + BN - 1) / BN;
+    // this CTA's N tile and M tiles mt0, mt0 + g, ... (no work past ntn * g)
+    const int g = (int)gridDim.x / ntn;
+    const int nt = (int)blockIdx.x % ntn;
+    const int mt0 = (int)blockIdx.x < ntn * g ? (int)blockIdx.x / ntn : mtiles;
+    const int n0 = nt * BN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -352,6 +363,7 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], 32 * kGemmPEpi);
         }
+        mbar_init(bfull, 1);
         *fail = 0;
         fence_barrier_init();
     }
@@ -366,14 +378,20 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
     const uint32_t tmem = *tmem_word;
 
     int issued = 0;
+    bool b_issued = false;
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer
+        // ---- TMA producer: the N tile's B slabs once, then the A slabs of each tile
         prefetch_tmap(&maps.a);
         prefetch_tmap(&maps.b);
+        if (mt0 < mtiles) {
+            mbar_arrive_expect_tx(bfull, (uint32_t)(nk * Cfg::B_BYTES));
+            for (int i = 0; i < nk; ++i)
+                tma_load_2d(smem + Cfg::OFF_B + i * Cfg::B_SLAB, &maps.b, bfull, i * kGemmBK, n0);
+            b_issued = true;
+        }
         int it = 0;   // slab counter across tiles
-        for (int t = blockIdx.x; t < ntiles && !*fail; t += gridDim.x) {
-            const int64_t m0 = (int64_t)(t % mtiles) * kGemmBM;
-            const int n0 = (t / mtiles) * BN;
+        for (int mt = mt0; mt < mtiles && !*fail; mt += g) {
+            const int64_t m0 = (int64_t)mt * kGemmBM;
             for (int i = 0; i < nk; ++i, ++it) {
                 const int s = it % S;
                 if (it >= S && !mbar_wait_bounded(&empty[s], (uint32_t)(((it / S) - 1) & 1))) {
@@ -381,17 +399,17 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
                     break;
                 }
                 unsigned char* st = smem + s * Cfg::STAGE;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(Cfg::A_BYTES + Cfg::B_BYTES));
+                mbar_arrive_expect_tx(&full[s], (uint32_t)Cfg::A_BYTES);
                 tma_load_2d(st, &maps.a, &full[s], i * kGemmBK, (int)m0);
-                tma_load_2d(st + Cfg::A_BYTES, &maps.b, &full[s], i * kGemmBK, n0);
                 issued = it + 1;
             }
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, BN);
+        if (mt0 < mtiles && !mbar_wait_bounded(bfull, 0u)) *fail = 1;
         int it = 0, j = 0;
-        for (int t = blockIdx.x; t < ntiles && !*fail; t += gridDim.x, ++j) {
+        for (int mt = mt0; mt < mtiles && !*fail; mt += g, ++j) {
             const int a = j & 1;
             const int use = j >> 1;
             if (use >= 1 && !mbar_wait_bounded(&acc_empty[a], (uint32_t)((use - 1) & 1))) {
@@ -408,7 +426,7 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t a0 = smem_addr(smem + s * Cfg::STAGE);
-                const uint32_t b0 = a0 + Cfg::A_BYTES;
+                const uint32_t b0 = smem_addr(smem + Cfg::OFF_B + i * Cfg::B_SLAB);
 #pragma unroll
                 for (int kk = 0; kk < kGemmBK / 16; ++kk)
                     tc_mma(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
@@ -424,11 +442,12 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
         constexpr int HALVES = kGemmPEpi / 4;                 // warps per lane quarter
         constexpr int CW = BN / HALVES;                       // columns of this warp
         const int c0 = ((warp - 2) / 4) * CW;
-        unsigned char* outrow = smem + Cfg::OFF_OUT + (q * 32 + lane) * Cfg::ROWB;
+        unsigned char* const out_tile = smem + Cfg::off_out(nk);
+        unsigned char* outrow = out_tile + (q * 32 + lane) * Cfg::ROWB;
         __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.seg[0].ptr);
         const int64_t ld = p.seg[0].ld;
         int j = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++j) {
+        for (int mt = mt0; mt < mtiles; mt += g, ++j) {
             const int a = j & 1;
             if (!mbar_wait_bounded(&acc_full[a], (uint32_t)((j >> 1) & 1))) {
                 *fail = 1;
@@ -437,7 +456,7 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
             __syncwarp();
             tc_fence_after();
             const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(a * Cfg::ACC_COLS);
-            const int n0e = (t / mtiles) * BN;
+            const int n0e = n0;
 #pragma unroll 1
             for (int c = c0; c < c0 + CW; c += 16) {
                 float vv[16];
@@ -463,8 +482,7 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
             mbar_arrive(&acc_empty[a]);   // TMEM buffer a may be overwritten now
             __syncwarp();
             // the warp's 32 rows leave as whole pieces of CW columns: lane l writes 16 bytes
-            const int64_t m0 = (int64_t)(t % mtiles) * kGemmBM;
-            const int n0 = (t / mtiles) * BN;
+            const int64_t m0 = (int64_t)mt * kGemmBM;
             constexpr int CH16 = CW * 2 / 16;                 // 16-byte chunks per row piece
             constexpr int RPI = 32 / CH16 > 0 ? 32 / CH16 : 1;   // rows per warp instruction
 #pragma unroll 4
@@ -476,7 +494,7 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
                 const int col = n0 + c0 + ch * 8;
                 if (row >= p.M || col >= p.N) continue;
                 const uint4 val = *reinterpret_cast<const uint4*>(
-                    smem + Cfg::OFF_OUT + (q * 32 + r) * Cfg::ROWB + (c0 + ch * 8) * 2);
+                    out_tile + (q * 32 + r) * Cfg::ROWB + (c0 + ch * 8) * 2);
                 __nv_bfloat16* dst = C + row * ld + col;
                 if (col + 8 <= p.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
                     *reinterpret_cast<uint4*>(dst) = val;
@@ -490,6 +508,9 @@ __global__ void __launch_bounds__(kGemmPThreads, 1)
     }
     if (*fail && threadIdx.x == 0) atomicExch(&g_ssm_device_error, kDevErrTimeout);
     if (warp == 0 && lane == 0 && *fail) {
+        // after a timeout, let the loads still in flight land before the CTA's
+        // shared memory is released
+        if (b_issued) mbar_wait_bounded(bfull, 0u, 100000000ull);
         for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i)
             mbar_wait_bounded(&full[i % S], (uint32_t)((i / S) & 1), 100000000ull);
     }

@@ -1253,17 +1253,22 @@ cudaError_t launch_gemm_persistent(const void* A, const void* Bw, int64_t M, int
         !encode_2d_sw128(&maps.b, Bw, K, N, K, BN))
         return cudaErrorInvalidValue;
     auto k = ssm::gemm_bf16_tn_persistent_kernel<BN, STAGES>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    const int nk = (K + ssm::kGemmBK - 1) / ssm::kGemmBK;
+    const int smem = Cfg::smem(nk);   // the N tile's B slabs stay resident
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    int per_sm = (228 * 1024) / (Cfg::SMEM + 1024);
+    int per_sm = (228 * 1024) / (smem + 1024);
     if (per_sm > 512 / Cfg::TMEM_COLS) per_sm = 512 / Cfg::TMEM_COLS;
     if (per_sm > 2048 / ssm::kGemmPThreads) per_sm = 2048 / ssm::kGemmPThreads;
     if (per_sm < 1) per_sm = 1;
-    const int64_t tiles = ((M + ssm::kGemmBM - 1) / ssm::kGemmBM) * ((N + BN - 1) / BN);
-    if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
-    int64_t grid = (int64_t)kPlanSMs * per_sm;
-    if (grid > tiles) grid = tiles;
-    k<<<(unsigned)grid, ssm::kGemmPThreads, Cfg::SMEM, s>>>(maps, p);
+    const int64_t mtiles = (M + ssm::kGemmBM - 1) / ssm::kGemmBM, ntn = (N + BN - 1) / BN;
+    if (mtiles * ntn > 0x7fffffff) return cudaErrorInvalidValue;
+    // g CTAs per N tile, each walking every g-th M tile; the grid is ntn * g
+    int64_t g = (int64_t)kPlanSMs * per_sm / ntn;
+    if (g < 1) g = 1;
+    if (g > mtiles) g = mtiles;
+    k<<<(unsigned)(ntn * g), ssm::kGemmPThreads, smem, s>>>(maps, p);
     return cudaGetLastError();
 }
 
