@@ -346,7 +346,8 @@ def ssm_scan_fwd_host(desc, slice_batch, x, delta, A, B, C, D, z, delta_bias, ou
                       initial_state, workspace, workspace_bytes, stream=None) -> int:
     """The scan over host tensors (x, delta, z, B, C, out, states: host
     memory, pinned for overlap; A, D, delta_bias: device), pipelined over
-    batch slices through a device workspace."""
+    slices through a device workspace (slice_batch > 0: whole sequences,
+    < 0: runs of that many steps of one sequence, 0: picked)."""
     return lib.ssm_scan_fwd_host(ctypes.byref(desc), int(slice_batch), _ptr(x), _ptr(delta), _ptr(A),
                                  _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(out),
                                  _ptr(last_state), _ptr(initial_state), _ptr(workspace),

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from parity import TOL, f64, oracle_full, rel_err
-from selective_state_space_137_b300 import ops, synth
+from selective_state_space_137_b300 import binding, ops, synth
 
 pytestmark = pytest.mark.gpu
 
@@ -74,3 +74,26 @@ def test_host_pipeline_full_size_sampled(cuda):
         idx = torch.tensor(ds)
         assert rel_err(f64(out[b].index_select(-1, idx)), ref) <= tol, (b, ds)
         assert rel_err(f64(last[b].index_select(0, idx)), ref_last) <= tol, (b, ds)
+
+
+@pytest.mark.parametrize("with_state", [False, True])
+def test_host_pipeline_runs_without_last_state(cuda, with_state):
+    """Runs of 100 steps through the C ABI with no last_state requested: the
+    state still passes from run to run on the device (and none is copied
+    out), with and without an initial state."""
+    w = dataclasses.replace(BASE, seed=71, init_state=with_state)
+    inp = synth.make_scan_inputs(w)
+    pin = lambda t: None if t is None else t.pin_memory()
+    desc = binding.make_desc(w.batch, w.seqlen, w.dim, w.dstate, inp["x"].dtype)
+    need = binding.ssm_scan_fwd_host_workspace_size(desc, -100)
+    wsb = torch.empty(need + 256, dtype=torch.uint8, device=cuda)
+    ws = wsb[(256 - wsb.data_ptr() % 256) % 256:]
+    out = torch.empty(inp["x"].shape, dtype=inp["x"].dtype).pin_memory()
+    st = binding.ssm_scan_fwd_host(desc, -100, pin(inp["x"]), pin(inp["delta"]), inp["A"].to(cuda),
+                                   pin(inp["B"]), pin(inp["C"]), inp["D"].to(cuda), pin(inp["z"]),
+                                   inp["delta_bias"].to(cuda), out, None, pin(inp["initial_state"]), ws,
+                                   ws.numel())
+    torch.cuda.synchronize()
+    assert st == binding.SSM_OK
+    ref, _ = oracle_full(inp)
+    assert rel_err(f64(out), ref) <= TOL[inp["x"].dtype]
