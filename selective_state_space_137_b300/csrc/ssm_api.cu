@@ -1958,7 +1958,8 @@ ssm_status ssm_scan_bwd_ex(const ssm_scan_desc* desc, const void* x, const void*
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// The scan over host-resident tensors, pipelined over batch slices.
+// The scan over host-resident tensors, pipelined over slices (whole sequences
+// or runs of steps of one sequence).
 namespace {
 
 constexpr int kHostBufs = 2;   // slices in flight per stage

@@ -371,8 +371,10 @@ def scan_fwd_host(x, delta, A, B, C, D=None, z=None, delta_bias=None, initial_st
                   delta_softplus=True, slice_batch=0, out=None, last_state=None, workspace=None,
                   stream=None):
     """The scan of host-resident tensors (x, delta, z, B, C, initial_state on
-    the CPU, ideally pinned) with A, D, delta_bias on the GPU: batch slices are
-    copied in, scanned and copied back in an overlapped pipeline.  Returns
+    the CPU, ideally pinned) with A, D, delta_bias on the GPU: slices (whole
+    sequences for ``slice_batch`` > 0, runs of -``slice_batch`` steps of one
+    sequence for < 0, picked for 0) are copied in, scanned and copied back in
+    an overlapped pipeline.  Returns
     ``(out, last_state)`` as CPU tensors (pinned) once the stream reaches the
     end of the call; synchronise the stream before reading them."""
     if x.is_cuda or not A.is_cuda:
